@@ -1,0 +1,370 @@
+"""Benchmark of the CVR scoring path on GB300: candidates scored per second, request latency, roofline.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config prod] [--impl reference]
+
+A step is one cvr_score call over one full batch of the workload (all stages of the forward pass:
+embedding bags, sequence encoders, tokeniser, Query Decoding, Token Mixer, PLE, heads), inputs
+resident in HBM, L2 flushed (256 MB write) before every step and each step timed alone with CUDA
+events on the scorer's stream. ``e2e`` repeats the measurement through cvr_score_host with pinned
+host buffers (input copies and the output read inside the timed region). ``roofline`` is the
+dominant kernel's algorithmic FLOPs per launch over its event-timed duration. ``cpu_baseline`` times
+the CPU oracle on a bounded sample of the same workload. ``--impl reference`` times that oracle
+alone (the method has no other runnable reference implementation).
+
+Under torchrun every rank scores its own replica of the batch (requests are independent: weak
+scaling, no collective on the data path); rank 0 prints the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "candidates scored/sec and p50 request latency on 1 GB300; % of roofline"
+UNIT = "candidates/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ---------------------------------------------------------------------------------------------
+# algorithmic work (user side once per request, K/V and mean-pool once per request)
+def algorithmic_work(wl, nnz: int):
+    D, H = 128, 256
+    R, B, SL, NL = wl.n_req, wl.n_cand, wl.sum_len, wl.n_layers
+    swiglu_row = 2 * D * 2 * H + 2 * H * D                       # 196,608 FLOP per row
+    flops = {
+        "seq_mlp": R * SL * swiglu_row,
+        "request_side": R * 2 * 256 * 1664 + NL * R * 3 * 2 * D * D,
+        "tokenizer": B * 2 * 256 * 1664,
+        "query": NL * B * 2 * 1664 * 384,
+        "attention": NL * B * 4 * D * SL,                        # q.k and p.v: 2 * 2 * 128 per position
+        "token_mixer": NL * B * 16 * swiglu_row,
+        "ple": B * 2 * 2048 * (768 + 6),
+        "heads": B * 2 * (2 * 256 * 128 + 128),
+    }
+    bf16_weights = (1664 * 512 + 3 * (512 * 128 + 128 * 256) + NL * (3 * 128 * 1792 + 512 * 128 + 128 * 256)
+                    + 774 * 2048 + 2 * 128 * 256) * 2
+    gathered = nnz * 128 + R * SL * 4 * 128                      # fp32 rows of 32
+    ids = nnz * 8 + R * SL * 4 * 8 + (R * 8 + B * 8 + 1) * 8 + B * 4
+    total_bytes = gathered + ids + bf16_weights + B * 8
+    sparse_bytes = gathered + ids + (R * 256 + B * 256 + R * SL * 128) * 2   # + bf16 outputs written
+    return flops, total_bytes, sparse_bytes
+
+
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.proc or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------------------------
+def oracle_baseline(cfg_name: str, budget_s: float = 15.0):
+    """The CPU oracle, as it stands, on a bounded sample of the workload: candidates of one request."""
+    import oracle
+    import synth
+    threads = oracle.threads_used(0)
+    n = 16
+    t = 0.0
+    while True:
+        wl = synth.make_workload(cfg_name, n_req=1, n_cand=n)
+        w = synth.make_weights(wl.n_layers, wl.seed)
+        t0 = time.perf_counter()
+        oracle.score(wl, w)
+        t = time.perf_counter() - t0
+        if t * 2 > budget_s or n >= 4096:
+            break
+        n = min(4096, n * max(2, int(budget_s / max(t, 1e-3) / 2)))
+    return {"value": n / t, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{cfg_name} shapes, 1 request x {n} candidates (fp64 loop-nest oracle, OpenMP over "
+                      f"candidates), {t:.1f} s wall"}
+
+
+def run_reference(args):
+    import oracle
+    import synth
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    threads = oracle.threads_used(0)
+    # per-step sample sized so that warmup + steps take ~2 minutes
+    wl = synth.make_workload(args.config, n_req=1, n_cand=8)
+    w = synth.make_weights(wl.n_layers, wl.seed)
+    t0 = time.perf_counter()
+    oracle.score(wl, w)
+    per = (time.perf_counter() - t0) / 8
+    total_steps = max(1, args.steps + args.warmup)
+    n = int(max(8, min(512, 120.0 / total_steps / max(per, 1e-6))))
+    wl = synth.make_workload(args.config, n_req=1, n_cand=n)
+    w = synth.make_weights(wl.n_layers, wl.seed)
+    for _ in range(args.warmup):
+        oracle.score(wl, w)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.score(wl, w)
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = n * args.steps / tot
+    p50 = statistics.median(times) * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.config} shapes, 1 request x {n} candidates per step (CPU oracle)"},
+            "p50_ms": p50,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"1 request x {n} candidates of the {args.config} workload per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="prod", choices=["tiny", "prod", "longseq", "embheavy", "deep"])
+    ap.add_argument("--n-cand", type=int, default=None, help="candidates per request (deep sweep)")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import cvr_ranking_model_gb300 as cvr
+    import synth
+    from synth.harness import DeviceWorkload, make_scorer
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    stream = torch.cuda.Stream(device=dev)
+
+    wl = synth.make_workload(args.config, n_cand=args.n_cand)
+    w = synth.make_weights(wl.n_layers, wl.seed)
+    with torch.cuda.stream(stream):
+        dw = DeviceWorkload(wl, device=dev)
+    torch.cuda.synchronize(dev)
+    sc = make_scorer(dw, w, stream=stream.cuda_stream)
+    sc.set_option(cvr.OPT_CUDA_GRAPH, 1)
+    sc.set_option(cvr.OPT_PROFILE, 1)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    r, b, o, s, out = dw.ptrs()
+    B = wl.n_cand
+
+    def step():
+        sc.score(wl.n_req, B, r, b, o, s, out)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+    torch.cuda.synchronize(dev)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stage_sum = {}
+    launches = 0
+    host_ms = []
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.zero_()
+                starts[i].record(stream)
+                t0 = time.perf_counter()
+                step()
+                host_ms.append((time.perf_counter() - t0) * 1e3)
+                ends[i].record(stream)
+                launches += sc.last_launch_count()
+                for name, ms in sc.stage_list():
+                    stage_sum.setdefault(name, []).append(ms)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    step_ms = [starts[i].elapsed_time(ends[i]) for i in range(args.steps)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * B * args.steps / (total_ms / 1e3)
+
+    # per-kernel times (events recorded between the kernels, on the scorer's stream, every timed step)
+    per_kernel = {}
+    for name, lst in stage_sum.items():
+        # a name repeats once per layer; stage_list already returns every launch -> group per step
+        per_kernel[name] = sum(lst) / args.steps
+    nnz = int(wl.bag_offsets[-1])
+    flops, total_bytes, sparse_bytes = algorithmic_work(wl, nnz)
+    peaks, peak_src = load_peaks()
+    peak_tf = float(peaks["bf16_tflops"])
+    peak_bw = float(peaks["hbm_gbs"])
+    gemm_like = {k: v for k, v in per_kernel.items() if k in flops and k != "attention"}
+    dom = max(gemm_like, key=lambda k: gemm_like[k]) if gemm_like else None
+    launches_per_kernel = {"query": wl.n_layers, "attention": wl.n_layers, "token_mixer": wl.n_layers}
+    roofline = None
+    if dom:
+        n_l = launches_per_kernel.get(dom, 1)
+        avg_launch_ms = per_kernel[dom] / n_l
+        ach = flops[dom] / n_l / (avg_launch_ms / 1e3) / 1e12
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
+                    "frac": ach / peak_tf, "traffic": None,
+                    "peak_source": f"{peak_src} bf16 dense burst (cuBLAS)",
+                    "flop_per_launch": flops[dom] / n_l, "launch_ms": avg_launch_ms}
+        tr = os.path.join(ROOT, "profiles", "traffic.json")
+        if os.path.exists(tr):
+            with open(tr) as f:
+                td = json.load(f)
+            ent = td.get(f"{args.config}:{dom}")
+            if ent and ent.get("valid", True):
+                roofline["traffic"] = ent["bytes_per_launch"]
+    sparse = None
+    if "sparse" in per_kernel:
+        gbs = sparse_bytes / (per_kernel["sparse"] / 1e3) / 1e9
+        sparse = {"kernel": "sparse", "bound": "hbm", "achieved": gbs, "peak": peak_bw, "unit": "GB/s",
+                  "frac": gbs / peak_bw, "bytes_per_launch": sparse_bytes}
+    p50 = statistics.median(step_ms)
+    p99 = float(np.percentile(step_ms, 99))
+    total_flop = sum(flops.values())
+    t_roof_us = max(total_flop / (peak_tf * 1e12), total_bytes / (peak_bw * 1e9)) * 1e6
+    path = {"t_roof_us": t_roof_us, "p50_us": p50 * 1e3, "frac": t_roof_us / (p50 * 1e3),
+            "gflop_per_batch": total_flop / 1e9, "mbytes_per_batch": total_bytes / 1e6,
+            "bound": "tensor" if total_flop / (peak_tf * 1e12) > total_bytes / (peak_bw * 1e9) else "hbm"}
+
+    # ---- end to end through the host-buffer entry point (pinned buffers, copies inside the timed region)
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory().numpy()
+        h_req, h_ids, h_off, h_seq = pin(wl.req_ids), pin(wl.bag_ids), pin(wl.bag_offsets), pin(wl.seq_ids)
+        h_out = torch.empty((B, 2), dtype=torch.float32).pin_memory().numpy()
+        sc.set_option(cvr.OPT_PROFILE, 0)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                sc.score_host(wl.n_req, B, h_req, h_ids, h_off, h_seq, h_out)
+            e_ms = []
+            for i in range(args.steps):
+                flush.zero_()
+                ev0 = torch.cuda.Event(enable_timing=True)
+                ev1 = torch.cuda.Event(enable_timing=True)
+                ev0.record(stream)
+                sc.score_host(wl.n_req, B, h_req, h_ids, h_off, h_seq, h_out)
+                ev1.record(stream)
+                ev1.synchronize()
+                e_ms.append(ev0.elapsed_time(ev1))
+        h2d = h_req.nbytes + h_ids.nbytes + h_off.nbytes + h_seq.nbytes
+        e_tot = sum(e_ms)
+        if world > 1:
+            t = torch.tensor([e_tot], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_tot = float(t.item())
+        e2e = {"value": world * B * args.steps / (e_tot / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(h_out.nbytes), "p50_ms": statistics.median(e_ms),
+               "api": "cvr_score_host (pinned host buffers)"}
+
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = oracle_baseline(args.config)
+        Lstr = "/".join(str(x) for x in wl.seq_len)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{args.config}: R={wl.n_req} requests x C={B // wl.n_req} candidates, "
+                                   f"L={Lstr}, {wl.n_layers} interaction layer(s), tables {wl.user_rows}/"
+                                   f"{wl.item_rows}/{wl.seq_rows} rows x 32 fp32, bags 1-8, Zipf({wl.zipf_s})",
+                       "global_batch": B * world, "parallelism": f"replicas x{world}",
+                       "l2": "flushed (256 MB write) before every timed step"},
+            "p50_ms": p50, "p99_ms": p99, "host_p50_ms": statistics.median(host_ms),
+            "roofline": roofline, "sparse_roofline": sparse, "path_roofline": path,
+            "stage_ms": {k: round(v, 5) for k, v in per_kernel.items()},
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks.summary(),
+            "gpu_launches": launches,
+        }
+        print(json.dumps(line))
+    sc.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

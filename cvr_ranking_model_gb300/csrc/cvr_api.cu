@@ -1,0 +1,780 @@
+// Host side of the CVR scoring library: the C ABI of include/cvr.h.
+//
+// cvr_create packs the dense weights into the layouts the kernels consume (bf16, W1/W3 rows interleaved
+// per 128 hidden units, the three query FFNs stacked, the PLE gates appended to the expert rows) and
+// builds their TMA tensor maps. cvr_score validates sizes on the host, grows the workspace for the
+// batch if needed, and runs the forward pass -- eagerly or by replaying a CUDA graph captured for the
+// batch's (n_req, n_cand) bucket (iQIYI ad-CVR article 3.4.4) -- then reads the device error word.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "../../include/cvr.h"
+#include "cvr_internal.cuh"
+
+using namespace cvr;
+typedef __nv_bfloat16 bf16;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+uint16_t f32_to_bf16_bits(float x) {
+  uint32_t u;
+  std::memcpy(&u, &x, 4);
+  if ((u & 0x7F800000u) == 0x7F800000u) return (uint16_t)((u >> 16) | ((u & 0xFFFF) ? 0x40 : 0));
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+struct GraphEntry {
+  cudaGraphExec_t exec = nullptr;
+  std::vector<const void*> key;
+  int launches = 0;
+};
+
+const char* kStageNames[] = {"sparse", "seq_mlp", "seq_colsum", "request_side", "tokenizer", "query", "attention",
+                             "token_mixer", "ple", "heads"};
+
+}  // namespace
+
+struct cvr_handle {
+  int device = 0;
+  cudaStream_t stream = nullptr;
+  cudaStream_t cap_stream = nullptr;
+  cvr_config cfg{};
+  int n_layers = 1, SL = 0;
+  int L[kG] = {0, 0, 0};
+  std::string last_error;
+  // packed weights
+  void* wblob = nullptr;
+  bf16 *tokI = nullptr, *tokU = nullptr, *seqW13 = nullptr, *seqW2 = nullptr, *qX = nullptr, *qm = nullptr;
+  bf16 *tmW13 = nullptr, *tmW2 = nullptr, *pleW = nullptr, *headW1 = nullptr;
+  float *tok_b = nullptr, *seq_b13 = nullptr, *seq_b2 = nullptr, *q_b = nullptr, *tm_b13 = nullptr, *tm_b2 = nullptr;
+  float *tm_gain = nullptr, *ple_b = nullptr, *head_b1 = nullptr, *head_w2 = nullptr, *head_b2 = nullptr;
+  const float* tables[kFu + kFi + 1] = {};
+  int64_t rows[kFu + kFi + 1] = {};
+  // workspace
+  int R_cap = 0, B_cap = 0, max_chunks = 0;
+  void* ws = nullptr;
+  bf16 *U = nullptr, *I = nullptr, *Xs = nullptr, *H = nullptr, *Z = nullptr, *Y = nullptr, *Q = nullptr, *Ex = nullptr;
+  float *colsum = nullptr, *xu = nullptr, *qb = nullptr, *gates = nullptr;
+  int* err = nullptr;
+  int* err_host = nullptr;
+  // host-input staging
+  void* stage = nullptr;
+  size_t stage_bytes = 0;
+  // tensor maps
+  CUtensorMap tm_seqW13, tm_seqW2, tm_tokI, tm_qW[kMaxLayers], tm_tmW13, tm_tmW2, tm_pleW, tm_headW1;
+  CUtensorMap tm_Xs, tm_I, tm_x_Z, tm_x_Y, tm_5_Z, tm_5_Y, tm_full_Z, tm_full_Y;
+  // graphs, profiling
+  bool use_graph = true, profile = false;
+  std::map<std::pair<int, int>, GraphEntry> graphs;
+  std::vector<cudaEvent_t> events;
+  std::vector<const char*> event_names;
+  int n_events_last = 0;
+  int last_launches = 0;
+  int last_R = 0, last_B = 0;
+  bf16 *last_zin = nullptr, *last_zout = nullptr;
+};
+
+namespace {
+
+cvr_status fail(cvr_handle* h, cvr_status s, const std::string& msg) {
+  if (h) h->last_error = msg;
+  return s;
+}
+cvr_status cuda_fail(cvr_handle* h, cudaError_t e, const char* what) {
+  return fail(h, CVR_E_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_elems,
+               uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_elems * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Token-mix view of Z[nb][16][128] (bf16): dims (inner -> outer) e(8), j%8(8), t(16), j/8(2), b(nb).
+// One box {8,8,16,2,8} lands in shared memory as [b][j/8][t][j%8][e]: for mixed row (b, j) and K index
+// 8t+e, 8x16-byte core matrices of 8 consecutive mixed rows, 128 B apart along K and 2048 B apart
+// between 8-row groups -- the no-swizzle K-major operand layout of tcgen05.
+bool encode_mix5d(CUtensorMap* m, const void* base, uint64_t nb) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[5] = {8, 8, (cuuint64_t)kT, 2, nb};
+  cuuint64_t strides[4] = {16, (cuuint64_t)kD * 2, 128, (cuuint64_t)kYD * 2};
+  cuuint32_t box[5] = {8, 8, (cuuint32_t)kT, 2, 8};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cvr_status check_config(const cvr_config* c, std::string* why) {
+  auto bad = [&](const char* m) {
+    *why = m;
+    return CVR_E_ARG;
+  };
+  if (c->n_user_fields != kFu || c->n_item_fields != kFi || c->emb_dim != kE || c->n_tokens != kN ||
+      c->token_dim != kD || c->n_groups != kG || c->seq_cols != kCols || c->ffn_hidden != kHid ||
+      c->heads != kHeads || c->n_experts != kNE || c->expert_dim != kDE || c->n_tasks != kNT ||
+      c->head_hidden != kHH)
+    return bad("unsupported model dimensions (the kernels are built for 8+8 fields of 32, 13 tokens of 128, "
+               "3 groups x 4 columns, SwiGLU 256, 4 heads, 3 experts of 256, 2 tasks, head 128)");
+  if (c->n_layers < 1 || c->n_layers > CVR_MAX_LAYERS) return bad("n_layers must be in [1, 4]");
+  for (int g = 0; g < kG; ++g)
+    if (c->seq_len[g] < 1 || c->seq_len[g] > (1 << 20)) return bad("seq_len must be in [1, 2^20]");
+  if (!(c->tau > 0.f) || !(c->clamp > 0.f) || !(c->rms_eps >= 0.f) || !std::isfinite(c->tau) ||
+      !std::isfinite(c->clamp) || !std::isfinite(c->rms_eps))
+    return bad("tau and clamp must be positive and finite, rms_eps finite and >= 0");
+  for (int f = 0; f < kFu; ++f)
+    if (c->user_rows[f] < 1) return bad("user_rows must be >= 1");
+  for (int f = 0; f < kFi; ++f)
+    if (c->item_rows[f] < 1) return bad("item_rows must be >= 1");
+  if (c->seq_rows < 1) return bad("seq_rows must be >= 1");
+  return CVR_OK;
+}
+
+// ---- weight packing ----
+struct Packer {
+  std::vector<uint16_t> bf;   // bf16 blob
+  std::vector<float> f32;     // fp32 blob
+  size_t add_bf(size_t n) {
+    size_t off = bf.size();
+    bf.resize(off + ((n + 63) / 64) * 64, 0);  // 128-byte aligned pieces
+    return off;
+  }
+  size_t add_f(size_t n) {
+    size_t off = f32.size();
+    f32.resize(off + ((n + 31) / 32) * 32, 0.f);
+    return off;
+  }
+};
+
+// rows [h*256, h*256+128) = W1 rows [h*128, h*128+128), rows [h*256+128, h*256+256) = W3 rows (h = 0, 1)
+void pack_w13(uint16_t* dst, const float* w1, const float* w3, int din) {
+  for (int h = 0; h < 2; ++h)
+    for (int i = 0; i < 128; ++i)
+      for (int k = 0; k < din; ++k) {
+        dst[(size_t)(h * 256 + i) * din + k] = f32_to_bf16_bits(w1[(size_t)(h * 128 + i) * din + k]);
+        dst[(size_t)(h * 256 + 128 + i) * din + k] = f32_to_bf16_bits(w3[(size_t)(h * 128 + i) * din + k]);
+      }
+}
+void pack_b13(float* dst, const float* b1, const float* b3) {
+  for (int h = 0; h < 2; ++h)
+    for (int i = 0; i < 128; ++i) {
+      dst[h * 256 + i] = b1[h * 128 + i];
+      dst[h * 256 + 128 + i] = b3[h * 128 + i];
+    }
+}
+
+cvr_status free_workspace(cvr_handle* h) {
+  for (auto& kv : h->graphs)
+    if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+  h->graphs.clear();
+  if (h->ws) cudaFree(h->ws);
+  h->ws = nullptr;
+  h->R_cap = h->B_cap = 0;
+  return CVR_OK;
+}
+
+cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
+  if (R <= h->R_cap && B <= h->B_cap) return CVR_OK;
+  free_workspace(h);
+  const int R_cap = std::max(R, h->R_cap);
+  const int B_cap = (int)(((int64_t)std::max(B, h->B_cap) + 127) / 128 * 128);
+  int max_chunks = 0;
+  for (int g = 0; g < kG; ++g) max_chunks = std::max(max_chunks, (h->L[g] + 63) / 64);
+  const int64_t seq_rows = (int64_t)R_cap * h->SL;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += (bytes + 1023) / 1024 * 1024;
+    return o;
+  };
+  const size_t oU = take((size_t)R_cap * kUD * 2), oI = take((size_t)B_cap * kID * 2);
+  const size_t oXs = take((size_t)seq_rows * kD * 2), oH = take((size_t)seq_rows * kD * 2);
+  const size_t oCs = take((size_t)R_cap * kG * max_chunks * kD * 4), oXu = take((size_t)R_cap * kXD * 4);
+  const size_t oQb = take((size_t)h->n_layers * R_cap * kG * kD * 4);
+  const size_t oZ = take((size_t)B_cap * kYD * 2), oY = take((size_t)B_cap * kYD * 2);
+  const size_t oQ = take((size_t)B_cap * kG * kD * 2), oEx = take((size_t)B_cap * kPleN * 2);
+  const size_t oG = take((size_t)B_cap * 8 * 4), oErr = take(64);
+  cudaError_t e = cudaMalloc(&h->ws, off);
+  if (e != cudaSuccess) {
+    h->ws = nullptr;
+    cudaGetLastError();
+    return fail(h, CVR_E_OOM, "workspace allocation failed: " + std::string(cudaGetErrorString(e)));
+  }
+  uint8_t* b = static_cast<uint8_t*>(h->ws);
+  h->U = (bf16*)(b + oU);
+  h->I = (bf16*)(b + oI);
+  h->Xs = (bf16*)(b + oXs);
+  h->H = (bf16*)(b + oH);
+  h->colsum = (float*)(b + oCs);
+  h->xu = (float*)(b + oXu);
+  h->qb = (float*)(b + oQb);
+  h->Z = (bf16*)(b + oZ);
+  h->Y = (bf16*)(b + oY);
+  h->Q = (bf16*)(b + oQ);
+  h->Ex = (bf16*)(b + oEx);
+  h->gates = (float*)(b + oG);
+  h->err = (int*)(b + oErr);
+  h->R_cap = R_cap;
+  h->B_cap = B_cap;
+  h->max_chunks = max_chunks;
+  bool ok = encode_2d(&h->tm_Xs, h->Xs, kD, (uint64_t)seq_rows, kD, 64, 128) &&
+            encode_2d(&h->tm_I, h->I, kID, B_cap, kID, 64, 128) &&
+            encode_2d(&h->tm_x_Z, h->Z, kXD, B_cap, kYD, 64, 128) &&
+            encode_2d(&h->tm_x_Y, h->Y, kXD, B_cap, kYD, 64, 128) && encode_mix5d(&h->tm_5_Z, h->Z, B_cap) &&
+            encode_mix5d(&h->tm_5_Y, h->Y, B_cap) && encode_2d(&h->tm_full_Z, h->Z, kYD, B_cap, kYD, 64, 128) &&
+            encode_2d(&h->tm_full_Y, h->Y, kYD, B_cap, kYD, 64, 128);
+  if (!ok) {
+    free_workspace(h);
+    return fail(h, CVR_E_CUDA, "cuTensorMapEncodeTiled failed for a workspace tensor");
+  }
+  return CVR_OK;
+}
+
+FwdArgs make_args(cvr_handle* h, int R, int B, const int32_t* req_ids, const int64_t* bag_ids,
+                  const int64_t* bag_offsets, const int64_t* seq_ids, float* out, float* dbg_pooled,
+                  int64_t* dbg_rows) {
+  FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.req_ids = req_ids;
+  a.bag_ids = bag_ids;
+  a.bag_offsets = bag_offsets;
+  a.seq_ids = seq_ids;
+  a.out = out;
+  a.dbg_pooled = dbg_pooled;
+  a.dbg_rows = dbg_rows;
+  for (int t = 0; t < kFu + kFi + 1; ++t) {
+    a.tables[t] = h->tables[t];
+    a.table_rows[t] = h->rows[t];
+  }
+  a.R = R;
+  a.B = B;
+  a.SL = h->SL;
+  int64_t acc = 0;
+  for (int g = 0; g < kG; ++g) {
+    a.L[g] = h->L[g];
+    a.goff[g] = acc;
+    acc += (int64_t)R * h->L[g];
+  }
+  a.n_layers = h->n_layers;
+  a.clamp = h->cfg.clamp;
+  a.tau = h->cfg.tau;
+  a.eps = h->cfg.rms_eps;
+  a.U = h->U;
+  a.I = h->I;
+  a.Xs = h->Xs;
+  a.H = h->H;
+  a.colsum = h->colsum;
+  a.max_chunks = h->max_chunks;
+  a.xu = h->xu;
+  a.qb = h->qb;
+  a.Z = h->Z;
+  a.Y = h->Y;
+  a.Q = h->Q;
+  a.Ex = h->Ex;
+  a.gates = h->gates;
+  a.err = h->err;
+  a.tokU = h->tokU;
+  a.tok_b = h->tok_b;
+  a.seq_b13 = h->seq_b13;
+  a.seq_b2 = h->seq_b2;
+  a.qm = h->qm;
+  a.q_b = h->q_b;
+  a.tm_b13 = h->tm_b13;
+  a.tm_b2 = h->tm_b2;
+  a.tm_gain = h->tm_gain;
+  a.ple_b = h->ple_b;
+  a.head_b1 = h->head_b1;
+  a.head_w2 = h->head_w2;
+  a.head_b2 = h->head_b2;
+  return a;
+}
+
+// Enqueues the whole forward pass on `s`. With `events`, records one after each kernel.
+cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, bool events, bool external_events,
+                            int* launches) {
+  int n = 0, ev = 0;
+  cudaError_t e = cudaSuccess;
+  auto mark = [&](const char* name) {
+    if (!events || e != cudaSuccess) return;
+    if ((size_t)ev + 1 >= h->events.size()) return;
+    h->event_names[ev] = name;
+    e = external_events ? cudaEventRecordWithFlags(h->events[ev + 1], s, cudaEventRecordExternal)
+                        : cudaEventRecord(h->events[ev + 1], s);
+    ++ev;
+  };
+  auto run = [&](cudaError_t r, const char* name) {
+    if (e != cudaSuccess) return;
+    e = r;
+    ++n;
+    mark(name);
+  };
+  if (events)
+    e = external_events ? cudaEventRecordWithFlags(h->events[0], s, cudaEventRecordExternal)
+                        : cudaEventRecord(h->events[0], s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->err, 0, sizeof(int), s);
+  run(launch_sparse(a, s), kStageNames[0]);
+  int seq_tiles = 0;
+  for (int g = 0; g < kG; ++g) seq_tiles += (int)(((int64_t)a.R * a.L[g] + 127) / 128);
+  run(launch_seq_mlp(a, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, s), kStageNames[1]);
+  run(launch_seq_colsum(a, s), kStageNames[2]);
+  run(launch_request_side(a, s), kStageNames[3]);
+  run(launch_tokenizer(a, h->tm_I, h->tm_tokI, s), kStageNames[4]);
+  bf16* zin = h->Z;
+  bf16* zout = h->Y;
+  for (int l = 0; l < a.n_layers; ++l) {
+    if (l > 0) std::swap(zin, zout);  // layer l reads the previous output (its first 13 tokens) in place
+    const bool in_is_Z = zin == h->Z;
+    run(launch_query(a, l, in_is_Z ? h->tm_x_Z : h->tm_x_Y, h->tm_qW[l], s), kStageNames[5]);
+    run(launch_attention(a, zin, s), kStageNames[6]);
+    run(launch_tm_mlp(a, l, zin, zout, in_is_Z ? h->tm_5_Z : h->tm_5_Y, h->tm_tmW13, h->tm_tmW2, s), kStageNames[7]);
+  }
+  run(launch_ple(a, zout == h->Z ? h->tm_full_Z : h->tm_full_Y, h->tm_pleW, s), kStageNames[8]);
+  run(launch_heads(a, h->tm_headW1, s), kStageNames[9]);
+  h->last_zin = zin;
+  h->last_zout = zout;
+  if (launches) *launches = n;
+  h->n_events_last = events ? ev : 0;
+  return e;
+}
+
+cvr_status run_forward(cvr_handle* h, int32_t R, int32_t B, const int32_t* req_ids, const int64_t* bag_ids,
+                       const int64_t* bag_offsets, const int64_t* seq_ids, float* out, float* dbg_pooled,
+                       int64_t* dbg_rows) {
+  if (!h) return CVR_E_ARG;
+  if (!req_ids || !bag_ids || !bag_offsets || !seq_ids || !out) return fail(h, CVR_E_ARG, "null input or output pointer");
+  if (R < 1 || B < 1 || R > 65535 || B > (1 << 20)) return fail(h, CVR_E_SHAPE, "need 1 <= n_req <= 65535, 1 <= n_cand <= 2^20");
+  cudaError_t ce = cudaSetDevice(h->device);
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaSetDevice");
+  cvr_status st = ensure_workspace(h, R, B);
+  if (st != CVR_OK) return st;
+  const FwdArgs a = make_args(h, R, B, req_ids, bag_ids, bag_offsets, seq_ids, out, dbg_pooled, dbg_rows);
+  cudaStream_t s = h->stream;
+  if (h->use_graph) {
+    std::vector<const void*> key = {req_ids, bag_ids, bag_offsets, seq_ids, out, dbg_pooled, dbg_rows,
+                                    reinterpret_cast<const void*>((intptr_t)h->profile)};
+    GraphEntry& ge = h->graphs[std::make_pair(R, B)];
+    if (!ge.exec || ge.key != key) {
+      cudaGraph_t graph = nullptr;
+      ce = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal);
+      if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaStreamBeginCapture");
+      int launches = 0;
+      cudaError_t le = enqueue_forward(h, a, h->cap_stream, h->profile, true, &launches);
+      ce = cudaStreamEndCapture(h->cap_stream, &graph);
+      if (le != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        return cuda_fail(h, le, "kernel launch during capture");
+      }
+      if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaStreamEndCapture");
+      bool updated = false;
+      if (ge.exec) {
+        cudaGraphExecUpdateResultInfo info;
+        if (cudaGraphExecUpdate(ge.exec, graph, &info) == cudaSuccess) {
+          updated = true;
+        } else {
+          cudaGetLastError();
+          cudaGraphExecDestroy(ge.exec);
+          ge.exec = nullptr;
+        }
+      }
+      if (!updated) {
+        ce = cudaGraphInstantiate(&ge.exec, graph, 0);
+        if (ce != cudaSuccess) {
+          cudaGraphDestroy(graph);
+          ge.exec = nullptr;
+          return cuda_fail(h, ce, "cudaGraphInstantiate");
+        }
+      }
+      cudaGraphDestroy(graph);
+      ge.key = key;
+      ge.launches = launches;
+    }
+    ce = cudaGraphLaunch(ge.exec, s);
+    if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaGraphLaunch");
+    h->last_launches = ge.launches;
+    // the zin/zout bookkeeping of the captured sequence
+    h->last_zin = (a.n_layers % 2 == 1) ? h->Z : h->Y;
+    h->last_zout = (a.n_layers % 2 == 1) ? h->Y : h->Z;
+  } else {
+    int launches = 0;
+    ce = enqueue_forward(h, a, s, h->profile, false, &launches);
+    if (ce != cudaSuccess) return cuda_fail(h, ce, "kernel launch");
+    h->last_launches = launches;
+  }
+  h->last_R = R;
+  h->last_B = B;
+  ce = cudaMemcpyAsync(h->err_host, h->err, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaMemcpyAsync(error word)");
+  ce = cudaStreamSynchronize(s);
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "forward pass");
+  const int ew = *h->err_host;
+  if (ew & kErrTimeout) return fail(h, CVR_E_TIMEOUT, "a bounded device-side wait gave up");
+  if (ew & (kErrOffsets | kErrReqIds))
+    return fail(h, CVR_E_INPUT, (ew & kErrOffsets) ? "bag offsets decrease" : "request ids out of range or decreasing");
+  if (ew & kErrIdRange) return fail(h, CVR_E_ID_RANGE, "an id is outside its table (row 0 was read)");
+  h->last_error.clear();
+  return CVR_OK;
+}
+
+}  // namespace
+
+// =============================================================================================
+extern "C" {
+
+const char* cvr_status_string(cvr_status s) {
+  switch (s) {
+    case CVR_OK: return "ok";
+    case CVR_E_ARG: return "invalid argument";
+    case CVR_E_SHAPE: return "size out of range";
+    case CVR_E_ID_RANGE: return "id out of table range";
+    case CVR_E_OOM: return "out of memory";
+    case CVR_E_CUDA: return "CUDA error";
+    case CVR_E_INPUT: return "invalid offsets or request ids";
+    case CVR_E_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* cvr_last_error(const cvr_handle* h) { return h ? h->last_error.c_str() : "null handle"; }
+
+int32_t cvr_last_launch_count(const cvr_handle* h) { return h ? h->last_launches : 0; }
+
+cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_stream, cvr_handle** out) {
+  if (!out) return CVR_E_ARG;
+  *out = nullptr;
+  if (!w || !cfg) return CVR_E_ARG;
+  std::string why;
+  if (check_config(cfg, &why) != CVR_OK) {
+    fprintf(stderr, "cvr_create: %s\n", why.c_str());
+    return CVR_E_ARG;
+  }
+  const int NL = cfg->n_layers;
+  // every pointer the configuration uses must be set
+  bool ok = w->seq_table && w->tok_w && w->tok_b;
+  for (int f = 0; f < 8; ++f) ok = ok && w->user_tables[f] && w->item_tables[f];
+  for (int g = 0; g < 3; ++g)
+    ok = ok && w->seq_w1[g] && w->seq_b1[g] && w->seq_w3[g] && w->seq_b3[g] && w->seq_w2[g] && w->seq_b2[g];
+  for (int l = 0; l < NL; ++l) {
+    for (int g = 0; g < 3; ++g) ok = ok && w->q_w[l][g] && w->q_b[l][g];
+    ok = ok && w->tm_w1[l] && w->tm_b1[l] && w->tm_w3[l] && w->tm_b3[l] && w->tm_w2[l] && w->tm_b2[l] && w->tm_gain[l];
+  }
+  for (int k = 0; k < 3; ++k) ok = ok && w->ple_w[k] && w->ple_b[k];
+  for (int t = 0; t < 2; ++t)
+    ok = ok && w->gate_w[t] && w->gate_b[t] && w->head_w1[t] && w->head_b1[t] && w->head_w2[t] && w->head_b2[t];
+  if (!ok) {
+    fprintf(stderr, "cvr_create: a weight or table pointer is NULL\n");
+    return CVR_E_ARG;
+  }
+  if (!get_encoder()) {
+    fprintf(stderr, "cvr_create: cuTensorMapEncodeTiled is unavailable\n");
+    return CVR_E_CUDA;
+  }
+  {
+    cudaError_t pe = prepare_gemm_kernels();
+    if (pe == cudaSuccess) pe = prepare_mlp_kernels();
+    if (pe != cudaSuccess) {
+      fprintf(stderr, "cvr_create: kernel attribute setup failed: %s\n", cudaGetErrorString(pe));
+      cudaGetLastError();
+      return CVR_E_CUDA;
+    }
+  }
+  cvr_handle* h = new cvr_handle();
+  h->cfg = *cfg;
+  h->n_layers = NL;
+  h->SL = 0;
+  for (int g = 0; g < kG; ++g) {
+    h->L[g] = cfg->seq_len[g];
+    h->SL += cfg->seq_len[g];
+  }
+  cudaGetDevice(&h->device);
+  h->stream = static_cast<cudaStream_t>(cuda_stream);
+  for (int f = 0; f < kFu; ++f) {
+    h->tables[f] = w->user_tables[f];
+    h->rows[f] = cfg->user_rows[f];
+  }
+  for (int f = 0; f < kFi; ++f) {
+    h->tables[kFu + f] = w->item_tables[f];
+    h->rows[kFu + f] = cfg->item_rows[f];
+  }
+  h->tables[kFu + kFi] = w->seq_table;
+  h->rows[kFu + kFi] = cfg->seq_rows;
+
+  // ---- pack dense weights ----
+  Packer P;
+  const size_t o_tokI = P.add_bf((size_t)kXD * kID), o_tokU = P.add_bf((size_t)kXD * kUD);
+  const size_t o_seqW13 = P.add_bf((size_t)kG * 512 * kD), o_seqW2 = P.add_bf((size_t)kG * kD * kHid);
+  const size_t o_qX = P.add_bf((size_t)NL * kG * kD * kXD), o_qm = P.add_bf((size_t)NL * kG * kD * kD);
+  const size_t o_tmW13 = P.add_bf((size_t)NL * 512 * kD), o_tmW2 = P.add_bf((size_t)NL * kD * kHid);
+  const size_t o_pleW = P.add_bf((size_t)kPleCols * kYD), o_headW1 = P.add_bf((size_t)kNT * kHH * kDE);
+  const size_t f_tok_b = P.add_f(kXD), f_seq_b13 = P.add_f(kG * 512), f_seq_b2 = P.add_f(kG * kD);
+  const size_t f_q_b = P.add_f((size_t)NL * kG * kD), f_tm_b13 = P.add_f((size_t)NL * 512);
+  const size_t f_tm_b2 = P.add_f((size_t)NL * kD), f_gain = P.add_f((size_t)NL * kD), f_ple_b = P.add_f(kPleCols);
+  const size_t f_hb1 = P.add_f(kNT * kHH), f_hw2 = P.add_f(kNT * kHH), f_hb2 = P.add_f(32);
+  uint16_t* B = P.bf.data();
+  float* F = P.f32.data();
+  const int IN = kUD + kID;
+  for (int n = 0; n < kXD; ++n)
+    for (int k = 0; k < kUD; ++k) {
+      B[o_tokU + (size_t)n * kUD + k] = f32_to_bf16_bits(w->tok_w[(size_t)n * IN + k]);
+      B[o_tokI + (size_t)n * kID + k] = f32_to_bf16_bits(w->tok_w[(size_t)n * IN + kUD + k]);
+    }
+  std::memcpy(F + f_tok_b, w->tok_b, sizeof(float) * kXD);
+  for (int g = 0; g < kG; ++g) {
+    pack_w13(B + o_seqW13 + (size_t)g * 512 * kD, w->seq_w1[g], w->seq_w3[g], kD);
+    for (size_t i = 0; i < (size_t)kD * kHid; ++i) B[o_seqW2 + (size_t)g * kD * kHid + i] = f32_to_bf16_bits(w->seq_w2[g][i]);
+    pack_b13(F + f_seq_b13 + g * 512, w->seq_b1[g], w->seq_b3[g]);
+    std::memcpy(F + f_seq_b2 + g * kD, w->seq_b2[g], sizeof(float) * kD);
+  }
+  const int QIN = kXD + kD;
+  for (int l = 0; l < NL; ++l) {
+    for (int g = 0; g < kG; ++g) {
+      for (int n = 0; n < kD; ++n) {
+        const float* row = w->q_w[l][g] + (size_t)n * QIN;
+        for (int k = 0; k < kXD; ++k) B[o_qX + ((size_t)(l * kG + g) * kD + n) * kXD + k] = f32_to_bf16_bits(row[k]);
+        for (int k = 0; k < kD; ++k) B[o_qm + ((size_t)(l * kG + g) * kD + n) * kD + k] = f32_to_bf16_bits(row[kXD + k]);
+      }
+      std::memcpy(F + f_q_b + (size_t)(l * kG + g) * kD, w->q_b[l][g], sizeof(float) * kD);
+    }
+    pack_w13(B + o_tmW13 + (size_t)l * 512 * kD, w->tm_w1[l], w->tm_w3[l], kD);
+    for (size_t i = 0; i < (size_t)kD * kHid; ++i) B[o_tmW2 + (size_t)l * kD * kHid + i] = f32_to_bf16_bits(w->tm_w2[l][i]);
+    pack_b13(F + f_tm_b13 + l * 512, w->tm_b1[l], w->tm_b3[l]);
+    std::memcpy(F + f_tm_b2 + l * kD, w->tm_b2[l], sizeof(float) * kD);
+    std::memcpy(F + f_gain + l * kD, w->tm_gain[l], sizeof(float) * kD);
+  }
+  for (int k = 0; k < kNE; ++k) {
+    for (size_t i = 0; i < (size_t)kDE * kYD; ++i) B[o_pleW + (size_t)k * kDE * kYD + i] = f32_to_bf16_bits(w->ple_w[k][i]);
+    std::memcpy(F + f_ple_b + k * kDE, w->ple_b[k], sizeof(float) * kDE);
+  }
+  for (int t = 0; t < kNT; ++t)
+    for (int k = 0; k < kNE; ++k) {
+      for (int c = 0; c < kYD; ++c)
+        B[o_pleW + (size_t)(kPleN + t * kNE + k) * kYD + c] = f32_to_bf16_bits(w->gate_w[t][(size_t)k * kYD + c]);
+      F[f_ple_b + kPleN + t * kNE + k] = w->gate_b[t][k];
+    }
+  for (int t = 0; t < kNT; ++t) {
+    for (size_t i = 0; i < (size_t)kHH * kDE; ++i) B[o_headW1 + (size_t)t * kHH * kDE + i] = f32_to_bf16_bits(w->head_w1[t][i]);
+    std::memcpy(F + f_hb1 + t * kHH, w->head_b1[t], sizeof(float) * kHH);
+    std::memcpy(F + f_hw2 + t * kHH, w->head_w2[t], sizeof(float) * kHH);
+    F[f_hb2 + t] = w->head_b2[t][0];
+  }
+  const size_t bf_bytes = P.bf.size() * 2, f_bytes = P.f32.size() * 4;
+  cudaError_t e = cudaMalloc(&h->wblob, bf_bytes + f_bytes);
+  if (e != cudaSuccess) {
+    delete h;
+    cudaGetLastError();
+    return CVR_E_OOM;
+  }
+  uint8_t* wb = static_cast<uint8_t*>(h->wblob);
+  e = cudaMemcpy(wb, P.bf.data(), bf_bytes, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(wb + bf_bytes, P.f32.data(), f_bytes, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMallocHost(&h->err_host, 64);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    cvr_destroy(h);
+    cudaGetLastError();
+    return CVR_E_CUDA;
+  }
+  bf16* wbf = reinterpret_cast<bf16*>(wb);
+  float* wf = reinterpret_cast<float*>(wb + bf_bytes);
+  h->tokI = wbf + o_tokI;
+  h->tokU = wbf + o_tokU;
+  h->seqW13 = wbf + o_seqW13;
+  h->seqW2 = wbf + o_seqW2;
+  h->qX = wbf + o_qX;
+  h->qm = wbf + o_qm;
+  h->tmW13 = wbf + o_tmW13;
+  h->tmW2 = wbf + o_tmW2;
+  h->pleW = wbf + o_pleW;
+  h->headW1 = wbf + o_headW1;
+  h->tok_b = wf + f_tok_b;
+  h->seq_b13 = wf + f_seq_b13;
+  h->seq_b2 = wf + f_seq_b2;
+  h->q_b = wf + f_q_b;
+  h->tm_b13 = wf + f_tm_b13;
+  h->tm_b2 = wf + f_tm_b2;
+  h->tm_gain = wf + f_gain;
+  h->ple_b = wf + f_ple_b;
+  h->head_b1 = wf + f_hb1;
+  h->head_w2 = wf + f_hw2;
+  h->head_b2 = wf + f_hb2;
+  ok = encode_2d(&h->tm_seqW13, h->seqW13, kD, kG * 512, kD, 64, 256) &&
+       encode_2d(&h->tm_seqW2, h->seqW2, kHid, kG * kD, kHid, 64, 128) &&
+       encode_2d(&h->tm_tokI, h->tokI, kID, kXD, kID, 64, 128) &&
+       encode_2d(&h->tm_tmW13, h->tmW13, kD, (uint64_t)NL * 512, kD, 64, 256) &&
+       encode_2d(&h->tm_tmW2, h->tmW2, kHid, (uint64_t)NL * kD, kHid, 64, 128) &&
+       encode_2d(&h->tm_pleW, h->pleW, kYD, kPleCols, kYD, 64, 112) &&
+       encode_2d(&h->tm_headW1, h->headW1, kDE, kNT * kHH, kDE, 64, 128);
+  for (int l = 0; l < NL && ok; ++l)
+    ok = encode_2d(&h->tm_qW[l], h->qX + (size_t)l * kG * kD * kXD, kXD, kG * kD, kXD, 64, 64);
+  if (!ok) {
+    cvr_destroy(h);
+    return CVR_E_CUDA;
+  }
+  *out = h;
+  return CVR_OK;
+}
+
+cvr_status cvr_score(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids, const int64_t* bag_ids,
+                     const int64_t* bag_offsets, const int64_t* seq_ids, float* out) {
+  return run_forward(h, n_req, n_cand, req_ids, bag_ids, bag_offsets, seq_ids, out, nullptr, nullptr);
+}
+
+cvr_status cvr_score_debug(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids,
+                           const int64_t* bag_ids, const int64_t* bag_offsets, const int64_t* seq_ids, float* out,
+                           float* pooled_fp32, int64_t* rows) {
+  return run_forward(h, n_req, n_cand, req_ids, bag_ids, bag_offsets, seq_ids, out, pooled_fp32, rows);
+}
+
+cvr_status cvr_score_host(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids, const int64_t* bag_ids,
+                          int64_t n_bag_ids, const int64_t* bag_offsets, const int64_t* seq_ids, float* out) {
+  if (!h) return CVR_E_ARG;
+  if (!req_ids || !bag_ids || !bag_offsets || !seq_ids || !out) return fail(h, CVR_E_ARG, "null input or output pointer");
+  if (n_req < 1 || n_cand < 1 || n_req > 65535 || n_cand > (1 << 20) || n_bag_ids < 0)
+    return fail(h, CVR_E_SHAPE, "need 1 <= n_req <= 65535, 1 <= n_cand <= 2^20, n_bag_ids >= 0");
+  cudaError_t ce = cudaSetDevice(h->device);
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaSetDevice");
+  const size_t b_req = (size_t)n_cand * 4, b_ids = (size_t)n_bag_ids * 8;
+  const size_t b_off = ((size_t)n_req * kFu + (size_t)n_cand * kFi + 1) * 8;
+  const size_t b_seq = (size_t)n_req * h->SL * kCols * 8, b_out = (size_t)n_cand * kNT * 4;
+  auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t need = al(b_req) + al(b_ids) + al(b_off) + al(b_seq) + al(b_out);
+  if (need > h->stage_bytes) {
+    // growing the staging area invalidates graphs that captured its addresses
+    for (auto& kv : h->graphs)
+      if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+    h->graphs.clear();
+    if (h->stage) cudaFree(h->stage);
+    h->stage = nullptr;
+    h->stage_bytes = 0;
+    const size_t cap = need + need / 4;
+    ce = cudaMalloc(&h->stage, cap);
+    if (ce != cudaSuccess) {
+      h->stage = nullptr;
+      cudaGetLastError();
+      return fail(h, CVR_E_OOM, "staging allocation failed");
+    }
+    h->stage_bytes = cap;
+  }
+  uint8_t* p = static_cast<uint8_t*>(h->stage);
+  int32_t* d_req = (int32_t*)p;
+  int64_t* d_ids = (int64_t*)(p + al(b_req));
+  int64_t* d_off = (int64_t*)(p + al(b_req) + al(b_ids));
+  int64_t* d_seq = (int64_t*)(p + al(b_req) + al(b_ids) + al(b_off));
+  float* d_out = (float*)(p + al(b_req) + al(b_ids) + al(b_off) + al(b_seq));
+  cudaStream_t s = h->stream;
+  ce = cudaMemcpyAsync(d_req, req_ids, b_req, cudaMemcpyHostToDevice, s);
+  if (ce == cudaSuccess && b_ids) ce = cudaMemcpyAsync(d_ids, bag_ids, b_ids, cudaMemcpyHostToDevice, s);
+  if (ce == cudaSuccess) ce = cudaMemcpyAsync(d_off, bag_offsets, b_off, cudaMemcpyHostToDevice, s);
+  if (ce == cudaSuccess) ce = cudaMemcpyAsync(d_seq, seq_ids, b_seq, cudaMemcpyHostToDevice, s);
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "host-to-device input copy");
+  cvr_status st = run_forward(h, n_req, n_cand, d_req, d_ids, d_off, d_seq, d_out, nullptr, nullptr);
+  ce = cudaMemcpyAsync(out, d_out, b_out, cudaMemcpyDeviceToHost, s);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "device-to-host output copy");
+  return st;
+}
+
+cvr_status cvr_debug_stage(cvr_handle* h, int32_t stage, void* dst, int64_t bytes) {
+  if (!h || !dst) return CVR_E_ARG;
+  if (h->last_B == 0) return fail(h, CVR_E_ARG, "no call has run yet");
+  const void* src = nullptr;
+  int64_t need = 0;
+  const int64_t B = h->last_B, R = h->last_R;
+  switch (stage) {
+    case CVR_STAGE_H: src = h->H; need = R * h->SL * kD * 2; break;
+    case CVR_STAGE_Z: src = h->last_zin; need = B * kYD * 2; break;
+    case CVR_STAGE_Q: src = h->Q; need = B * kG * kD * 2; break;
+    case CVR_STAGE_Y: src = h->last_zout; need = B * kYD * 2; break;
+    case CVR_STAGE_EXPERTS: src = h->Ex; need = B * kPleN * 2; break;
+    case CVR_STAGE_GATES: src = h->gates; need = B * 8 * 4; break;
+    default: return fail(h, CVR_E_ARG, "unknown stage");
+  }
+  if (bytes != need) return fail(h, CVR_E_SHAPE, "stage size mismatch: expected " + std::to_string(need) + " bytes");
+  cudaError_t ce = cudaMemcpyAsync(dst, src, (size_t)need, cudaMemcpyDeviceToDevice, h->stream);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(h->stream);
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "stage copy");
+  return CVR_OK;
+}
+
+cvr_status cvr_set_option(cvr_handle* h, int32_t option, int64_t value) {
+  if (!h) return CVR_E_ARG;
+  if (option == CVR_OPT_PROFILE) {
+    const bool on = value != 0;
+    if (on && h->events.empty()) {
+      const int n = 2 + 5 + 3 * CVR_MAX_LAYERS + 2 + 4;
+      h->events.resize(n);
+      h->event_names.assign(n, nullptr);
+      for (int i = 0; i < n; ++i) {
+        cudaError_t e = cudaEventCreate(&h->events[i]);
+        if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventCreate");
+      }
+    }
+    h->profile = on;
+    return CVR_OK;
+  }
+  if (option == CVR_OPT_CUDA_GRAPH) {
+    h->use_graph = value != 0;
+    return CVR_OK;
+  }
+  return fail(h, CVR_E_ARG, "unknown option");
+}
+
+cvr_status cvr_stage_times(cvr_handle* h, float* ms, const char** names, int32_t cap, int32_t* n) {
+  if (!h || !n) return CVR_E_ARG;
+  *n = 0;
+  if (!h->profile || h->n_events_last == 0) return fail(h, CVR_E_ARG, "profiling is off or no call was profiled");
+  const int cnt = std::min<int>(cap, h->n_events_last);
+  for (int i = 0; i < cnt; ++i) {
+    float t = 0.f;
+    cudaError_t e = cudaEventElapsedTime(&t, h->events[i], h->events[i + 1]);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventElapsedTime");
+    if (ms) ms[i] = t;
+    if (names) names[i] = h->event_names[i];
+  }
+  *n = cnt;
+  return CVR_OK;
+}
+
+void cvr_destroy(cvr_handle* h) {
+  if (!h) return;
+  cudaSetDevice(h->device);
+  if (h->stream) cudaStreamSynchronize(h->stream);
+  free_workspace(h);
+  if (h->stage) cudaFree(h->stage);
+  if (h->wblob) cudaFree(h->wblob);
+  if (h->err_host) cudaFreeHost(h->err_host);
+  for (auto ev : h->events) cudaEventDestroy(ev);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  delete h;
+}
+
+}  // extern "C"

@@ -1,0 +1,245 @@
+// Internal definitions shared by the CVR scoring kernels: model constants, device error bits,
+// the forward-pass argument block and thin inline-PTX wrappers for mbarrier, TMA (cp.async.bulk.tensor)
+// and the 5th-generation tensor core (tcgen05 + TMEM) on sm_103a.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cvr {
+
+// ---- model dimensions (HyFormer-style CVR model of the iQIYI ad-CVR article, section 3.2) ----
+constexpr int kFu = 8;            // user/context fields (one bag per request)
+constexpr int kFi = 8;            // item fields (one bag per candidate)
+constexpr int kE = 32;            // embedding width
+constexpr int kUD = kFu * kE;     // 256: user half of the non-sequence embedding
+constexpr int kID = kFi * kE;     // 256: item half
+constexpr int kN = 13;            // non-sequence tokens
+constexpr int kD = 128;           // token_dim
+constexpr int kG = 3;             // behaviour-sequence groups (= decoded tokens)
+constexpr int kT = kN + kG;       // 16 tokens into the Token Mixer
+constexpr int kXD = kN * kD;      // 1664
+constexpr int kYD = kT * kD;      // 2048
+constexpr int kCols = 4;          // id columns per sequence event
+constexpr int kHid = 256;         // SwiGLU hidden width
+constexpr int kHeads = 4;         // cross-attention heads
+constexpr int kHD = kD / kHeads;  // 32
+constexpr int kNE = 3;            // PLE experts
+constexpr int kDE = 256;          // expert width
+constexpr int kNT = 2;            // tasks
+constexpr int kHH = 128;          // head hidden width
+constexpr int kPleN = kNE * kDE;  // 768 expert columns
+constexpr int kPleCols = 784;     // + 2x3 gate logits, padded to 7 tiles of 112
+constexpr int kMaxLayers = 4;
+
+// ---- device error word bits ----
+constexpr int kErrIdRange = 1;      // a bag or sequence id outside its table
+constexpr int kErrOffsets = 2;      // bag offsets not non-decreasing
+constexpr int kErrReqIds = 4;       // request ids out of range or decreasing
+constexpr int kErrTimeout = 8;      // a bounded wait in a tensor-core kernel gave up
+constexpr int kErrDebugCap = 16;
+
+// ---- arguments of the forward pass, one copy per call ----
+struct FwdArgs {
+  // caller inputs (device)
+  const int32_t* req_ids;
+  const int64_t* bag_ids;
+  const int64_t* bag_offsets;
+  const int64_t* seq_ids;
+  float* out;
+  // debug outputs (device, optional)
+  float* dbg_pooled;
+  int64_t* dbg_rows;
+  // tables (device, borrowed)
+  const float* tables[kFu + kFi + 1];
+  int64_t table_rows[kFu + kFi + 1];
+  // sizes
+  int R, B, SL;
+  int L[kG];
+  int64_t goff[kG];   // first row of group g in the grouped sequence layout = R * (L0 + .. + L_{g-1})
+  int n_layers;
+  float clamp, tau, eps;
+  // workspace
+  __nv_bfloat16* U;       // [R][256]
+  __nv_bfloat16* I;       // [B][256]
+  __nv_bfloat16* Xs;      // [sum_g R*L_g][128] sequence rows, group-major
+  __nv_bfloat16* H;       // same layout: encoded sequence states
+  float* colsum;          // [R][G][max_chunks][128] partial column sums of H
+  int max_chunks;
+  float* xu;              // [R][1664] user half of the tokeniser (+ bias)
+  float* qb;              // [layers][R][384] per-request query term (+ bias)
+  __nv_bfloat16* Z;       // [B][2048] interaction-layer buffers (ping-pong with Y)
+  __nv_bfloat16* Y;       // [B][2048]
+  __nv_bfloat16* Q;       // [B][384]
+  __nv_bfloat16* Ex;      // [B][768] expert outputs (after ReLU)
+  float* gates;           // [B][8] task gate probabilities (2 x 3, padded)
+  int* err;
+  // packed weights (device)
+  const __nv_bfloat16* tokU;   // [1664][256]
+  const float* tok_b;          // [1664]
+  const float* seq_b13;        // [3][512] (interleaved like the weights)
+  const float* seq_b2;         // [3][128]
+  const __nv_bfloat16* qm;     // [layers][3][128][128]: query weights applied to the mean-pooled sequence
+  const float* q_b;            // [layers][384]
+  const float* tm_b13;         // [layers][512]
+  const float* tm_b2;          // [layers][128]
+  const float* tm_gain;        // [layers][128]
+  const float* ple_b;          // [784]
+  const float* head_b1;        // [2][128]
+  const float* head_w2;        // [2][128]
+  const float* head_b2;        // [2]
+};
+
+// ------------------------------------------------------------------------------------------
+// inline PTX
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: gives up after ~1 s, raises the CTA's abort flag and the device error word.
+// Every wait of a CTA checks the abort flag first, so one timeout ends the whole CTA quickly.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (*abort_flag) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > 1000000000ull) {
+      *abort_flag = 1;
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// TMA tiled loads into shared memory, completing on an mbarrier (transaction bytes)
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, uint64_t* bar, int x0, int x1, int x2,
+                                            int x3, int x4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, "
+      "%7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x0), "r"(x1), "r"(x2), "r"(x3), "r"(x4)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---- tcgen05 / TMEM ----
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Instruction descriptor for kind::f16 with bf16 A/B, fp32 accumulate, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// Shared-memory matrix descriptors (tcgen05 format, version 1).
+// K-major, 128-byte swizzle: rows of 128 B, 8-row atoms 1024 B apart (tile base 1024-B aligned).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// K-major, no swizzle: 8x16-byte core matrices; lbo = byte step between core matrices along K,
+// sbo = byte step between 8-row groups along M/N.
+__device__ __forceinline__ uint64_t sdesc_noswz(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
+         ((uint64_t)1 << 46);
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+// mbarrier arrives once every previously issued tcgen05.mma of this thread has completed
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+// 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets lane (base lane + i)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// byte offset of 16-byte chunk `c` of row `r` inside a 128B-swizzled K-major tile (rows of 128 B)
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// ------------------------------------------------------------------------------------------
+// kernel launchers (each returns cudaGetLastError() of its launch)
+cudaError_t prepare_gemm_kernels();  // shared-memory attributes; once per device before any launch
+cudaError_t prepare_mlp_kernels();
+cudaError_t launch_sparse(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_seq_colsum(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_request_side(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_seq_mlp(const FwdArgs& a, const CUtensorMap& tmXs, const CUtensorMap& tmW13,
+                           const CUtensorMap& tmW2, int n_tiles, cudaStream_t s);
+cudaError_t launch_tm_mlp(const FwdArgs& a, int layer, const __nv_bfloat16* zin, __nv_bfloat16* yout,
+                          const CUtensorMap& tmZ, const CUtensorMap& tmW13, const CUtensorMap& tmW2, cudaStream_t s);
+cudaError_t launch_tokenizer(const FwdArgs& a, const CUtensorMap& tmI, const CUtensorMap& tmW, cudaStream_t s);
+cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, const CUtensorMap& tmW, cudaStream_t s);
+cudaError_t launch_attention(const FwdArgs& a, __nv_bfloat16* zin, cudaStream_t s);
+cudaError_t launch_ple(const FwdArgs& a, const CUtensorMap& tmY, const CUtensorMap& tmW, cudaStream_t s);
+cudaError_t launch_heads(const FwdArgs& a, const CUtensorMap& tmW1, cudaStream_t s);
+
+}  // namespace cvr

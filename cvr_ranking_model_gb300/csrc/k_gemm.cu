@@ -1,0 +1,324 @@
+// tcgen05 GEMMs of the CVR forward pass with fused epilogues, and the prediction heads.
+//
+//  gemm_kernel<EPI>  D[128 x BN] = A[128 x K] . W[BN x K]^T, both operands bf16 K-major in 128B-swizzled
+//                    shared memory loaded by TMA through a STAGES-deep mbarrier ring; one elected thread
+//                    issues tcgen05.mma into a TMEM accumulator; four epilogue warps drain TMEM with
+//                    tcgen05.ld (one accumulator row per thread) and apply:
+//    EPI_TOKENIZE    Z[:, 0:1664] = bf16(I . Wtok_item^T + xu[request])        (iQIYI 3.2.2; the user half
+//                    xu, bias included, is computed once per request: iQIYI 3.4.5)
+//    EPI_QUERY       Q = bf16(flat(X) . Wq_x^T + qb[request])                   (iQIYI 3.2.3, item 1)
+//    EPI_PLE         Ex = bf16(ReLU(Y . We^T + be)); the 6 gate logits of the last tile become per-task
+//                    softmax weights over the 3 experts                          (iQIYI 3.2.4)
+//  heads_kernel      per task t: r_t = sum_k gate_t[k] e_k built in shared memory, ReLU(W1_t r_t + b1)
+//                    on tcgen05, then the 128 -> 1 output and sigmoid in the epilogue (iQIYI 3.2.4).
+#include "cvr_internal.cuh"
+
+namespace cvr {
+
+namespace {
+
+enum { EPI_TOKENIZE = 0, EPI_QUERY = 1, EPI_PLE = 2 };
+constexpr int kThreads = 192;  // warp 0: TMA, warp 1: MMA + TMEM owner, warps 2..5: epilogue
+constexpr int kBM = 128, kBK = 64;
+constexpr int kATile = kBM * kBK * 2;  // 16 KB
+
+template <int BN>
+__host__ __device__ constexpr uint32_t tmem_cols() {
+  return BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+}
+template <int BN, int STAGES>
+__host__ __device__ constexpr int gemm_smem_bytes() {
+  return 1024 + STAGES * (kATile + BN * kBK * 2) + 256;
+}
+
+template <int BN, int STAGES, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap tmA,
+                const __grid_constant__ CUtensorMap tmB, int M, int K, int layer) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int B_TILE = BN * kBK * 2;
+  constexpr uint32_t TCOLS = tmem_cols<BN>();
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * kATile;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_TILE);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(tfull + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * BN;
+  const int nk = K / kBK;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) tmem_alloc(tslot, TCOLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % STAGES;
+        if (kb >= STAGES && !mbar_wait(&empty[s], ((kb / STAGES) & 1) ^ 1, abort_flag, a.err)) break;
+        mbar_expect_tx(&full[s], kATile + B_TILE);
+        tma_load_2d(sA + s * kATile, &tmA, &full[s], kb * kBK, m0);
+        tma_load_2d(sB + s * B_TILE, &tmB, &full[s], kb * kBK, n0);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(kBM, BN);
+      bool ok = true;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % STAGES;
+        if (!mbar_wait(&full[s], (kb / STAGES) & 1, abort_flag, a.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t aa = smem_u32(sA + s * kATile), bb = smem_u32(sB + s * B_TILE);
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k)
+          tc_mma(tbase, sdesc_sw128(aa + k * 32), sdesc_sw128(bb + k * 32), idesc, (kb | k) != 0);
+        tc_commit(&empty[s]);
+      }
+      if (ok) tc_commit(tfull);
+    }
+  } else {
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = m0 + q * 32 + lane;
+    if (mbar_wait(tfull, 0, abort_flag, a.err)) {
+      tc_fence_after();
+      const bool live = row < M;
+      int req = 0;
+      if (EPI != EPI_PLE && live) req = min(max(a.req_ids[row], 0), a.R - 1);
+#pragma unroll 1
+      for (int c = 0; c < (BN + 31) / 32; ++c) {
+        float v[32];
+        tmem_ld32(tbase + ((uint32_t)(q * 32) << 16) + c * 32, v);
+        if (!live) continue;
+        const int nb = n0 + c * 32;
+        if (EPI == EPI_TOKENIZE) {
+          const float* add = a.xu + (int64_t)req * kXD + nb;
+          uint4* dst = reinterpret_cast<uint4*>(a.Z + (int64_t)row * kYD + nb);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 p;
+            p.x = pack_bf16(v[8 * j + 0] + add[8 * j + 0], v[8 * j + 1] + add[8 * j + 1]);
+            p.y = pack_bf16(v[8 * j + 2] + add[8 * j + 2], v[8 * j + 3] + add[8 * j + 3]);
+            p.z = pack_bf16(v[8 * j + 4] + add[8 * j + 4], v[8 * j + 5] + add[8 * j + 5]);
+            p.w = pack_bf16(v[8 * j + 6] + add[8 * j + 6], v[8 * j + 7] + add[8 * j + 7]);
+            dst[j] = p;
+          }
+        } else if (EPI == EPI_QUERY) {
+          const float* add = a.qb + ((int64_t)layer * a.R + req) * (kG * kD) + nb;
+          uint4* dst = reinterpret_cast<uint4*>(a.Q + (int64_t)row * (kG * kD) + nb);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 p;
+            p.x = pack_bf16(v[8 * j + 0] + add[8 * j + 0], v[8 * j + 1] + add[8 * j + 1]);
+            p.y = pack_bf16(v[8 * j + 2] + add[8 * j + 2], v[8 * j + 3] + add[8 * j + 3]);
+            p.z = pack_bf16(v[8 * j + 4] + add[8 * j + 4], v[8 * j + 5] + add[8 * j + 5]);
+            p.w = pack_bf16(v[8 * j + 6] + add[8 * j + 6], v[8 * j + 7] + add[8 * j + 7]);
+            dst[j] = p;
+          }
+        } else {  // EPI_PLE
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const int n = nb + j;
+            if (c * 32 + j < BN && n < kPleN) {
+              const float x0 = fmaxf(v[j] + a.ple_b[n], 0.f), x1 = fmaxf(v[j + 1] + a.ple_b[n + 1], 0.f);
+              *reinterpret_cast<uint32_t*>(a.Ex + (int64_t)row * kPleN + n) = pack_bf16(x0, x1);
+            }
+          }
+          if (nb <= kPleN && kPleN < nb + 32 && kPleN + kNT * kNE <= n0 + BN) {
+            const int o = kPleN - nb;  // gate logits sit in columns [768, 774)
+#pragma unroll
+            for (int t = 0; t < kNT; ++t) {
+              float l0 = v[o + 3 * t] + a.ple_b[kPleN + 3 * t];
+              float l1 = v[o + 3 * t + 1] + a.ple_b[kPleN + 3 * t + 1];
+              float l2 = v[o + 3 * t + 2] + a.ple_b[kPleN + 3 * t + 2];
+              const float mx = fmaxf(l0, fmaxf(l1, l2));
+              l0 = expf(l0 - mx);
+              l1 = expf(l1 - mx);
+              l2 = expf(l2 - mx);
+              const float inv = 1.f / (l0 + l1 + l2);
+              float* gd = a.gates + (int64_t)row * 8 + 3 * t;
+              gd[0] = l0 * inv;
+              gd[1] = l1 * inv;
+              gd[2] = l2 * inv;
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, TCOLS);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// prediction heads: grid (ceil(B/128), tasks)
+constexpr int kHeadSmem = 1024 + 4 * kATile + 4 * kATile + 256;
+
+__global__ void __launch_bounds__(kThreads, 1) heads_kernel(const __grid_constant__ FwdArgs a,
+                                                            const __grid_constant__ CUtensorMap tmW1) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;                 // r_t tile: 4 K-blocks of [128][64] bf16, 128B-swizzled
+  uint8_t* sW = smem + 4 * kATile;    // W1_t: 4 K-blocks of [128][64]
+  uint64_t* barA = reinterpret_cast<uint64_t*>(sW + 4 * kATile);
+  uint64_t* barW = barA + 1;
+  uint64_t* barD = barW + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(barD + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * kBM, t = blockIdx.y;
+  if (threadIdx.x == 0) {
+    mbar_init(barA, 128);
+    mbar_init(barW, 1);
+    mbar_init(barD, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tslot, 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_expect_tx(barW, 4 * kATile);
+      for (int kb = 0; kb < 4; ++kb) tma_load_2d(sW + kb * kATile, &tmW1, barW, kb * kBK, t * kHH);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      if (mbar_wait(barA, 0, abort_flag, a.err) && mbar_wait(barW, 0, abort_flag, a.err)) {
+        tc_fence_after();
+        constexpr uint32_t idesc = idesc_bf16(kBM, kHH);
+        for (int kb = 0; kb < 4; ++kb)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc_mma(tbase, sdesc_sw128(smem_u32(sA + kb * kATile) + k * 32), sdesc_sw128(smem_u32(sW + kb * kATile) + k * 32),
+                   idesc, (kb | k) != 0);
+        tc_commit(barD);
+      }
+    }
+  } else {
+    const int q = warp & 3;
+    const int rl = q * 32 + lane;
+    const int row = m0 + rl;
+    const bool live = row < a.B;
+    float g0 = 0.f, g1 = 0.f, g2 = 0.f;
+    if (live) {
+      g0 = a.gates[(int64_t)row * 8 + 3 * t];
+      g1 = a.gates[(int64_t)row * 8 + 3 * t + 1];
+      g2 = a.gates[(int64_t)row * 8 + 3 * t + 2];
+    }
+    const uint4* e = reinterpret_cast<const uint4*>(a.Ex + (int64_t)(live ? row : 0) * kPleN);
+#pragma unroll 4
+    for (int c16 = 0; c16 < kDE / 8; ++c16) {
+      uint4 p = make_uint4(0, 0, 0, 0);
+      if (live) {
+        const uint4 u0 = e[c16], u1 = e[kDE / 8 + c16], u2 = e[2 * kDE / 8 + c16];
+        const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&u0);
+        const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&u1);
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u2);
+        uint32_t* pp = reinterpret_cast<uint32_t*>(&p);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float x0 = g0 * __low2float(h0[i]) + g1 * __low2float(h1[i]) + g2 * __low2float(h2[i]);
+          const float x1 = g0 * __high2float(h0[i]) + g1 * __high2float(h1[i]) + g2 * __high2float(h2[i]);
+          pp[i] = pack_bf16(x0, x1);
+        }
+      }
+      *reinterpret_cast<uint4*>(sA + (c16 >> 3) * kATile + sw128_offset(rl, c16 & 7)) = p;
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(barA);
+    if (mbar_wait(barD, 0, abort_flag, a.err)) {
+      tc_fence_after();
+      float logit = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < kHH / 32; ++c) {
+        float v[32];
+        tmem_ld32(tbase + ((uint32_t)(q * 32) << 16) + c * 32, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int n = t * kHH + c * 32 + j;
+          logit += fmaxf(v[j] + a.head_b1[n], 0.f) * a.head_w2[n];
+        }
+      }
+      if (live) a.out[(int64_t)row * kNT + t] = 1.f / (1.f + expf(-(logit + a.head_b2[t])));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 128);
+  }
+}
+
+template <int BN, int STAGES, int EPI>
+cudaError_t prepare_gemm() {
+  return cudaFuncSetAttribute(gemm_kernel<BN, STAGES, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              gemm_smem_bytes<BN, STAGES>());
+}
+
+template <int BN, int STAGES, int EPI>
+cudaError_t launch_gemm(const FwdArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
+                        int layer, cudaStream_t s) {
+  dim3 grid((M + kBM - 1) / kBM, N / BN);
+  gemm_kernel<BN, STAGES, EPI><<<grid, kThreads, gemm_smem_bytes<BN, STAGES>(), s>>>(a, tmA, tmB, M, K, layer);
+  return cudaGetLastError();
+}
+
+constexpr int kTokBN = 128, kTokStages = 4;
+constexpr int kQryBN = 64, kQryStages = 8;
+constexpr int kPleBN = 112, kPleStages = 6;
+
+}  // namespace
+
+cudaError_t prepare_gemm_kernels() {
+  cudaError_t e = prepare_gemm<kTokBN, kTokStages, EPI_TOKENIZE>();
+  if (e == cudaSuccess) e = prepare_gemm<kQryBN, kQryStages, EPI_QUERY>();
+  if (e == cudaSuccess) e = prepare_gemm<kPleBN, kPleStages, EPI_PLE>();
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(heads_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kHeadSmem);
+  return e;
+}
+
+cudaError_t launch_tokenizer(const FwdArgs& a, const CUtensorMap& tmI, const CUtensorMap& tmW, cudaStream_t s) {
+  return launch_gemm<kTokBN, kTokStages, EPI_TOKENIZE>(a, tmI, tmW, a.B, kXD, kID, 0, s);
+}
+
+cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, const CUtensorMap& tmW, cudaStream_t s) {
+  return launch_gemm<kQryBN, kQryStages, EPI_QUERY>(a, tmX, tmW, a.B, kG * kD, kXD, layer, s);
+}
+
+cudaError_t launch_ple(const FwdArgs& a, const CUtensorMap& tmY, const CUtensorMap& tmW, cudaStream_t s) {
+  return launch_gemm<kPleBN, kPleStages, EPI_PLE>(a, tmY, tmW, a.B, kPleCols, kYD, 0, s);
+}
+
+cudaError_t launch_heads(const FwdArgs& a, const CUtensorMap& tmW1, cudaStream_t s) {
+  heads_kernel<<<dim3((a.B + kBM - 1) / kBM, kNT), kThreads, kHeadSmem, s>>>(a, tmW1);
+  return cudaGetLastError();
+}
+
+}  // namespace cvr

@@ -1,0 +1,254 @@
+// Sparse side of the CVR forward pass and the small per-request GEMVs.
+//
+//  sparse_kernel       mean-pooled multi-hot embedding bags (user bags once per request, item bags per
+//                      candidate; iQIYI ad-CVR article 3.1 item 2 and 3.4.5) with the [-clamp, clamp]
+//                      clamp and bf16 cast after the lookup (GPU CTR inference article, section 三),
+//                      plus the sequence-event gather from the shared id table (iQIYI 3.2.1): one launch
+//                      for every lookup of the batch (iQIYI 3.4.2).
+//  seq_colsum_kernel   partial column sums of the encoded sequences (for the mean-pooled sequence vector
+//                      of Query Decoding, iQIYI 3.2.3).
+//  request_side_kernel the work done once per request: the user half of the tokeniser and the
+//                      mean-pool half of each group's query FFN (the "lazy user repeat" of iQIYI 3.4.5).
+#include "cvr_internal.cuh"
+
+namespace cvr {
+
+namespace {
+
+constexpr int kBagsPerBlock = 32;     // 8 lanes per bag, 256 threads
+constexpr int kEventsPerBlock = 8;    // one warp per sequence event
+
+__device__ __forceinline__ float clampf(float v, float c) { return fminf(fmaxf(v, -c), c); }
+
+__device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float4 v) {
+  uint2 p;
+  p.x = pack_bf16(v.x, v.y);
+  p.y = pack_bf16(v.z, v.w);
+  *reinterpret_cast<uint2*>(dst) = p;
+}
+
+__global__ void __launch_bounds__(256) sparse_kernel(const __grid_constant__ FwdArgs a, int n_bag_blocks) {
+  const int tid = threadIdx.x;
+  if ((int)blockIdx.x < n_bag_blocks) {
+    // request ids: in range and non-decreasing (checked once per candidate)
+    const int64_t cand = (int64_t)blockIdx.x * 256 + tid;
+    if (cand < a.B) {
+      const int r = a.req_ids[cand];
+      bool bad = r < 0 || r >= a.R;
+      if (cand + 1 < a.B && a.req_ids[cand + 1] < r) bad = true;
+      if (bad) atomicOr(a.err, kErrReqIds);
+    }
+    const int64_t n_user_bags = (int64_t)a.R * kFu;
+    const int64_t n_bags = n_user_bags + (int64_t)a.B * kFi;
+    const int64_t bag = (int64_t)blockIdx.x * kBagsPerBlock + (tid >> 3);
+    if (bag >= n_bags) return;
+    const int sub = tid & 7;  // this lane's 4 of the 32 columns
+    int field;
+    __nv_bfloat16* dst;
+    if (bag < n_user_bags) {
+      field = (int)(bag % kFu);
+      dst = a.U + (bag / kFu) * kUD + field * kE;
+    } else {
+      const int64_t ib = bag - n_user_bags;
+      const int f = (int)(ib % kFi);
+      field = kFu + f;
+      dst = a.I + (ib / kFi) * kID + f * kE;
+    }
+    const float* table = a.tables[field];
+    const int64_t rows = a.table_rows[field];
+    const int64_t s = a.bag_offsets[bag];
+    int64_t e = a.bag_offsets[bag + 1];
+    int errbits = 0;
+    if (e < s) {
+      errbits |= kErrOffsets;
+      e = s;
+    }
+    // fp32 sum in bag order from 0 (bit-exact with the definition); 4 rows in flight per step
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t j = s; j < e; j += 4) {
+      int64_t id[4];
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        id[u] = 0;
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j + u < e) {
+          int64_t x = a.bag_ids[j + u];
+          if (x < 0 || x >= rows) {
+            errbits |= kErrIdRange;
+            x = 0;
+          }
+          id[u] = x;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (j + u < e) v[u] = __ldg(reinterpret_cast<const float4*>(table + id[u] * kE) + sub);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (j + u < e) {
+          acc.x = __fadd_rn(acc.x, v[u].x);
+          acc.y = __fadd_rn(acc.y, v[u].y);
+          acc.z = __fadd_rn(acc.z, v[u].z);
+          acc.w = __fadd_rn(acc.w, v[u].w);
+        }
+      }
+      if (a.dbg_rows && sub == 0) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (j + u < e) a.dbg_rows[j + u] = id[u];
+      }
+    }
+    const int64_t n = e - s;
+    float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (n > 0) {
+      const float fn = (float)n;
+      m.x = __fdiv_rn(acc.x, fn);
+      m.y = __fdiv_rn(acc.y, fn);
+      m.z = __fdiv_rn(acc.z, fn);
+      m.w = __fdiv_rn(acc.w, fn);
+    }
+    m.x = clampf(m.x, a.clamp);
+    m.y = clampf(m.y, a.clamp);
+    m.z = clampf(m.z, a.clamp);
+    m.w = clampf(m.w, a.clamp);
+    store_bf16x4(dst + sub * 4, m);
+    if (a.dbg_pooled) reinterpret_cast<float4*>(a.dbg_pooled + bag * kE)[sub] = m;
+    if (errbits) atomicOr(a.err, errbits);
+  } else {
+    // sequence events: 4 id columns -> 4 rows of the shared table -> one 128-wide row
+    const int64_t ev = (int64_t)(blockIdx.x - n_bag_blocks) * kEventsPerBlock + (tid >> 5);
+    if (ev >= (int64_t)a.R * a.SL) return;
+    const int lane = tid & 31, c = lane >> 3, part = lane & 7;
+    const int64_t r = ev / a.SL;
+    int l = (int)(ev - r * a.SL);
+    int g = 0;
+    while (g < kG - 1 && l >= a.L[g]) {
+      l -= a.L[g];
+      ++g;
+    }
+    const int64_t row = a.goff[g] + r * a.L[g] + l;
+    int64_t id = a.seq_ids[ev * kCols + c];
+    if (id < 0 || id >= a.table_rows[kFu + kFi]) {
+      atomicOr(a.err, kErrIdRange);
+      id = 0;
+    }
+    float4 v = __ldg(reinterpret_cast<const float4*>(a.tables[kFu + kFi] + id * kE) + part);
+    v.x = clampf(v.x, a.clamp);
+    v.y = clampf(v.y, a.clamp);
+    v.z = clampf(v.z, a.clamp);
+    v.w = clampf(v.w, a.clamp);
+    store_bf16x4(a.Xs + row * kD + c * kE + part * 4, v);
+  }
+}
+
+// Partial column sums of H over chunks of 64 positions; grid (max_chunks, G, R), 128 threads.
+__global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__ FwdArgs a) {
+  const int chunk = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
+  const int L = a.L[g];
+  if (chunk * 64 >= L) return;
+  const int t = threadIdx.x, cp = t & 63, half = t >> 6;
+  const __nv_bfloat16* base = a.H + (a.goff[g] + (int64_t)r * L) * kD;
+  const int l_end = min(L, chunk * 64 + 64);
+  float s0 = 0.f, s1 = 0.f;
+  for (int l = chunk * 64 + half; l < l_end; l += 2) {
+    const __nv_bfloat162 v = reinterpret_cast<const __nv_bfloat162*>(base + (int64_t)l * kD)[cp];
+    s0 += __low2float(v);
+    s1 += __high2float(v);
+  }
+  __shared__ float part[2][128];
+  part[half][2 * cp] = s0;
+  part[half][2 * cp + 1] = s1;
+  __syncthreads();
+  float* dst = a.colsum + (((int64_t)r * kG + g) * a.max_chunks + chunk) * kD;
+  dst[t] = part[0][t] + part[1][t];
+}
+
+constexpr int kXuBlocks = kXD / 8;  // one warp per tokeniser output column, 8 warps per block
+constexpr int kQbReqPerBlock = 8;
+
+// Blocks [0, kXuBlocks): xu[r][n] = tok_b[n] + sum_k Wtok[n][k] * U[r][k] (user half of the tokeniser).
+// Blocks after: qb[l][r][g*128+n] = q_b[l][g*128+n] + sum_k Wq[l][g][n][1664+k] * m_g[r][k], m_g the
+// mean over positions of the encoded sequence of group g.
+__global__ void __launch_bounds__(256) request_side_kernel(const __grid_constant__ FwdArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((int)blockIdx.x < kXuBlocks) {
+    const int n = blockIdx.x * 8 + warp;
+    const uint4 wraw = reinterpret_cast<const uint4*>(a.tokU + (int64_t)n * kUD)[lane];
+    const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wraw);
+    float w[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w[2 * i] = __low2float(wp[i]);
+      w[2 * i + 1] = __high2float(wp[i]);
+    }
+    const float bias = a.tok_b[n];
+    for (int r = 0; r < a.R; ++r) {
+      const uint4 uraw = reinterpret_cast<const uint4*>(a.U + (int64_t)r * kUD)[lane];
+      const __nv_bfloat162* up = reinterpret_cast<const __nv_bfloat162*>(&uraw);
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc += w[2 * i] * __low2float(up[i]) + w[2 * i + 1] * __high2float(up[i]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) a.xu[(int64_t)r * kXD + n] = acc + bias;
+    }
+    return;
+  }
+  const int nrc = (a.R + kQbReqPerBlock - 1) / kQbReqPerBlock;
+  const int idx = blockIdx.x - kXuBlocks;
+  const int rc = idx % nrc, g = (idx / nrc) % kG, layer = idx / (nrc * kG);
+  __shared__ float m[kQbReqPerBlock][kD];
+  const int L = a.L[g];
+  const int chunks = (L + 63) / 64;
+  for (int i = threadIdx.x; i < kQbReqPerBlock * kD; i += blockDim.x) {
+    const int rr = i / kD, k = i % kD, r = rc * kQbReqPerBlock + rr;
+    float s = 0.f;
+    if (r < a.R) {
+      const float* src = a.colsum + ((int64_t)r * kG + g) * a.max_chunks * kD + k;
+      for (int c = 0; c < chunks; ++c) s += src[(int64_t)c * kD];
+      s /= (float)L;
+    }
+    m[rr][k] = s;
+  }
+  __syncthreads();
+  const __nv_bfloat16* W = a.qm + ((int64_t)layer * kG + g) * kD * kD;
+  for (int n = warp; n < kD; n += 8) {
+    const uint2 wraw = reinterpret_cast<const uint2*>(W + (int64_t)n * kD)[lane];
+    const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wraw);
+    const float w0 = __low2float(wp[0]), w1 = __high2float(wp[0]), w2 = __low2float(wp[1]), w3 = __high2float(wp[1]);
+    const float bias = a.q_b[layer * kG * kD + g * kD + n];
+    for (int rr = 0; rr < kQbReqPerBlock; ++rr) {
+      const int r = rc * kQbReqPerBlock + rr;
+      if (r >= a.R) break;
+      float acc = w0 * m[rr][lane * 4] + w1 * m[rr][lane * 4 + 1] + w2 * m[rr][lane * 4 + 2] + w3 * m[rr][lane * 4 + 3];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) a.qb[((int64_t)layer * a.R + r) * (kG * kD) + g * kD + n] = acc + bias;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_sparse(const FwdArgs& a, cudaStream_t s) {
+  const int64_t n_bags = (int64_t)a.R * kFu + (int64_t)a.B * kFi;
+  const int n_bag_blocks = (int)((n_bags + kBagsPerBlock - 1) / kBagsPerBlock);
+  const int64_t n_events = (int64_t)a.R * a.SL;
+  const int n_seq_blocks = (int)((n_events + kEventsPerBlock - 1) / kEventsPerBlock);
+  sparse_kernel<<<n_bag_blocks + n_seq_blocks, 256, 0, s>>>(a, n_bag_blocks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_seq_colsum(const FwdArgs& a, cudaStream_t s) {
+  seq_colsum_kernel<<<dim3(a.max_chunks, kG, a.R), 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_request_side(const FwdArgs& a, cudaStream_t s) {
+  const int nrc = (a.R + kQbReqPerBlock - 1) / kQbReqPerBlock;
+  request_side_kernel<<<kXuBlocks + a.n_layers * kG * nrc, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace cvr

@@ -1,0 +1,177 @@
+/*
+ * cvr.h -- C ABI of the GB300 CVR scoring library.
+ *
+ * The library scores ad candidates with the HyFormer-style CVR ranking model described in the
+ * iQIYI ad-CVR article ("爱奇艺广告CVR模型参数量10倍增长 ...", m.bobobaike.com/news/370088.html):
+ *
+ *   1. mean-pooled multi-hot embedding bags over fp32 tables (section 3.1 item 2; 3.2.1), clamped to
+ *      [-clamp, clamp] and cast to bf16 after the lookup (GPU CTR inference article,
+ *      gtnt.cn/news/20674, section 三);
+ *   2. tokenisation of the non-sequence embedding [user ; item] into 13 tokens of 128 (3.2.2);
+ *   3. a SwiGLU encoder per behaviour-sequence group, the three groups sharing one id table (3.2.1-3.2.2);
+ *   4. Query Decoding: per group, one query from the 13 tokens and the mean-pooled encoded sequence,
+ *      cross-attending over that sequence with a temperature-scaled softmax (3.2.3);
+ *   5. the Query Boosting Token Mixer over 16 tokens: split -> mix -> SwiGLU -> revert, residual,
+ *      RMSNorm (3.2.3); steps 4-5 stack n_layers times;
+ *   6. a PLE of 3 single-layer experts with per-task softmax gates and a two-layer head per task,
+ *      ending in a sigmoid pCVR (3.2.4).
+ *
+ * Requests follow the user/item split of section 3.4.5: each request carries one user (user bags,
+ * behaviour sequences) and many candidates (item bags), linked by a per-candidate request id; all
+ * user-side work runs once per request. Every per-call size is an argument (section 3.3).
+ *
+ * All work runs in hand-written sm_103a CUDA kernels on the device and stream given at creation.
+ * Conventions:
+ *  - Per-call pointers of cvr_score are DEVICE pointers, borrowed for the duration of the call.
+ *  - Calls are synchronous: they return after the batch is scored and the device error word read.
+ *  - No call aborts, traps or waits on a device flag without a time limit.
+ *  - A handle is not thread-safe; use one handle per host thread / stream.
+ */
+#ifndef CVR_H
+#define CVR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CVR_MAX_LAYERS 4
+#define CVR_N_USER_FIELDS 8
+#define CVR_N_ITEM_FIELDS 8
+#define CVR_N_GROUPS 3
+#define CVR_N_EXPERTS 3
+#define CVR_N_TASKS 2
+
+typedef enum {
+  CVR_OK = 0,
+  CVR_E_ARG = 1,      /* null pointer, unsupported configuration or option */
+  CVR_E_SHAPE = 2,    /* a size out of range */
+  CVR_E_ID_RANGE = 3, /* an id outside its table; the id read row 0 and `out` is not meaningful */
+  CVR_E_OOM = 4,      /* device or pinned-host allocation failed */
+  CVR_E_CUDA = 5,     /* a CUDA call failed (message in cvr_last_error) */
+  CVR_E_INPUT = 6,    /* bag offsets decreasing, or request ids out of range / decreasing */
+  CVR_E_TIMEOUT = 7   /* a bounded device-side wait gave up (reported instead of hanging) */
+} cvr_status;
+
+typedef struct cvr_handle cvr_handle;
+
+/* Model configuration. The kernels are built for the dimensions of the model above; the fixed
+ * fields must hold exactly the values in brackets, otherwise cvr_create returns CVR_E_ARG. */
+typedef struct {
+  int32_t n_user_fields; /* [8]  user/context fields, one bag each per request */
+  int32_t n_item_fields; /* [8]  item fields, one bag each per candidate */
+  int32_t emb_dim;       /* [32] embedding width of every table */
+  int32_t n_tokens;      /* [13] non-sequence tokens N */
+  int32_t token_dim;     /* [128] */
+  int32_t n_groups;      /* [3]  behaviour-sequence groups */
+  int32_t seq_len[3];    /* events per request in each group, >= 1 */
+  int32_t seq_cols;      /* [4]  id columns per event (rows of the shared table, concatenated) */
+  int32_t ffn_hidden;    /* [256] SwiGLU hidden width (sequence encoder and Token Mixer) */
+  int32_t heads;         /* [4]  cross-attention heads (of token_dim / heads = 32) */
+  int32_t n_layers;      /* 1 .. CVR_MAX_LAYERS stacked Query Decoding + Token Mixer layers */
+  int32_t n_experts;     /* [3]  PLE experts */
+  int32_t expert_dim;    /* [256] */
+  int32_t n_tasks;       /* [2]  tasks, one pCVR each */
+  int32_t head_hidden;   /* [128] */
+  float tau;             /* softmax temperature: logits are q.k / (tau * sqrt(32)), > 0 */
+  float clamp;           /* embeddings are clamped to [-clamp, clamp] after pooling / lookup, > 0 */
+  float rms_eps;         /* RMSNorm epsilon, >= 0 */
+  int64_t user_rows[8];  /* rows of each user-field table, >= 1 */
+  int64_t item_rows[8];  /* rows of each item-field table, >= 1 */
+  int64_t seq_rows;      /* rows of the shared sequence table, >= 1 */
+} cvr_config;
+
+/* Weights. Tables are DEVICE fp32 [rows][32] arrays, BORROWED: they must stay valid and unchanged
+ * for the life of the handle. Dense weights are HOST fp32 arrays in [out][in] row-major layout
+ * (biases [out]); they are COPIED and rounded to bf16 (round-to-nearest-even) at creation, except the
+ * biases, RMSNorm gains and the last head layer, which stay fp32. Every pointer is required. */
+typedef struct {
+  const float* user_tables[8];
+  const float* item_tables[8];
+  const float* seq_table;
+  const float* tok_w; /* [13*128][512]: [user 256 ; item 256] -> 13 tokens of 128 */
+  const float* tok_b; /* [1664] */
+  const float *seq_w1[3], *seq_b1[3]; /* [256][128], [256]   group encoders: */
+  const float *seq_w3[3], *seq_b3[3]; /* [256][128], [256]   W2(silu(W1 x+b1)*(W3 x+b3))+b2 */
+  const float *seq_w2[3], *seq_b2[3]; /* [128][256], [128] */
+  const float *q_w[CVR_MAX_LAYERS][3], *q_b[CVR_MAX_LAYERS][3]; /* [128][13*128+128], [128] query FFN */
+  const float *tm_w1[CVR_MAX_LAYERS], *tm_b1[CVR_MAX_LAYERS];   /* [256][128], [256] Token Mixer SwiGLU */
+  const float *tm_w3[CVR_MAX_LAYERS], *tm_b3[CVR_MAX_LAYERS];   /* [256][128], [256] */
+  const float *tm_w2[CVR_MAX_LAYERS], *tm_b2[CVR_MAX_LAYERS];   /* [128][256], [128] */
+  const float* tm_gain[CVR_MAX_LAYERS];                          /* [128] RMSNorm gain */
+  const float *ple_w[3], *ple_b[3];     /* [256][2048], [256] experts over the 16 x 128 tokens */
+  const float *gate_w[2], *gate_b[2];   /* [3][2048], [3]     per-task gates */
+  const float *head_w1[2], *head_b1[2]; /* [128][256], [128] */
+  const float *head_w2[2], *head_b2[2]; /* [1][128], [1] */
+} cvr_weights;
+
+/* Creates a scorer on the current CUDA device, working on `cuda_stream` (a cudaStream_t; NULL =
+ * the legacy default stream). Returns CVR_E_ARG for a bad configuration or a null weight pointer,
+ * CVR_E_OOM / CVR_E_CUDA on device failures. On success *out owns device memory until cvr_destroy. */
+cvr_status cvr_create(const cvr_weights* weights, const cvr_config* cfg, void* cuda_stream, cvr_handle** out);
+
+/* Scores one batch of n_req requests and n_cand candidates (all DEVICE pointers):
+ *   req_ids     [n_cand] int32: request index of each candidate, in [0, n_req), non-decreasing.
+ *   bag_offsets [n_req*8 + n_cand*8 + 1] int64 CSR offsets into bag_ids: first the user bags in
+ *               (request, field) order, then the item bags in (candidate, field) order; non-decreasing.
+ *   bag_ids     [bag_offsets[last]] int64 row ids, local to each field's table. An empty bag pools to 0.
+ *   seq_ids     [n_req][sum(seq_len)][4] int64 rows of the shared sequence table; per request the
+ *               events of group 0, then group 1, then group 2.
+ *   out         [n_cand][2] fp32 pCVR per task, written by the call (caller-owned).
+ * Sizes: 1 <= n_req <= n_cand <= 2^20. Workspace grows on demand (first call at a size allocates).
+ * Returns CVR_E_SHAPE on sizes out of range, CVR_E_ID_RANGE / CVR_E_INPUT on bad ids, offsets or
+ * request ids (detected on the device, never read out of bounds), CVR_E_CUDA on CUDA errors. */
+cvr_status cvr_score(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids, const int64_t* bag_ids,
+                     const int64_t* bag_offsets, const int64_t* seq_ids, float* out);
+
+/* As cvr_score, and also writes the exact pooled embeddings and the rows read (DEVICE pointers, each
+ * may be NULL): pooled_fp32 [n_req*8 + n_cand*8][32] -- the clamped fp32 means of every bag, in
+ * bag_offsets order, before the bf16 cast; rows [bag_offsets[last]] -- the row each id read (the id
+ * itself, or 0 when out of range). */
+cvr_status cvr_score_debug(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids,
+                           const int64_t* bag_ids, const int64_t* bag_offsets, const int64_t* seq_ids, float* out,
+                           float* pooled_fp32, int64_t* rows);
+
+/* As cvr_score with HOST inputs and output: the inputs are copied to device staging buffers owned by
+ * the handle (one asynchronous copy per array; pinned host memory makes them truly asynchronous) and
+ * `out` is copied back before return. n_bag_ids = bag_offsets[last] (the length of bag_ids). */
+cvr_status cvr_score_host(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids, const int64_t* bag_ids,
+                          int64_t n_bag_ids, const int64_t* bag_offsets, const int64_t* seq_ids, float* out);
+
+/* Intermediate results of the last call, copied to `dst` (DEVICE) for inspection; `bytes` must equal
+ * the stage's size for the last call, else CVR_E_SHAPE:
+ *   CVR_STAGE_H   bf16 [group][request][position][128]: encoded sequence states
+ *   CVR_STAGE_Z   bf16 [n_cand][16][128]: input of the last Token Mixer (13 tokens + 3 decoded tokens)
+ *   CVR_STAGE_Q   bf16 [n_cand][3][128]: queries of the last layer
+ *   CVR_STAGE_Y   bf16 [n_cand][16][128]: output of the last Token Mixer
+ *   CVR_STAGE_EXPERTS bf16 [n_cand][768]: PLE expert outputs (after ReLU)
+ *   CVR_STAGE_GATES fp32 [n_cand][8]: task gates (2 x 3, padded to 8) */
+enum { CVR_STAGE_H = 0, CVR_STAGE_Z = 1, CVR_STAGE_Q = 2, CVR_STAGE_Y = 3, CVR_STAGE_EXPERTS = 4, CVR_STAGE_GATES = 5 };
+cvr_status cvr_debug_stage(cvr_handle* h, int32_t stage, void* dst, int64_t bytes);
+
+/* Options (cvr_set_option):
+ *   CVR_OPT_PROFILE      1 = record a CUDA event after every kernel of a call (read with cvr_stage_times)
+ *   CVR_OPT_CUDA_GRAPH   1 = replay the call's kernel sequence from a CUDA graph captured per (n_req, n_cand)
+ *                            (default 1); 0 = launch eagerly */
+enum { CVR_OPT_PROFILE = 0, CVR_OPT_CUDA_GRAPH = 1 };
+cvr_status cvr_set_option(cvr_handle* h, int32_t option, int64_t value);
+
+/* With CVR_OPT_PROFILE set: per-kernel device times of the last call, in launch order. Writes up to
+ * `cap` entries of ms[] and names[] (static strings) and returns the count through *n. */
+cvr_status cvr_stage_times(cvr_handle* h, float* ms, const char** names, int32_t cap, int32_t* n);
+
+/* Number of kernels the last call launched (graph replays count the kernels in the graph). */
+int32_t cvr_last_launch_count(const cvr_handle* h);
+
+/* Human-readable detail of the last failure of this handle ("" if none). */
+const char* cvr_last_error(const cvr_handle* h);
+const char* cvr_status_string(cvr_status s);
+
+/* Frees the handle's device memory, graphs and events. NULL is ignored. */
+void cvr_destroy(cvr_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CVR_H */

@@ -113,7 +113,7 @@ def f32(a) -> np.ndarray:
     return np.ascontiguousarray(a, dtype=np.float32)
 
 
-def model_struct(wl: "synth.Workload") -> Model:
+def model_struct(wl: "synth.Workload", **over) -> Model:
     d = synth.DIMS
     m = Model()
     for k in ("n_user_fields", "n_item_fields", "emb_dim", "n_tokens", "token_dim", "n_groups", "seq_cols",
@@ -123,6 +123,8 @@ def model_struct(wl: "synth.Workload") -> Model:
         m.seq_len[g] = wl.seq_len[g]
     m.n_layers = wl.n_layers
     m.tau, m.clamp, m.rms_eps = d["tau"], d["clamp"], d["rms_eps"]
+    for k, v in over.items():
+        setattr(m, k, v)
     return m
 
 
@@ -169,11 +171,12 @@ class Result:
 
 
 def score(wl: "synth.Workload", w: Dict[str, np.ndarray], requests: Optional[Sequence[int]] = None,
-          dumps: bool = False, threads: int = 0, host_tables: Optional[Dict[int, np.ndarray]] = None) -> Result:
+          dumps: bool = False, threads: int = 0, host_tables: Optional[Dict[int, np.ndarray]] = None,
+          **model_over) -> Result:
     """Runs the oracle over ``requests`` (default: all). ``out`` is [n_cand][n_tasks] fp64 (NaN for the
-    candidates of requests not scored)."""
+    candidates of requests not scored). ``model_over`` overrides tau, clamp or rms_eps."""
     d = synth.DIMS
-    m = model_struct(wl)
+    m = model_struct(wl, **model_over)
     ws = weights_struct(w, wl.n_layers)
     tabs = tables_array(wl, host_tables)
     B, R, SL, D = wl.n_cand, wl.n_req, wl.sum_len, d["token_dim"]

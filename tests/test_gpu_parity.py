@@ -1,0 +1,219 @@
+"""Parity of the CUDA scoring path (through the C ABI) with the CPU oracle.
+
+Bit-exact: the pooled fp32 embedding means and the rows each id read. Within abs 2e-3 / rel 1e-2:
+every pCVR. Small workloads are compared on every candidate and every stage; the full-size
+workloads, in the launch configuration the benchmark times, on the candidates of sampled requests
+(requests are independent, so a sampled request is scored exactly as in the full batch).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import GpuRun, assert_pcvr_close, rel_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_full(wl, w, graph=True, stages=False, **cfg):
+    g = GpuRun(wl, w, graph=graph, **cfg)
+    g.run()
+    ref = oracle.score(wl, w, dumps=True, **cfg)
+    assert ref.status == 0
+    pooled = g.pooled.cpu().numpy()
+    assert np.array_equal(pooled.view(np.uint32), ref.dumps["pooled"].view(np.uint32)), "pooled fp32 not bit-exact"
+    assert np.array_equal(g.rows.cpu().numpy()[: len(wl.bag_ids)], ref.dumps["rows"]), "gather rows differ"
+    if stages:
+        import torch
+        import cvr_ranking_model_gb300 as cvr
+        B, R, SL = wl.n_cand, wl.n_req, wl.sum_len
+        L = wl.seq_len
+        Hg = g.stage(cvr.STAGE_H, (R * SL, 128), torch.bfloat16)
+        # GPU layout: group-major [g][r][l]; oracle: [r][sum_len]
+        off = 0
+        parts = []
+        for gi in range(3):
+            parts.append(Hg[off: off + R * L[gi]].reshape(R, L[gi], 128))
+            off += R * L[gi]
+        H = np.concatenate(parts, axis=1)
+        rel_close(H, ref.dumps["H"], 0.03, "H")
+        last = wl.n_layers - 1
+        Z = g.stage(cvr.STAGE_Z, (B, 16, 128), torch.bfloat16)
+        rel_close(Z[:, :13], ref.dumps["Z"][last][:, :13], 0.03, "tokens x")
+        Q = g.stage(cvr.STAGE_Q, (B, 3, 128), torch.bfloat16)
+        rel_close(Q, ref.dumps["Q"][last], 0.03, "queries")
+        for gi in range(3):
+            rel_close(Z[:, 13 + gi], ref.dumps["Z"][last][:, 13 + gi], 0.05, f"decoded token {gi}")
+        Y = g.stage(cvr.STAGE_Y, (B, 16, 128), torch.bfloat16)
+        rel_close(Y, ref.dumps["Y"][last], 0.03, "token mixer output")
+    return assert_pcvr_close(g.out(), ref.out, wl.name)
+
+
+def test_tiny_every_candidate_and_stage():
+    wl = synth.make_workload("tiny")
+    w = synth.make_weights(wl.n_layers, wl.seed)
+    _check_full(wl, w, stages=True)
+
+
+def test_tiny_with_biases_and_gains():
+    wl = synth.make_workload("tiny")
+    w = synth.make_weights(wl.n_layers, wl.seed, bias_scale=0.05, gain_jitter=0.1)
+    _check_full(wl, w, stages=True)
+
+
+def test_clamp_binds():
+    # tables ~ U(-20, 20): the [-10, 10] clamp binds on pooled means and on sequence rows; small dense
+    # weights keep the rest of the network in its ordinary range
+    wl = synth.make_workload("tiny", table_scale=20.0)
+    w = synth.make_weights(wl.n_layers, wl.seed, weight_scale=0.1, bias_scale=0.05)
+    ref = oracle.score(wl, w, dumps=True)
+    assert np.mean(np.abs(ref.dumps["pooled"]) == 10.0) > 0.2
+    _check_full(wl, w, stages=True)
+
+
+def test_peaked_attention():
+    # tables ~ U(-1, 1) and tau = 0.05: the softmax puts 15-60% of its mass on one position (uniform: 6%)
+    wl = synth.make_workload("tiny", table_scale=1.0)
+    w = synth.make_weights(wl.n_layers, wl.seed, bias_scale=0.05)
+    ref = oracle.score(wl, w, dumps=True, tau=0.05)
+    H, Q = ref.dumps["H"], ref.dumps["Q"][0]
+    pmax = [oracle.cross_attention(Q[b, 2], H[wl.req_ids[b], 32:48], 4, 0.05)[1].max() for b in range(wl.n_cand)]
+    assert np.median(pmax) > 0.15
+    _check_full(wl, w, stages=True, tau=0.05)
+
+
+def test_ragged_requests_and_odd_lengths():
+    # candidates per request 1..70, 130-row tiles crossing requests, sequence lengths off the 64-chunk
+    wl = synth.make_workload("tiny", n_req=5, cand_per_req=[1, 70, 3, 64, 9], seq_len=(3, 70, 129),
+                             user_rows=5000, item_rows=3000)
+    w = synth.make_weights(wl.n_layers, wl.seed, bias_scale=0.02, gain_jitter=0.05)
+    _check_full(wl, w, stages=True)
+
+
+def test_two_layers_small():
+    wl = synth.make_workload("deep", n_req=3, n_cand=40, seq_len=(17, 33, 65), user_rows=1000, item_rows=1000,
+                             seq_rows=10_000)
+    w = synth.make_weights(wl.n_layers, wl.seed, bias_scale=0.02, gain_jitter=0.05)
+    _check_full(wl, w, stages=True)
+
+
+def test_single_request_single_candidate():
+    wl = synth.make_workload("tiny", n_req=1, n_cand=1, seq_len=(1, 1, 1))
+    w = synth.make_weights(wl.n_layers, wl.seed)
+    _check_full(wl, w)
+
+
+def test_eager_and_graph_agree_and_repeat():
+    wl = synth.make_workload("tiny", n_req=3, n_cand=50)
+    w = synth.make_weights(wl.n_layers, wl.seed)
+    g = GpuRun(wl, w, graph=False)
+    g.run()
+    a = g.out()
+    import cvr_ranking_model_gb300 as cvr
+    g.sc.set_option(cvr.OPT_CUDA_GRAPH, 1)
+    g.run()
+    b = g.out()
+    g.run()
+    c = g.out()
+    assert np.array_equal(a, b) and np.array_equal(b, c)
+
+
+def test_host_entry_point_matches_device_entry_point():
+    wl = synth.make_workload("tiny", n_req=2, n_cand=33)
+    w = synth.make_weights(wl.n_layers, wl.seed)
+    g = GpuRun(wl, w)
+    g.run()
+    dev = g.out()
+    out = np.zeros((wl.n_cand, 2), np.float32)
+    g.sc.score_host(wl.n_req, wl.n_cand, wl.req_ids, wl.bag_ids, wl.bag_offsets, np.ascontiguousarray(wl.seq_ids), out)
+    assert np.array_equal(out.astype(np.float64), dev)
+
+
+# ------------------------------------------------------------------ error reporting (no fault)
+def test_out_of_range_id_is_reported_not_read():
+    import cvr_ranking_model_gb300 as cvr
+    wl = synth.make_workload("tiny")
+    wl.bag_ids = wl.bag_ids.copy()
+    wl.bag_ids[5] = 10 ** 12
+    wl.seq_ids = wl.seq_ids.copy()
+    wl.seq_ids[0, 3, 1] = -4
+    w = synth.make_weights(wl.n_layers, wl.seed)
+    g = GpuRun(wl, w)
+    st = g.run(check=False)
+    assert st == 3, cvr.binding.STATUS.get(st)
+    assert g.rows.cpu().numpy()[5] == 0
+
+
+def test_bad_offsets_and_request_ids_are_reported():
+    wl = synth.make_workload("tiny")
+    w = synth.make_weights(wl.n_layers, wl.seed)
+    wl2 = synth.make_workload("tiny")
+    wl2.bag_offsets = wl2.bag_offsets.copy()
+    wl2.bag_offsets[7] = wl2.bag_offsets[9] + 1   # bag 6 ends after bag 7 starts... offsets decrease at 8
+    g = GpuRun(wl2, w)
+    assert g.run(check=False) == 6
+    wl3 = synth.make_workload("tiny")
+    wl3.req_ids = wl3.req_ids.copy()
+    wl3.req_ids[0] = 1                             # decreasing sequence 1, 0, ...
+    g = GpuRun(wl3, w)
+    assert g.run(check=False) == 6
+    wl4 = synth.make_workload("tiny")
+    wl4.req_ids = wl4.req_ids.copy()
+    wl4.req_ids[-1] = 99                           # out of range
+    g = GpuRun(wl4, w)
+    assert g.run(check=False) == 6
+
+
+def test_shape_errors_on_the_host():
+    wl = synth.make_workload("tiny")
+    w = synth.make_weights(wl.n_layers, wl.seed)
+    g = GpuRun(wl, w, debug=False)
+    r, b, o, s, out = g.dw.ptrs()
+    assert g.sc.score(0, 4, r, b, o, s, out, check=False) == 2
+    assert g.sc.score(2, 0, r, b, o, s, out, check=False) == 2
+    assert g.sc.score(2, 8, 0, b, o, s, out, check=False) == 1
+    assert g.sc.score(2, 8, r, b, o, s, out, check=False) == 0   # the handle still works
+
+
+# ------------------------------------------------------------------ full-size workloads (sampled)
+_TABLES = {}
+
+
+def _full(name, requests, n_cand=None):
+    wl = synth.make_workload(name, n_cand=n_cand)
+    w = synth.make_weights(wl.n_layers, wl.seed)
+    g = GpuRun(wl, w, graph=True)
+    g.run()
+    ref = oracle.score(wl, w, requests=requests, dumps=True)
+    assert ref.status == 0
+    sel = np.isin(wl.req_ids, requests)
+    assert_pcvr_close(g.out()[sel], ref.out[sel], name)
+    # pooled sums of the sampled requests' bags, bit for bit
+    pooled = g.pooled.cpu().numpy()
+    nb_user = wl.n_req * 8
+    user_bags = np.concatenate([np.arange(r * 8, r * 8 + 8) for r in requests])
+    item_bags = nb_user + np.concatenate([np.arange(c * 8, c * 8 + 8) for c in np.nonzero(sel)[0]])
+    bags = np.concatenate([user_bags, item_bags])
+    assert np.array_equal(pooled[bags].view(np.uint32), ref.dumps["pooled"][bags].view(np.uint32))
+    rows = g.rows.cpu().numpy()
+    for bag in bags[:: max(1, len(bags) // 2000)]:
+        lo, hi = wl.bag_offsets[bag], wl.bag_offsets[bag + 1]
+        assert np.array_equal(rows[lo:hi], ref.dumps["rows"][lo:hi])
+    return g
+
+
+def test_prod_full_batch():
+    _full("prod", requests=list(range(8)))
+
+
+def test_longseq_sampled():
+    _full("longseq", requests=[0, 15])
+
+
+def test_embheavy_sampled():
+    _full("embheavy", requests=[0, 37, 63])
+
+
+@pytest.mark.parametrize("c", [64, 512, 2048])
+def test_deep_sampled(c):
+    _full("deep", requests=[0, 31] if c < 2048 else [5], n_cand=c)
