@@ -106,12 +106,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (EPI != EPI_PLE && live) req = min(max(a.req_ids[row], 0), a.R - 1);
 #pragma unroll 1
       for (int c = 0; c < (BN + 31) / 32; ++c) {
-        float v[32];
+        float v[32], add[32];
+        const int nb = n0 + c * 32;
+        if (live) {
+          if (EPI == EPI_TOKENIZE) ldg32(a.xu + (int64_t)req * kXD + nb, add);
+          else if (EPI == EPI_QUERY) ldg32(a.qb + ((int64_t)layer * a.R + req) * (kG * kD) + nb, add);
+          else ldg32(a.ple_b + nb, add);
+        }
         tmem_ld32(tbase + ((uint32_t)(q * 32) << 16) + c * 32, v);
         if (!live) continue;
-        const int nb = n0 + c * 32;
         if (EPI == EPI_TOKENIZE) {
-          const float* add = a.xu + (int64_t)req * kXD + nb;
           uint4* dst = reinterpret_cast<uint4*>(a.Z + (int64_t)row * kYD + nb);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -123,7 +127,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[j] = p;
           }
         } else if (EPI == EPI_QUERY) {
-          const float* add = a.qb + ((int64_t)layer * a.R + req) * (kG * kD) + nb;
           uint4* dst = reinterpret_cast<uint4*>(a.Q + (int64_t)row * (kG * kD) + nb);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -139,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 32; j += 2) {
             const int n = nb + j;
             if (c * 32 + j < BN && n < kPleN) {
-              const float x0 = fmaxf(v[j] + a.ple_b[n], 0.f), x1 = fmaxf(v[j + 1] + a.ple_b[n + 1], 0.f);
+              const float x0 = fmaxf(v[j] + add[j], 0.f), x1 = fmaxf(v[j + 1] + add[j + 1], 0.f);
               *reinterpret_cast<uint32_t*>(a.Ex + (int64_t)row * kPleN + n) = pack_bf16(x0, x1);
             }
           }
@@ -147,9 +150,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int o = kPleN - nb;  // gate logits sit in columns [768, 774)
 #pragma unroll
             for (int t = 0; t < kNT; ++t) {
-              float l0 = v[o + 3 * t] + a.ple_b[kPleN + 3 * t];
-              float l1 = v[o + 3 * t + 1] + a.ple_b[kPleN + 3 * t + 1];
-              float l2 = v[o + 3 * t + 2] + a.ple_b[kPleN + 3 * t + 2];
+              float l0 = v[o + 3 * t] + add[o + 3 * t];
+              float l1 = v[o + 3 * t + 1] + add[o + 3 * t + 1];
+              float l2 = v[o + 3 * t + 2] + add[o + 3 * t + 2];
               const float mx = fmaxf(l0, fmaxf(l1, l2));
               l0 = expf(l0 - mx);
               l1 = expf(l1 - mx);
@@ -257,13 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1) heads_kernel(const __grid_constan
       float logit = 0.f;
 #pragma unroll 1
       for (int c = 0; c < kHH / 32; ++c) {
-        float v[32];
+        float v[32], b1[32], w2[32];
+        ldg32(a.head_b1 + t * kHH + c * 32, b1);
+        ldg32(a.head_w2 + t * kHH + c * 32, w2);
         tmem_ld32(tbase + ((uint32_t)(q * 32) << 16) + c * 32, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int n = t * kHH + c * 32 + j;
-          logit += fmaxf(v[j] + a.head_b1[n], 0.f) * a.head_w2[n];
-        }
+        for (int j = 0; j < 32; ++j) logit += fmaxf(v[j] + b1[j], 0.f) * w2[j];
       }
       if (live) a.out[(int64_t)row * kNT + t] = 1.f / (1.f + expf(-(logit + a.head_b2[t])));
     }

@@ -31,7 +31,7 @@ constexpr int kSmemBytes = 1024 + kOffBar + 128;
 
 enum { MODE_SEQ = 0, MODE_TM = 1 };
 
-__device__ __forceinline__ float silu(float x) { return x / (1.f + __expf(-x)); }
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -163,11 +163,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
-        float va[32], vg[32];
+        float va[32], vg[32], ba[32], bg[32];
+        ldg32(b13 + h * 256 + c * 32, ba);
+        ldg32(b13 + h * 256 + 128 + c * 32, bg);
         tmem_ld32(tbase + lane_off + h * 256 + c * 32, va);
         tmem_ld32(tbase + lane_off + h * 256 + 128 + c * 32, vg);
-        const float* ba = b13 + h * 256 + c * 32;
-        const float* bg = ba + 128;
         const int kb = h * 2 + (c >> 1);
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
@@ -194,7 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool live = row < rows_end;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
-          float v[32];
+          float v[32], bb[32];
+          ldg32(b2 + c * 32, bb);
           tmem_ld32(tbase + lane_off + c * 32, v);
           if (!live) continue;
           uint4* dst = reinterpret_cast<uint4*>(a.H + row * kD + c * 32);
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int j = jj * 8 + 2 * i;
-              pp[i] = pack_bf16(v[j] + b2[c * 32 + j], v[j + 1] + b2[c * 32 + j + 1]);
+              pp[i] = pack_bf16(v[j] + bb[j], v[j + 1] + bb[j + 1]);
             }
             dst[jj] = p;
           }
@@ -224,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 8; ++e) gj[e] = gain[j * 8 + e];
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
-          float v[32];
+          float v[32], bb[32];
+          ldg32(b2 + c * 32, bb);
           tmem_ld32(tbase + lane_off + c * 32, v);
 #pragma unroll
           for (int tt = 0; tt < 4; ++tt) {
@@ -235,8 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float ss = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              x[2 * i] = v[tt * 8 + 2 * i] + b2[t * 8 + 2 * i] + __low2float(zp[i]);
-              x[2 * i + 1] = v[tt * 8 + 2 * i + 1] + b2[t * 8 + 2 * i + 1] + __high2float(zp[i]);
+              x[2 * i] = v[tt * 8 + 2 * i] + bb[tt * 8 + 2 * i] + __low2float(zp[i]);
+              x[2 * i + 1] = v[tt * 8 + 2 * i + 1] + bb[tt * 8 + 2 * i + 1] + __high2float(zp[i]);
               ss += x[2 * i] * x[2 * i] + x[2 * i + 1] * x[2 * i + 1];
             }
             ss += __shfl_xor_sync(0xffffffffu, ss, 1);

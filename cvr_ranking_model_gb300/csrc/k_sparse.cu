@@ -164,44 +164,56 @@ __global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__
   dst[t] = part[0][t] + part[1][t];
 }
 
-constexpr int kXuBlocks = kXD / 8;  // one warp per tokeniser output column, 8 warps per block
+constexpr int kXuCols = 32;                 // tokeniser outputs per block
+constexpr int kXuBlocks = kXD / kXuCols;    // 52
+constexpr int kXuReq = 16;                  // requests staged per pass
 constexpr int kQbReqPerBlock = 8;
+constexpr int kXuWStride = kXuCols + 2;     // bf16 elements per staged k-row
+constexpr int kQbWStride = kD + 2;
 
-// Blocks [0, kXuBlocks): xu[r][n] = tok_b[n] + sum_k Wtok[n][k] * U[r][k] (user half of the tokeniser).
-// Blocks after: qb[l][r][g*128+n] = q_b[l][g*128+n] + sum_k Wq[l][g][n][1664+k] * m_g[r][k], m_g the
-// mean over positions of the encoded sequence of group g.
+// Blocks [0, kXuBlocks): xu[r][n] = tok_b[n] + sum_k Wtok[n][k] * U[r][k] (user half of the tokeniser), for
+// 32 columns n per block: the weight slice is staged transposed in shared memory (conflict-free column
+// reads), the users 16 at a time, and every thread finishes whole dot products (no cross-lane reductions).
+// Blocks after: qb[l][r][g*128+n] = q_b[l][g*128+n] + sum_k Wq[l][g][n][1664+k] * m_g[r][k], m_g the mean
+// over positions of the encoded sequence of group g (from the partial column sums).
 __global__ void __launch_bounds__(256) request_side_kernel(const __grid_constant__ FwdArgs a) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ __align__(16) unsigned char smem[40 * 1024];
+  const int tid = threadIdx.x;
   if ((int)blockIdx.x < kXuBlocks) {
-    const int n = blockIdx.x * 8 + warp;
-    const uint4 wraw = reinterpret_cast<const uint4*>(a.tokU + (int64_t)n * kUD)[lane];
-    const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wraw);
-    float w[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      w[2 * i] = __low2float(wp[i]);
-      w[2 * i + 1] = __high2float(wp[i]);
+    __nv_bfloat16* w = reinterpret_cast<__nv_bfloat16*>(smem);                     // [256][34]: w[k][nn]
+    float* act = reinterpret_cast<float*>(smem + kUD * kXuWStride * 2);            // [16][256]
+    const int n0 = blockIdx.x * kXuCols;
+    for (int i = tid; i < kXuCols * kUD; i += blockDim.x) {
+      const int nn = i / kUD, k = i % kUD;
+      w[k * kXuWStride + nn] = a.tokU[(int64_t)(n0 + nn) * kUD + k];
     }
-    const float bias = a.tok_b[n];
-    for (int r = 0; r < a.R; ++r) {
-      const uint4 uraw = reinterpret_cast<const uint4*>(a.U + (int64_t)r * kUD)[lane];
-      const __nv_bfloat162* up = reinterpret_cast<const __nv_bfloat162*>(&uraw);
-      float acc = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc += w[2 * i] * __low2float(up[i]) + w[2 * i + 1] * __high2float(up[i]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (lane == 0) a.xu[(int64_t)r * kXD + n] = acc + bias;
+    const int nn = tid & (kXuCols - 1), rs = tid >> 5;  // 8 request slots per pass
+    const float bias = a.tok_b[n0 + nn];
+    for (int r0 = 0; r0 < a.R; r0 += kXuReq) {
+      const int nr = min(kXuReq, a.R - r0);
+      __syncthreads();
+      for (int i = tid; i < nr * kUD; i += blockDim.x)
+        act[i] = __bfloat162float(a.U[(int64_t)r0 * kUD + i]);
+      __syncthreads();
+      for (int rr = rs; rr < nr; rr += 8) {
+        float acc = 0.f;
+#pragma unroll 8
+        for (int k = 0; k < kUD; ++k) acc += __bfloat162float(w[k * kXuWStride + nn]) * act[rr * kUD + k];
+        a.xu[(int64_t)(r0 + rr) * kXD + n0 + nn] = acc + bias;
+      }
     }
     return;
   }
+  __nv_bfloat16* wt = reinterpret_cast<__nv_bfloat16*>(smem);                       // [128][130]: wt[k][n]
+  float* m = reinterpret_cast<float*>(smem + kD * kQbWStride * 2);                  // [8][128]
   const int nrc = (a.R + kQbReqPerBlock - 1) / kQbReqPerBlock;
   const int idx = blockIdx.x - kXuBlocks;
   const int rc = idx % nrc, g = (idx / nrc) % kG, layer = idx / (nrc * kG);
-  __shared__ float m[kQbReqPerBlock][kD];
   const int L = a.L[g];
   const int chunks = (L + 63) / 64;
-  for (int i = threadIdx.x; i < kQbReqPerBlock * kD; i += blockDim.x) {
+  const __nv_bfloat16* W = a.qm + ((int64_t)layer * kG + g) * kD * kD;
+  for (int i = tid; i < kD * kD; i += blockDim.x) wt[(i % kD) * kQbWStride + i / kD] = W[i];
+  for (int i = tid; i < kQbReqPerBlock * kD; i += blockDim.x) {
     const int rr = i / kD, k = i % kD, r = rc * kQbReqPerBlock + rr;
     float s = 0.f;
     if (r < a.R) {
@@ -209,23 +221,24 @@ __global__ void __launch_bounds__(256) request_side_kernel(const __grid_constant
       for (int c = 0; c < chunks; ++c) s += src[(int64_t)c * kD];
       s /= (float)L;
     }
-    m[rr][k] = s;
+    m[i] = s;
   }
   __syncthreads();
-  const __nv_bfloat16* W = a.qm + ((int64_t)layer * kG + g) * kD * kD;
-  for (int n = warp; n < kD; n += 8) {
-    const uint2 wraw = reinterpret_cast<const uint2*>(W + (int64_t)n * kD)[lane];
-    const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wraw);
-    const float w0 = __low2float(wp[0]), w1 = __high2float(wp[0]), w2 = __low2float(wp[1]), w3 = __high2float(wp[1]);
-    const float bias = a.q_b[layer * kG * kD + g * kD + n];
-    for (int rr = 0; rr < kQbReqPerBlock; ++rr) {
-      const int r = rc * kQbReqPerBlock + rr;
-      if (r >= a.R) break;
-      float acc = w0 * m[rr][lane * 4] + w1 * m[rr][lane * 4 + 1] + w2 * m[rr][lane * 4 + 2] + w3 * m[rr][lane * 4 + 3];
+  const int n = tid & (kD - 1), half = tid >> 7;
+  const float bias = a.q_b[layer * kG * kD + g * kD + n];
+  float acc[kQbReqPerBlock / 2];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (lane == 0) a.qb[((int64_t)layer * a.R + r) * (kG * kD) + g * kD + n] = acc + bias;
-    }
+  for (int j = 0; j < kQbReqPerBlock / 2; ++j) acc[j] = 0.f;
+#pragma unroll 4
+  for (int k = 0; k < kD; ++k) {
+    const float wk = __bfloat162float(wt[k * kQbWStride + n]);
+#pragma unroll
+    for (int j = 0; j < kQbReqPerBlock / 2; ++j) acc[j] += wk * m[(half + 2 * j) * kD + k];
+  }
+#pragma unroll
+  for (int j = 0; j < kQbReqPerBlock / 2; ++j) {
+    const int r = rc * kQbReqPerBlock + half + 2 * j;
+    if (r < a.R) a.qb[((int64_t)layer * a.R + r) * (kG * kD) + g * kD + n] = acc[j] + bias;
   }
 }
 
