@@ -58,6 +58,7 @@ const char* kStageNames[] = {"sparse", "seq_mlp", "seq_colsum", "request_side", 
 
 struct cvr_handle {
   int device = 0;
+  int num_sms = 1;
   cudaStream_t stream = nullptr;
   cudaStream_t cap_stream = nullptr;
   cvr_config cfg{};
@@ -86,7 +87,7 @@ struct cvr_handle {
   CUtensorMap tm_seqW13, tm_seqW2, tm_tokI, tm_qW[kMaxLayers], tm_tmW13, tm_tmW2, tm_pleW, tm_headW1;
   CUtensorMap tm_Xs, tm_I, tm_x_Z, tm_x_Y, tm_5_Z, tm_5_Y, tm_full_Z, tm_full_Y;
   // graphs, profiling
-  bool use_graph = true, profile = false;
+  bool use_graph = true, profile = false, pdl = true;
   std::map<std::pair<int, int>, GraphEntry> graphs;
   std::vector<cudaEvent_t> events;
   std::vector<const char*> event_names;
@@ -176,20 +177,21 @@ struct Packer {
   }
 };
 
-// rows [h*256, h*256+128) = W1 rows [h*128, h*128+128), rows [h*256+128, h*256+256) = W3 rows (h = 0, 1)
+// Hidden chunk c (c = 0..3) of a SwiGLU occupies rows [128c, 128c+64) = W1 rows [64c, 64c+64) and rows
+// [128c+64, 128c+128) = W3 rows [64c, 64c+64): one N=128 MMA yields matching pre-activation columns.
 void pack_w13(uint16_t* dst, const float* w1, const float* w3, int din) {
-  for (int h = 0; h < 2; ++h)
-    for (int i = 0; i < 128; ++i)
+  for (int c = 0; c < 4; ++c)
+    for (int i = 0; i < 64; ++i)
       for (int k = 0; k < din; ++k) {
-        dst[(size_t)(h * 256 + i) * din + k] = f32_to_bf16_bits(w1[(size_t)(h * 128 + i) * din + k]);
-        dst[(size_t)(h * 256 + 128 + i) * din + k] = f32_to_bf16_bits(w3[(size_t)(h * 128 + i) * din + k]);
+        dst[(size_t)(c * 128 + i) * din + k] = f32_to_bf16_bits(w1[(size_t)(c * 64 + i) * din + k]);
+        dst[(size_t)(c * 128 + 64 + i) * din + k] = f32_to_bf16_bits(w3[(size_t)(c * 64 + i) * din + k]);
       }
 }
 void pack_b13(float* dst, const float* b1, const float* b3) {
-  for (int h = 0; h < 2; ++h)
-    for (int i = 0; i < 128; ++i) {
-      dst[h * 256 + i] = b1[h * 128 + i];
-      dst[h * 256 + 128 + i] = b3[h * 128 + i];
+  for (int c = 0; c < 4; ++c)
+    for (int i = 0; i < 64; ++i) {
+      dst[c * 128 + i] = b1[c * 64 + i];
+      dst[c * 128 + 64 + i] = b3[c * 64 + i];
     }
 }
 
@@ -286,6 +288,8 @@ FwdArgs make_args(cvr_handle* h, int R, int B, const int32_t* req_ids, const int
     acc += (int64_t)R * h->L[g];
   }
   a.n_layers = h->n_layers;
+  a.num_sms = h->num_sms;
+  a.pdl = h->pdl ? 1 : 0;
   a.clamp = h->cfg.clamp;
   a.tau = h->cfg.tau;
   a.eps = h->cfg.rms_eps;
@@ -438,6 +442,7 @@ cvr_status run_forward(cvr_handle* h, int32_t R, int32_t B, const int32_t* req_i
   if (ce != cudaSuccess) return cuda_fail(h, ce, "forward pass");
   const int ew = *h->err_host;
   if (ew & kErrTimeout) return fail(h, CVR_E_TIMEOUT, "a bounded device-side wait gave up");
+  if (ew & kErrLayout) return fail(h, CVR_E_CUDA, "a kernel's shared-memory window was not 1024-byte aligned");
   if (ew & (kErrOffsets | kErrReqIds))
     return fail(h, CVR_E_INPUT, (ew & kErrOffsets) ? "bag offsets decrease" : "request ids out of range or decreasing");
   if (ew & kErrIdRange) return fail(h, CVR_E_ID_RANGE, "an id is outside its table (row 0 was read)");
@@ -516,6 +521,8 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
     h->SL += cfg->seq_len[g];
   }
   cudaGetDevice(&h->device);
+  cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (h->num_sms < 1) h->num_sms = 1;
   h->stream = static_cast<cudaStream_t>(cuda_stream);
   for (int f = 0; f < kFu; ++f) {
     h->tables[f] = w->user_tables[f];
@@ -537,7 +544,7 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
   const size_t o_pleW = P.add_bf((size_t)kPleCols * kYD), o_headW1 = P.add_bf((size_t)kNT * kHH * kDE);
   const size_t f_tok_b = P.add_f(kXD), f_seq_b13 = P.add_f(kG * 512), f_seq_b2 = P.add_f(kG * kD);
   const size_t f_q_b = P.add_f((size_t)NL * kG * kD), f_tm_b13 = P.add_f((size_t)NL * 512);
-  const size_t f_tm_b2 = P.add_f((size_t)NL * kD), f_gain = P.add_f((size_t)NL * kD), f_ple_b = P.add_f(kPleCols);
+  const size_t f_tm_b2 = P.add_f((size_t)NL * kD), f_gain = P.add_f((size_t)NL * kD), f_ple_b = P.add_f(kPleCols + 32);
   const size_t f_hb1 = P.add_f(kNT * kHH), f_hw2 = P.add_f(kNT * kHH), f_hb2 = P.add_f(32);
   uint16_t* B = P.bf.data();
   float* F = P.f32.data();
@@ -626,15 +633,15 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
   h->head_b1 = wf + f_hb1;
   h->head_w2 = wf + f_hw2;
   h->head_b2 = wf + f_hb2;
-  ok = encode_2d(&h->tm_seqW13, h->seqW13, kD, kG * 512, kD, 64, 256) &&
+  ok = encode_2d(&h->tm_seqW13, h->seqW13, kD, kG * 512, kD, 64, 128) &&
        encode_2d(&h->tm_seqW2, h->seqW2, kHid, kG * kD, kHid, 64, 128) &&
        encode_2d(&h->tm_tokI, h->tokI, kID, kXD, kID, 64, 128) &&
-       encode_2d(&h->tm_tmW13, h->tmW13, kD, (uint64_t)NL * 512, kD, 64, 256) &&
+       encode_2d(&h->tm_tmW13, h->tmW13, kD, (uint64_t)NL * 512, kD, 64, 128) &&
        encode_2d(&h->tm_tmW2, h->tmW2, kHid, (uint64_t)NL * kD, kHid, 64, 128) &&
-       encode_2d(&h->tm_pleW, h->pleW, kYD, kPleCols, kYD, 64, 112) &&
+       encode_2d(&h->tm_pleW, h->pleW, kYD, kPleCols, kYD, 64, 208) &&
        encode_2d(&h->tm_headW1, h->headW1, kDE, kNT * kHH, kDE, 64, 128);
   for (int l = 0; l < NL && ok; ++l)
-    ok = encode_2d(&h->tm_qW[l], h->qX + (size_t)l * kG * kD * kXD, kXD, kG * kD, kXD, 64, 64);
+    ok = encode_2d(&h->tm_qW[l], h->qX + (size_t)l * kG * kD * kXD, kXD, kG * kD, kXD, 64, 96);
   if (!ok) {
     cvr_destroy(h);
     return CVR_E_CUDA;
@@ -743,6 +750,13 @@ cvr_status cvr_set_option(cvr_handle* h, int32_t option, int64_t value) {
   }
   if (option == CVR_OPT_CUDA_GRAPH) {
     h->use_graph = value != 0;
+    return CVR_OK;
+  }
+  if (option == CVR_OPT_PDL) {
+    h->pdl = value != 0;
+    for (auto& kv : h->graphs)
+      if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+    h->graphs.clear();
     return CVR_OK;
   }
   return fail(h, CVR_E_ARG, "unknown option");

@@ -31,7 +31,7 @@ constexpr int kDE = 256;          // expert width
 constexpr int kNT = 2;            // tasks
 constexpr int kHH = 128;          // head hidden width
 constexpr int kPleN = kNE * kDE;  // 768 expert columns
-constexpr int kPleCols = 784;     // + 2x3 gate logits, padded to 7 tiles of 112
+constexpr int kPleCols = 832;     // + 2x3 gate logits, zero-padded to 4 tiles of 208
 constexpr int kMaxLayers = 4;
 
 // ---- device error word bits ----
@@ -40,6 +40,7 @@ constexpr int kErrOffsets = 2;      // bag offsets not non-decreasing
 constexpr int kErrReqIds = 4;       // request ids out of range or decreasing
 constexpr int kErrTimeout = 8;      // a bounded wait in a tensor-core kernel gave up
 constexpr int kErrDebugCap = 16;
+constexpr int kErrLayout = 32;      // a kernel found its shared-memory window misaligned and did nothing
 
 // ---- arguments of the forward pass, one copy per call ----
 struct FwdArgs {
@@ -60,6 +61,8 @@ struct FwdArgs {
   int L[kG];
   int64_t goff[kG];   // first row of group g in the grouped sequence layout = R * (L0 + .. + L_{g-1})
   int n_layers;
+  int num_sms;            // persistent-kernel grid size
+  int pdl;                // launch with programmatic dependent launch
   float clamp, tau, eps;
   // workspace
   __nv_bfloat16* U;       // [R][256]
@@ -86,7 +89,7 @@ struct FwdArgs {
   const float* tm_b13;         // [layers][512]
   const float* tm_b2;          // [layers][128]
   const float* tm_gain;        // [layers][128]
-  const float* ple_b;          // [784]
+  const float* ple_b;          // [832 + 32]
   const float* head_b1;        // [2][128]
   const float* head_w2;        // [2][128]
   const float* head_b2;        // [2]
@@ -136,6 +139,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
   }
 }
+// Programmatic dependent launch: let the next kernel in the stream launch (its prologue overlaps this
+// kernel), and wait until the previous kernel has completed and its writes are visible. Every kernel of
+// the forward pass waits before touching data an earlier kernel wrote, which keeps the ordering transitive.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -195,14 +204,23 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
           d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T: A (M=128 rows = lanes, 16-bit elements packed two per column) read
+// from tensor memory, issued by one thread
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
 // mbarrier arrives once every previously issued tcgen05.mma of this thread has completed
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
-// 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets lane (base lane + i)
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-  uint32_t r[32];
+// 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets lane (base lane + i). The _nowait form
+// leaves the registers pending until tmem_ld_wait(), so several loads can be in flight at once.
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
       "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
@@ -211,9 +229,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
         "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 32 lanes x 16 consecutive 32-bit columns from registers (thread i -> lane base + i)
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  tmem_ld32_nowait(taddr, r);
+  tmem_ld_wait();
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+// silu(x) = x * sigmoid(x) = x * (0.5 + 0.5 tanh(x / 2)): one MUFU op (tanh.approx) per value
+__device__ __forceinline__ float silu_tanh(float x) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+  return x * fmaf(0.5f, t, 0.5f);
 }
 
 // 32 consecutive fp32 values (16-byte aligned, read-only for the kernel) into registers, issued together
@@ -233,13 +272,62 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
 }
+// Packed fp32 pairs (Blackwell f32x2 ALU ops): two values per instruction.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// silu(a) * g for two pairs at once: silu(a) = a * (0.5 + 0.5 tanh(a / 2)), one tanh.approx per value;
+// returns the two products packed as bf16x2 (round to nearest even)
+__device__ __forceinline__ uint32_t silu_mul_bf16x2(uint64_t a, uint64_t g) {
+  const uint64_t half = f2pack(0.5f, 0.5f);
+  const uint64_t h = mul_f32x2(a, half);
+  float t0, t1;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t0) : "f"(__uint_as_float((uint32_t)h)));
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t1) : "f"(__uint_as_float((uint32_t)(h >> 32))));
+  const uint64_t sg = fma_f32x2(f2pack(t0, t1), half, half);
+  const uint64_t r = mul_f32x2(mul_f32x2(a, sg), g);
+  return pack_bf16(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
+}
 // byte offset of 16-byte chunk `c` of row `r` inside a 128B-swizzled K-major tile (rows of 128 B)
 __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
 // ------------------------------------------------------------------------------------------
-// kernel launchers (each returns cudaGetLastError() of its launch)
+// Launch with the programmatic-stream-serialization attribute when `pdl` (the first kernel of a sequence
+// is launched without it).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                                 Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
+// kernel launchers (each returns the launch's error code)
 cudaError_t prepare_gemm_kernels();  // shared-memory attributes; once per device before any launch
 cudaError_t prepare_mlp_kernels();
 cudaError_t launch_sparse(const FwdArgs& a, cudaStream_t s);

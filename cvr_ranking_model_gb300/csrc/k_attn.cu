@@ -47,6 +47,8 @@ __global__ void __launch_bounds__(128) attention_kernel(const __grid_constant__ 
   const int gid = lane >> 2, tig = lane & 3;
   const int L = a.L[g];
   const int R = a.R, B = a.B;
+  pdl_trigger();
+  pdl_wait();
   const int b_last = min(b0 + kCandPerCta, B) - 1;
   // request ids are validated by the sparse kernel; here they are only kept in range
   const int r_first = min(max(a.req_ids[b0], 0), R - 1);
@@ -57,18 +59,21 @@ __global__ void __launch_bounds__(128) attention_kernel(const __grid_constant__ 
   const int reqB = rowB < B ? a.req_ids[rowB] : -1;
 
   // query fragments (A operand, rows = candidates), 4 heads x 2 k-steps of 16
+  // rows past the batch load the last candidate's query (their results are never stored): unconditional
+  // loads keep all 32 in flight together
   uint32_t qf[kHeads][2][4];
+  const int64_t qrA = min(rowA, B - 1), qrB = min(rowB, B - 1);
 #pragma unroll
   for (int h = 0; h < kHeads; ++h)
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
       const int col = g * kD + h * kHD + ks * 16 + 2 * tig;
-      const uint32_t* qa = reinterpret_cast<const uint32_t*>(a.Q + (int64_t)rowA * (kG * kD) + col);
-      const uint32_t* qb = reinterpret_cast<const uint32_t*>(a.Q + (int64_t)rowB * (kG * kD) + col);
-      qf[h][ks][0] = rowA < B ? qa[0] : 0u;
-      qf[h][ks][1] = rowB < B ? qb[0] : 0u;
-      qf[h][ks][2] = rowA < B ? qa[4] : 0u;
-      qf[h][ks][3] = rowB < B ? qb[4] : 0u;
+      const uint32_t* qa = reinterpret_cast<const uint32_t*>(a.Q + qrA * (kG * kD) + col);
+      const uint32_t* qb = reinterpret_cast<const uint32_t*>(a.Q + qrB * (kG * kD) + col);
+      qf[h][ks][0] = __ldg(qa);
+      qf[h][ks][1] = __ldg(qb);
+      qf[h][ks][2] = __ldg(qa + 4);
+      qf[h][ks][3] = __ldg(qb + 4);
     }
   // logits * log2(e) / (tau * sqrt(head_dim)) so that the softmax runs on exp2
   const float sl2 = 1.4426950408889634f / (a.tau * sqrtf((float)kHD));
@@ -205,8 +210,7 @@ __global__ void __launch_bounds__(128) attention_kernel(const __grid_constant__ 
 
 cudaError_t launch_attention(const FwdArgs& a, __nv_bfloat16* zin, cudaStream_t s) {
   const int nblk = (a.B + kCandPerCta - 1) / kCandPerCta;
-  attention_kernel<<<dim3(nblk, kG), 128, 0, s>>>(a, zin);
-  return cudaGetLastError();
+  return launch_kernel(attention_kernel, dim3(nblk, kG), dim3(128), 0, s, a.pdl != 0, a, zin);
 }
 
 }  // namespace cvr

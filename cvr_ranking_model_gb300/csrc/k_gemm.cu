@@ -18,7 +18,7 @@ namespace cvr {
 namespace {
 
 enum { EPI_TOKENIZE = 0, EPI_QUERY = 1, EPI_PLE = 2 };
-constexpr int kThreads = 192;  // warp 0: TMA, warp 1: MMA + TMEM owner, warps 2..5: epilogue
+constexpr int kThreads = 192;  // heads kernel: warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
 constexpr int kBM = 128, kBK = 64;
 constexpr int kATile = kBM * kBK * 2;  // 16 KB
 
@@ -31,81 +31,114 @@ __host__ __device__ constexpr int gemm_smem_bytes() {
   return 1024 + STAGES * (kATile + BN * kBK * 2) + 256;
 }
 
-template <int BN, int STAGES, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+// Persistent GEMM: CTAs loop over 128 x BN output tiles (n fastest, so co-running CTAs share A rows in L2).
+// Warp 0 streams A/B k-blocks through a STAGES-deep ring; warp 1 issues the MMAs into one of two TMEM
+// accumulators; NEPI epilogue warps drain the other one, so a tile's epilogue overlaps the next tile's
+// MMAs. With 8 epilogue warps the two warpgroups split the 32-column chunks of a tile.
+template <int BN, int STAGES, int EPI, int NEPI>
+__global__ void __launch_bounds__(64 + NEPI * 32, 1)
     gemm_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap tmA,
-                const __grid_constant__ CUtensorMap tmB, int M, int K, int layer) {
+                const __grid_constant__ CUtensorMap tmB, int M, int N, int K, int layer) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int B_TILE = BN * kBK * 2;
-  constexpr uint32_t TCOLS = tmem_cols<BN>();
+  constexpr uint32_t TC = tmem_cols<BN>();
+  constexpr int NCHUNK = (BN + 31) / 32;
+  constexpr int NGRP = NEPI / 4;
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * kATile;
   uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_TILE);
   uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(tfull + 1);
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * BN;
+  const int tiles_n = N / BN;
+  const int n_tiles = ((M + kBM - 1) / kBM) * tiles_n;
   const int nk = K / kBK;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tfull, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], NEPI);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  if (warp == 1) tmem_alloc(tslot, TCOLS);
+  if (warp == 1) tmem_alloc(tslot, 2 * TC);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
+  pdl_trigger();
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % STAGES;
-        if (kb >= STAGES && !mbar_wait(&empty[s], ((kb / STAGES) & 1) ^ 1, abort_flag, a.err)) break;
-        mbar_expect_tx(&full[s], kATile + B_TILE);
-        tma_load_2d(sA + s * kATile, &tmA, &full[s], kb * kBK, m0);
-        tma_load_2d(sB + s * B_TILE, &tmB, &full[s], kb * kBK, n0);
+      int kc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile / tiles_n) * kBM, n0 = (tile % tiles_n) * BN;
+        for (int kb = 0; kb < nk; ++kb, ++kc) {
+          const int s = kc % STAGES;
+          if (kc >= STAGES && !mbar_wait(&empty[s], ((kc / STAGES) & 1) ^ 1, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&full[s], kATile + B_TILE);
+          tma_load_2d(sA + s * kATile, &tmA, &full[s], kb * kBK, m0);
+          tma_load_2d(sB + s * B_TILE, &tmB, &full[s], kb * kBK, n0);
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(kBM, BN);
+      int kc = 0, i = 0;
       bool ok = true;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % STAGES;
-        if (!mbar_wait(&full[s], (kb / STAGES) & 1, abort_flag, a.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t aa = smem_u32(sA + s * kATile), bb = smem_u32(sB + s * B_TILE);
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++i) {
+        const int buf = i & 1;
+        if (i >= 2 && !mbar_wait(&acc_empty[buf], ((i >> 1) & 1) ^ 1, abort_flag, a.err)) break;
+        const uint32_t dacc = tbase + buf * TC;
+        for (int kb = 0; kb < nk; ++kb, ++kc) {
+          const int s = kc % STAGES;
+          if (!mbar_wait(&full[s], (kc / STAGES) & 1, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t aa = smem_u32(sA + s * kATile), bb = smem_u32(sB + s * B_TILE);
 #pragma unroll
-        for (int k = 0; k < kBK / 16; ++k)
-          tc_mma(tbase, sdesc_sw128(aa + k * 32), sdesc_sw128(bb + k * 32), idesc, (kb | k) != 0);
-        tc_commit(&empty[s]);
+          for (int k = 0; k < kBK / 16; ++k)
+            tc_mma(dacc, sdesc_sw128(aa + k * 32), sdesc_sw128(bb + k * 32), idesc, (kb | k) != 0);
+          tc_commit(&empty[s]);
+        }
+        if (ok) tc_commit(&acc_full[buf]);
       }
-      if (ok) tc_commit(tfull);
     }
   } else {
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int row = m0 + q * 32 + lane;
-    if (mbar_wait(tfull, 0, abort_flag, a.err)) {
-      tc_fence_after();
+    const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int grp = (warp - 2) >> 2;     // chunk group
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    int i = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++i) {
+      const int m0 = (tile / tiles_n) * kBM, n0 = (tile % tiles_n) * BN;
+      const int buf = i & 1;
+      const int row = m0 + q * 32 + lane;
       const bool live = row < M;
       int req = 0;
       if (EPI != EPI_PLE && live) req = min(max(a.req_ids[row], 0), a.R - 1);
+      if (!mbar_wait(&acc_full[buf], (i >> 1) & 1, abort_flag, a.err)) break;
+      tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < (BN + 31) / 32; ++c) {
+      for (int c = grp; c < NCHUNK; c += NGRP) {
         float v[32], add[32];
         const int nb = n0 + c * 32;
         if (live) {
@@ -113,23 +146,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           else if (EPI == EPI_QUERY) ldg32(a.qb + ((int64_t)layer * a.R + req) * (kG * kD) + nb, add);
           else ldg32(a.ple_b + nb, add);
         }
-        tmem_ld32(tbase + ((uint32_t)(q * 32) << 16) + c * 32, v);
+        tmem_ld32(tbase + lane_off + buf * TC + c * 32, v);
         if (!live) continue;
-        if (EPI == EPI_TOKENIZE) {
-          uint4* dst = reinterpret_cast<uint4*>(a.Z + (int64_t)row * kYD + nb);
+        if (EPI == EPI_TOKENIZE || EPI == EPI_QUERY) {
+          __nv_bfloat16* out = EPI == EPI_TOKENIZE ? a.Z + (int64_t)row * kYD + nb : a.Q + (int64_t)row * (kG * kD) + nb;
+          uint4* dst = reinterpret_cast<uint4*>(out);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            uint4 p;
-            p.x = pack_bf16(v[8 * j + 0] + add[8 * j + 0], v[8 * j + 1] + add[8 * j + 1]);
-            p.y = pack_bf16(v[8 * j + 2] + add[8 * j + 2], v[8 * j + 3] + add[8 * j + 3]);
-            p.z = pack_bf16(v[8 * j + 4] + add[8 * j + 4], v[8 * j + 5] + add[8 * j + 5]);
-            p.w = pack_bf16(v[8 * j + 6] + add[8 * j + 6], v[8 * j + 7] + add[8 * j + 7]);
-            dst[j] = p;
-          }
-        } else if (EPI == EPI_QUERY) {
-          uint4* dst = reinterpret_cast<uint4*>(a.Q + (int64_t)row * (kG * kD) + nb);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
+            if (c * 32 + j * 8 >= BN) break;
             uint4 p;
             p.x = pack_bf16(v[8 * j + 0] + add[8 * j + 0], v[8 * j + 1] + add[8 * j + 1]);
             p.y = pack_bf16(v[8 * j + 2] + add[8 * j + 2], v[8 * j + 3] + add[8 * j + 3]);
@@ -138,12 +162,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[j] = p;
           }
         } else {  // EPI_PLE
+          if (nb < kPleN) {
+            uint4* dst = reinterpret_cast<uint4*>(a.Ex + (int64_t)row * kPleN + nb);
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const int n = nb + j;
-            if (c * 32 + j < BN && n < kPleN) {
-              const float x0 = fmaxf(v[j] + add[j], 0.f), x1 = fmaxf(v[j + 1] + add[j + 1], 0.f);
-              *reinterpret_cast<uint32_t*>(a.Ex + (int64_t)row * kPleN + n) = pack_bf16(x0, x1);
+            for (int j = 0; j < 4; ++j) {
+              if (c * 32 + j * 8 >= BN || nb + j * 8 >= kPleN) break;
+              uint4 p;
+              uint32_t* pp = reinterpret_cast<uint32_t*>(&p);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                pp[e] = pack_bf16(fmaxf(v[8 * j + 2 * e] + add[8 * j + 2 * e], 0.f),
+                                  fmaxf(v[8 * j + 2 * e + 1] + add[8 * j + 2 * e + 1], 0.f));
+              dst[j] = p;
             }
           }
           if (nb <= kPleN && kPleN < nb + 32 && kPleN + kNT * kNE <= n0 + BN) {
@@ -166,13 +196,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tbase, TCOLS);
+    tmem_dealloc(tbase, 2 * TC);
   }
 }
 
@@ -205,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1) heads_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
+  pdl_trigger();
+  pdl_wait();
   if (warp == 0) {
     if (lane == 0) {
       mbar_expect_tx(barW, 4 * kATile);
@@ -228,30 +263,40 @@ __global__ void __launch_bounds__(kThreads, 1) heads_kernel(const __grid_constan
     const int rl = q * 32 + lane;
     const int row = m0 + rl;
     const bool live = row < a.B;
-    float g0 = 0.f, g1 = 0.f, g2 = 0.f;
-    if (live) {
-      g0 = a.gates[(int64_t)row * 8 + 3 * t];
-      g1 = a.gates[(int64_t)row * 8 + 3 * t + 1];
-      g2 = a.gates[(int64_t)row * 8 + 3 * t + 2];
-    }
-    const uint4* e = reinterpret_cast<const uint4*>(a.Ex + (int64_t)(live ? row : 0) * kPleN);
-#pragma unroll 4
-    for (int c16 = 0; c16 < kDE / 8; ++c16) {
-      uint4 p = make_uint4(0, 0, 0, 0);
-      if (live) {
-        const uint4 u0 = e[c16], u1 = e[kDE / 8 + c16], u2 = e[2 * kDE / 8 + c16];
-        const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&u0);
-        const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&u1);
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u2);
+    // r_t = sum_k gate_t[k] e_k for the tile's 128 rows: warp w builds rows w, w+4, ...; lane l covers
+    // hidden units [8l, 8l+8) (a 16-byte vector of each expert), four rows' loads in flight at once.
+    const int ew = warp - 2;
+#pragma unroll 1
+    for (int r0 = ew; r0 < kBM; r0 += 16) {
+      uint4 u[4][3];
+      float g[4][3];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int rr = r0 + 4 * k, grow = m0 + rr;
+        const bool ok = grow < a.B;
+        const uint4* e = reinterpret_cast<const uint4*>(a.Ex + (int64_t)(ok ? grow : 0) * kPleN);
+#pragma unroll
+        for (int x = 0; x < 3; ++x) {
+          u[k][x] = ok ? __ldg(e + x * (kDE / 8) + lane) : make_uint4(0, 0, 0, 0);
+          g[k][x] = ok ? __ldg(a.gates + (int64_t)grow * 8 + 3 * t + x) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int rr = r0 + 4 * k;
+        const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&u[k][0]);
+        const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&u[k][1]);
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u[k][2]);
+        uint4 p;
         uint32_t* pp = reinterpret_cast<uint32_t*>(&p);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float x0 = g0 * __low2float(h0[i]) + g1 * __low2float(h1[i]) + g2 * __low2float(h2[i]);
-          const float x1 = g0 * __high2float(h0[i]) + g1 * __high2float(h1[i]) + g2 * __high2float(h2[i]);
+          const float x0 = g[k][0] * __low2float(h0[i]) + g[k][1] * __low2float(h1[i]) + g[k][2] * __low2float(h2[i]);
+          const float x1 = g[k][0] * __high2float(h0[i]) + g[k][1] * __high2float(h1[i]) + g[k][2] * __high2float(h2[i]);
           pp[i] = pack_bf16(x0, x1);
         }
+        *reinterpret_cast<uint4*>(sA + (lane >> 3) * kATile + sw128_offset(rr, lane & 7)) = p;
       }
-      *reinterpret_cast<uint4*>(sA + (c16 >> 3) * kATile + sw128_offset(rl, c16 & 7)) = p;
     }
     fence_proxy_async_smem();
     mbar_arrive(barA);
@@ -278,49 +323,50 @@ __global__ void __launch_bounds__(kThreads, 1) heads_kernel(const __grid_constan
   }
 }
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, int NEPI>
 cudaError_t prepare_gemm() {
-  return cudaFuncSetAttribute(gemm_kernel<BN, STAGES, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(gemm_kernel<BN, STAGES, EPI, NEPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               gemm_smem_bytes<BN, STAGES>());
 }
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, int NEPI>
 cudaError_t launch_gemm(const FwdArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
                         int layer, cudaStream_t s) {
-  dim3 grid((M + kBM - 1) / kBM, N / BN);
-  gemm_kernel<BN, STAGES, EPI><<<grid, kThreads, gemm_smem_bytes<BN, STAGES>(), s>>>(a, tmA, tmB, M, K, layer);
-  return cudaGetLastError();
+  const int tiles = ((M + kBM - 1) / kBM) * (N / BN);
+  const int grid = tiles < a.num_sms ? tiles : a.num_sms;
+  return launch_kernel(gemm_kernel<BN, STAGES, EPI, NEPI>, dim3(grid), dim3(64 + NEPI * 32), gemm_smem_bytes<BN, STAGES>(),
+                       s, a.pdl != 0, a, tmA, tmB, M, N, K, layer);
 }
 
-constexpr int kTokBN = 128, kTokStages = 4;
-constexpr int kQryBN = 64, kQryStages = 8;
-constexpr int kPleBN = 112, kPleStages = 6;
+constexpr int kTokBN = 128, kTokStages = 4, kTokEpi = 4;
+constexpr int kQryBN = 96, kQryStages = 6, kQryEpi = 4;
+constexpr int kPleBN = 208, kPleStages = 5, kPleEpi = 8;
+static_assert(kPleCols % kPleBN == 0, "PLE columns are a whole number of tiles");
 
 }  // namespace
 
 cudaError_t prepare_gemm_kernels() {
-  cudaError_t e = prepare_gemm<kTokBN, kTokStages, EPI_TOKENIZE>();
-  if (e == cudaSuccess) e = prepare_gemm<kQryBN, kQryStages, EPI_QUERY>();
-  if (e == cudaSuccess) e = prepare_gemm<kPleBN, kPleStages, EPI_PLE>();
+  cudaError_t e = prepare_gemm<kTokBN, kTokStages, EPI_TOKENIZE, kTokEpi>();
+  if (e == cudaSuccess) e = prepare_gemm<kQryBN, kQryStages, EPI_QUERY, kQryEpi>();
+  if (e == cudaSuccess) e = prepare_gemm<kPleBN, kPleStages, EPI_PLE, kPleEpi>();
   if (e == cudaSuccess) e = cudaFuncSetAttribute(heads_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kHeadSmem);
   return e;
 }
 
 cudaError_t launch_tokenizer(const FwdArgs& a, const CUtensorMap& tmI, const CUtensorMap& tmW, cudaStream_t s) {
-  return launch_gemm<kTokBN, kTokStages, EPI_TOKENIZE>(a, tmI, tmW, a.B, kXD, kID, 0, s);
+  return launch_gemm<kTokBN, kTokStages, EPI_TOKENIZE, kTokEpi>(a, tmI, tmW, a.B, kXD, kID, 0, s);
 }
 
 cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, const CUtensorMap& tmW, cudaStream_t s) {
-  return launch_gemm<kQryBN, kQryStages, EPI_QUERY>(a, tmX, tmW, a.B, kG * kD, kXD, layer, s);
+  return launch_gemm<kQryBN, kQryStages, EPI_QUERY, kQryEpi>(a, tmX, tmW, a.B, kG * kD, kXD, layer, s);
 }
 
 cudaError_t launch_ple(const FwdArgs& a, const CUtensorMap& tmY, const CUtensorMap& tmW, cudaStream_t s) {
-  return launch_gemm<kPleBN, kPleStages, EPI_PLE>(a, tmY, tmW, a.B, kPleCols, kYD, 0, s);
+  return launch_gemm<kPleBN, kPleStages, EPI_PLE, kPleEpi>(a, tmY, tmW, a.B, kPleCols, kYD, 0, s);
 }
 
 cudaError_t launch_heads(const FwdArgs& a, const CUtensorMap& tmW1, cudaStream_t s) {
-  heads_kernel<<<dim3((a.B + kBM - 1) / kBM, kNT), kThreads, kHeadSmem, s>>>(a, tmW1);
-  return cudaGetLastError();
+  return launch_kernel(heads_kernel, dim3((a.B + kBM - 1) / kBM, kNT), dim3(kThreads), kHeadSmem, s, a.pdl != 0, a, tmW1);
 }
 
 }  // namespace cvr

@@ -29,6 +29,8 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float4 v) {
 
 __global__ void __launch_bounds__(256) sparse_kernel(const __grid_constant__ FwdArgs a, int n_bag_blocks) {
   const int tid = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();
   if ((int)blockIdx.x < n_bag_blocks) {
     // request ids: in range and non-decreasing (checked once per candidate)
     const int64_t cand = (int64_t)blockIdx.x * 256 + tid;
@@ -40,8 +42,9 @@ __global__ void __launch_bounds__(256) sparse_kernel(const __grid_constant__ Fwd
     }
     const int64_t n_user_bags = (int64_t)a.R * kFu;
     const int64_t n_bags = n_user_bags + (int64_t)a.B * kFi;
-    const int64_t bag = (int64_t)blockIdx.x * kBagsPerBlock + (tid >> 3);
-    if (bag >= n_bags) return;
+    const int64_t bag_raw = (int64_t)blockIdx.x * kBagsPerBlock + (tid >> 3);
+    const bool live = bag_raw < n_bags;             // dead lanes still take part in the shuffles
+    const int64_t bag = live ? bag_raw : n_bags - 1;
     const int sub = tid & 7;  // this lane's 4 of the 32 columns
     int field;
     __nv_bfloat16* dst;
@@ -63,40 +66,39 @@ __global__ void __launch_bounds__(256) sparse_kernel(const __grid_constant__ Fwd
       errbits |= kErrOffsets;
       e = s;
     }
-    // fp32 sum in bag order from 0 (bit-exact with the definition); 4 rows in flight per step
+    // The 8 lanes of a bag load 8 ids at once (one each), share them by shuffle, then have all 8 rows in
+    // flight; the fp32 sum still runs in bag order from 0 (bit-exact with the definition). The loop count
+    // is the warp's largest bag, so every lane reaches every shuffle.
+    int64_t nmax = e - s;
+    nmax = max(nmax, (int64_t)__shfl_xor_sync(0xffffffffu, (long long)nmax, 8));
+    nmax = max(nmax, (int64_t)__shfl_xor_sync(0xffffffffu, (long long)nmax, 16));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t j = s; j < e; j += 4) {
-      int64_t id[4];
-      float4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        id[u] = 0;
-        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j + u < e) {
-          int64_t x = a.bag_ids[j + u];
-          if (x < 0 || x >= rows) {
-            errbits |= kErrIdRange;
-            x = 0;
-          }
-          id[u] = x;
+    for (int64_t base = 0; base < nmax; base += 8) {
+      const int64_t j = s + base + sub;
+      int64_t mine = 0;
+      if (j < e) {
+        mine = a.bag_ids[j];
+        if (mine < 0 || mine >= rows) {
+          errbits |= kErrIdRange;
+          mine = 0;
         }
+        if (a.dbg_rows && live) a.dbg_rows[j] = mine;
+      }
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t id = __shfl_sync(0xffffffffu, (long long)mine, u, 8);
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s + base + u < e) v[u] = __ldg(reinterpret_cast<const float4*>(table + id * kE) + sub);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (j + u < e) v[u] = __ldg(reinterpret_cast<const float4*>(table + id[u] * kE) + sub);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (j + u < e) {
+      for (int u = 0; u < 8; ++u) {
+        if (s + base + u < e) {
           acc.x = __fadd_rn(acc.x, v[u].x);
           acc.y = __fadd_rn(acc.y, v[u].y);
           acc.z = __fadd_rn(acc.z, v[u].z);
           acc.w = __fadd_rn(acc.w, v[u].w);
         }
-      }
-      if (a.dbg_rows && sub == 0) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (j + u < e) a.dbg_rows[j + u] = id[u];
       }
     }
     const int64_t n = e - s;
@@ -112,6 +114,7 @@ __global__ void __launch_bounds__(256) sparse_kernel(const __grid_constant__ Fwd
     m.y = clampf(m.y, a.clamp);
     m.z = clampf(m.z, a.clamp);
     m.w = clampf(m.w, a.clamp);
+    if (!live) return;
     store_bf16x4(dst + sub * 4, m);
     if (a.dbg_pooled) reinterpret_cast<float4*>(a.dbg_pooled + bag * kE)[sub] = m;
     if (errbits) atomicOr(a.err, errbits);
@@ -146,13 +149,16 @@ __global__ void __launch_bounds__(256) sparse_kernel(const __grid_constant__ Fwd
 __global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__ FwdArgs a) {
   const int chunk = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
   const int L = a.L[g];
+  pdl_trigger();
+  pdl_wait();
   if (chunk * 64 >= L) return;
   const int t = threadIdx.x, cp = t & 63, half = t >> 6;
   const __nv_bfloat16* base = a.H + (a.goff[g] + (int64_t)r * L) * kD;
   const int l_end = min(L, chunk * 64 + 64);
   float s0 = 0.f, s1 = 0.f;
+#pragma unroll 8
   for (int l = chunk * 64 + half; l < l_end; l += 2) {
-    const __nv_bfloat162 v = reinterpret_cast<const __nv_bfloat162*>(base + (int64_t)l * kD)[cp];
+    const __nv_bfloat162 v = __ldg(reinterpret_cast<const __nv_bfloat162*>(base + (int64_t)l * kD) + cp);
     s0 += __low2float(v);
     s1 += __high2float(v);
   }
@@ -179,21 +185,42 @@ constexpr int kQbWStride = kD + 2;
 __global__ void __launch_bounds__(256) request_side_kernel(const __grid_constant__ FwdArgs a) {
   __shared__ __align__(16) unsigned char smem[40 * 1024];
   const int tid = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();
   if ((int)blockIdx.x < kXuBlocks) {
     __nv_bfloat16* w = reinterpret_cast<__nv_bfloat16*>(smem);                     // [256][34]: w[k][nn]
     float* act = reinterpret_cast<float*>(smem + kUD * kXuWStride * 2);            // [16][256]
     const int n0 = blockIdx.x * kXuCols;
-    for (int i = tid; i < kXuCols * kUD; i += blockDim.x) {
-      const int nn = i / kUD, k = i % kUD;
-      w[k * kXuWStride + nn] = a.tokU[(int64_t)(n0 + nn) * kUD + k];
+    // 32 rows x 256 bf16 = 1024 16-byte vectors: 4 per thread, all loads issued before any store
+    {
+      uint4 raw[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int v = tid + t * 256, nn = v >> 5, k8 = v & 31;
+        raw[t] = __ldg(reinterpret_cast<const uint4*>(a.tokU + (int64_t)(n0 + nn) * kUD) + k8);
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int v = tid + t * 256, nn = v >> 5, k8 = v & 31;
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[t]);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) w[(k8 * 8 + q) * kXuWStride + nn] = e[q];
+      }
     }
     const int nn = tid & (kXuCols - 1), rs = tid >> 5;  // 8 request slots per pass
     const float bias = a.tok_b[n0 + nn];
     for (int r0 = 0; r0 < a.R; r0 += kXuReq) {
       const int nr = min(kXuReq, a.R - r0);
       __syncthreads();
-      for (int i = tid; i < nr * kUD; i += blockDim.x)
-        act[i] = __bfloat162float(a.U[(int64_t)r0 * kUD + i]);
+      for (int v = tid; v < nr * (kUD / 8); v += blockDim.x) {   // 16-byte vectors of U
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(a.U + (int64_t)r0 * kUD) + v);
+        const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          act[v * 8 + 2 * q] = __low2float(e[q]);
+          act[v * 8 + 2 * q + 1] = __high2float(e[q]);
+        }
+      }
       __syncthreads();
       for (int rr = rs; rr < nr; rr += 8) {
         float acc = 0.f;
@@ -212,13 +239,25 @@ __global__ void __launch_bounds__(256) request_side_kernel(const __grid_constant
   const int L = a.L[g];
   const int chunks = (L + 63) / 64;
   const __nv_bfloat16* W = a.qm + ((int64_t)layer * kG + g) * kD * kD;
-  for (int i = tid; i < kD * kD; i += blockDim.x) wt[(i % kD) * kQbWStride + i / kD] = W[i];
+  {  // wt[k][n] = W[n][k]: 2048 16-byte vectors, 8 per thread, loads issued before the stores
+    uint4 raw[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) raw[t] = __ldg(reinterpret_cast<const uint4*>(W) + tid + t * 256);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int v = tid + t * 256, n = v >> 4, k8 = v & 15;
+      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[t]);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) wt[(k8 * 8 + q) * kQbWStride + n] = e[q];
+    }
+  }
   for (int i = tid; i < kQbReqPerBlock * kD; i += blockDim.x) {
     const int rr = i / kD, k = i % kD, r = rc * kQbReqPerBlock + rr;
     float s = 0.f;
     if (r < a.R) {
       const float* src = a.colsum + ((int64_t)r * kG + g) * a.max_chunks * kD + k;
-      for (int c = 0; c < chunks; ++c) s += src[(int64_t)c * kD];
+#pragma unroll 8
+      for (int c = 0; c < chunks; ++c) s += __ldg(src + (int64_t)c * kD);
       s /= (float)L;
     }
     m[i] = s;
@@ -249,19 +288,16 @@ cudaError_t launch_sparse(const FwdArgs& a, cudaStream_t s) {
   const int n_bag_blocks = (int)((n_bags + kBagsPerBlock - 1) / kBagsPerBlock);
   const int64_t n_events = (int64_t)a.R * a.SL;
   const int n_seq_blocks = (int)((n_events + kEventsPerBlock - 1) / kEventsPerBlock);
-  sparse_kernel<<<n_bag_blocks + n_seq_blocks, 256, 0, s>>>(a, n_bag_blocks);
-  return cudaGetLastError();
+  return launch_kernel(sparse_kernel, dim3(n_bag_blocks + n_seq_blocks), dim3(256), 0, s, false, a, n_bag_blocks);
 }
 
 cudaError_t launch_seq_colsum(const FwdArgs& a, cudaStream_t s) {
-  seq_colsum_kernel<<<dim3(a.max_chunks, kG, a.R), 128, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(seq_colsum_kernel, dim3(a.max_chunks, kG, a.R), dim3(128), 0, s, a.pdl != 0, a);
 }
 
 cudaError_t launch_request_side(const FwdArgs& a, cudaStream_t s) {
   const int nrc = (a.R + kQbReqPerBlock - 1) / kQbReqPerBlock;
-  request_side_kernel<<<kXuBlocks + a.n_layers * kG * nrc, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(request_side_kernel, dim3(kXuBlocks + a.n_layers * kG * nrc), dim3(256), 0, s, a.pdl != 0, a);
 }
 
 }  // namespace cvr
