@@ -64,6 +64,10 @@ def lib() -> ctypes.CDLL:
         L.cvr_create.restype = ctypes.c_int
         L.cvr_score.argtypes = [V, i32, i32, V, V, V, V, V]
         L.cvr_score.restype = ctypes.c_int
+        L.cvr_score_async.argtypes = [V, i32, i32, V, V, V, V, V]
+        L.cvr_score_async.restype = ctypes.c_int
+        L.cvr_sync.argtypes = [V]
+        L.cvr_sync.restype = ctypes.c_int
         L.cvr_score_debug.argtypes = [V, i32, i32, V, V, V, V, V, V, V]
         L.cvr_score_debug.restype = ctypes.c_int
         L.cvr_score_host.argtypes = [V, i32, i32, V, V, i64, V, V, V]
@@ -163,6 +167,16 @@ class Scorer:
             self._check(st)
         return st
 
+    def score_async(self, n_req: int, n_cand: int, req_ids: int, bag_ids: int, bag_offsets: int, seq_ids: int,
+                    out: int) -> None:
+        self._check(self._lib.cvr_score_async(self._h, n_req, n_cand, req_ids, bag_ids, bag_offsets, seq_ids, out))
+
+    def sync(self, check: bool = True) -> int:
+        st = self._lib.cvr_sync(self._h)
+        if check:
+            self._check(st)
+        return st
+
     def score_debug(self, n_req, n_cand, req_ids, bag_ids, bag_offsets, seq_ids, out, pooled: Optional[int],
                     rows: Optional[int], check: bool = True) -> int:
         st = self._lib.cvr_score_debug(self._h, n_req, n_cand, req_ids, bag_ids, bag_offsets, seq_ids, out, pooled,
@@ -227,5 +241,5 @@ class Scorer:
             pass
 
 
-EXPORTED = ["cvr_create", "cvr_score", "cvr_score_debug", "cvr_score_host", "cvr_debug_stage", "cvr_set_option",
+EXPORTED = ["cvr_create", "cvr_score", "cvr_score_async", "cvr_sync", "cvr_score_debug", "cvr_score_host", "cvr_debug_stage", "cvr_set_option",
             "cvr_stage_times", "cvr_last_launch_count", "cvr_last_error", "cvr_status_string", "cvr_destroy"]

@@ -79,7 +79,9 @@ struct cvr_handle {
   bf16 *U = nullptr, *I = nullptr, *Xs = nullptr, *H = nullptr, *Z = nullptr, *Y = nullptr, *Q = nullptr, *Ex = nullptr;
   float *colsum = nullptr, *xu = nullptr, *qb = nullptr, *gates = nullptr;
   int* err = nullptr;
-  int* err_host = nullptr;
+  unsigned* done = nullptr;
+  int* err_host = nullptr;      // pinned, mapped: the call's error bits
+  int* err_host_dev = nullptr;  // its device address
   // host-input staging
   void* stage = nullptr;
   size_t stage_bytes = 0;
@@ -225,7 +227,7 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   const size_t oQb = take((size_t)h->n_layers * R_cap * kG * kD * 4);
   const size_t oZ = take((size_t)B_cap * kYD * 2), oY = take((size_t)B_cap * kYD * 2);
   const size_t oQ = take((size_t)B_cap * kG * kD * 2), oEx = take((size_t)B_cap * kPleN * 2);
-  const size_t oG = take((size_t)B_cap * 8 * 4), oErr = take(64);
+  const size_t oG = take((size_t)B_cap * 8 * 4), oErr = take(1024);
   cudaError_t e = cudaMalloc(&h->ws, off);
   if (e != cudaSuccess) {
     h->ws = nullptr;
@@ -246,6 +248,12 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   h->Ex = (bf16*)(b + oEx);
   h->gates = (float*)(b + oG);
   h->err = (int*)(b + oErr);
+  h->done = (unsigned*)(b + oErr + 256);
+  e = cudaMemset(h->err, 0, 1024);  // error word and CTA counter start at zero; the last kernel resets them
+  if (e != cudaSuccess) {
+    free_workspace(h);
+    return fail(h, CVR_E_CUDA, "workspace initialisation failed");
+  }
   h->R_cap = R_cap;
   h->B_cap = B_cap;
   h->max_chunks = max_chunks;
@@ -307,6 +315,8 @@ FwdArgs make_args(cvr_handle* h, int R, int B, const int32_t* req_ids, const int
   a.Ex = h->Ex;
   a.gates = h->gates;
   a.err = h->err;
+  a.done = h->done;
+  a.err_host = h->err_host_dev;
   a.tokU = h->tokU;
   a.tok_b = h->tok_b;
   a.seq_b13 = h->seq_b13;
@@ -345,7 +355,6 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
   if (events)
     e = external_events ? cudaEventRecordWithFlags(h->events[0], s, cudaEventRecordExternal)
                         : cudaEventRecord(h->events[0], s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(h->err, 0, sizeof(int), s);
   run(launch_sparse(a, s), kStageNames[0]);
   int seq_tiles = 0;
   for (int g = 0; g < kG; ++g) seq_tiles += (int)(((int64_t)a.R * a.L[g] + 127) / 128);
@@ -371,13 +380,17 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
   return e;
 }
 
+cvr_status sync_status(cvr_handle* h);
+
 cvr_status run_forward(cvr_handle* h, int32_t R, int32_t B, const int32_t* req_ids, const int64_t* bag_ids,
                        const int64_t* bag_offsets, const int64_t* seq_ids, float* out, float* dbg_pooled,
-                       int64_t* dbg_rows) {
+                       int64_t* dbg_rows, bool sync = true) {
   if (!h) return CVR_E_ARG;
   if (!req_ids || !bag_ids || !bag_offsets || !seq_ids || !out) return fail(h, CVR_E_ARG, "null input or output pointer");
   if (R < 1 || B < 1 || R > 65535 || B > (1 << 20)) return fail(h, CVR_E_SHAPE, "need 1 <= n_req <= 65535, 1 <= n_cand <= 2^20");
-  cudaError_t ce = cudaSetDevice(h->device);
+  int cur = -1;
+  cudaError_t ce = cudaGetDevice(&cur);
+  if (ce == cudaSuccess && cur != h->device) ce = cudaSetDevice(h->device);
   if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaSetDevice");
   cvr_status st = ensure_workspace(h, R, B);
   if (st != CVR_OK) return st;
@@ -436,11 +449,17 @@ cvr_status run_forward(cvr_handle* h, int32_t R, int32_t B, const int32_t* req_i
   }
   h->last_R = R;
   h->last_B = B;
-  ce = cudaMemcpyAsync(h->err_host, h->err, sizeof(int), cudaMemcpyDeviceToHost, s);
-  if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaMemcpyAsync(error word)");
-  ce = cudaStreamSynchronize(s);
+  if (!sync) return CVR_OK;
+  return sync_status(h);
+}
+
+// Waits for the stream, then reads and clears the error bits every call since the last sync published.
+cvr_status sync_status(cvr_handle* h) {
+  cudaError_t ce = cudaStreamSynchronize(h->stream);
   if (ce != cudaSuccess) return cuda_fail(h, ce, "forward pass");
-  const int ew = *h->err_host;
+  volatile int* hw = h->err_host;
+  const int ew = *hw;
+  *hw = 0;
   if (ew & kErrTimeout) return fail(h, CVR_E_TIMEOUT, "a bounded device-side wait gave up");
   if (ew & kErrLayout) return fail(h, CVR_E_CUDA, "a kernel's shared-memory window was not 1024-byte aligned");
   if (ew & (kErrOffsets | kErrReqIds))
@@ -506,6 +525,7 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
   {
     cudaError_t pe = prepare_gemm_kernels();
     if (pe == cudaSuccess) pe = prepare_mlp_kernels();
+    if (pe == cudaSuccess) pe = prepare_attention_kernel();
     if (pe != cudaSuccess) {
       fprintf(stderr, "cvr_create: kernel attribute setup failed: %s\n", cudaGetErrorString(pe));
       cudaGetLastError();
@@ -603,7 +623,11 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
   uint8_t* wb = static_cast<uint8_t*>(h->wblob);
   e = cudaMemcpy(wb, P.bf.data(), bf_bytes, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(wb + bf_bytes, P.f32.data(), f_bytes, cudaMemcpyHostToDevice);
-  if (e == cudaSuccess) e = cudaMallocHost(&h->err_host, 64);
+  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&h->err_host), 64, cudaHostAllocMapped);
+  if (e == cudaSuccess) {
+    *h->err_host = 0;
+    e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->err_host_dev), h->err_host, 0);
+  }
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking);
   if (e != cudaSuccess) {
     cvr_destroy(h);
@@ -653,6 +677,16 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
 cvr_status cvr_score(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids, const int64_t* bag_ids,
                      const int64_t* bag_offsets, const int64_t* seq_ids, float* out) {
   return run_forward(h, n_req, n_cand, req_ids, bag_ids, bag_offsets, seq_ids, out, nullptr, nullptr);
+}
+
+cvr_status cvr_score_async(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids, const int64_t* bag_ids,
+                           const int64_t* bag_offsets, const int64_t* seq_ids, float* out) {
+  return run_forward(h, n_req, n_cand, req_ids, bag_ids, bag_offsets, seq_ids, out, nullptr, nullptr, false);
+}
+
+cvr_status cvr_sync(cvr_handle* h) {
+  if (!h) return CVR_E_ARG;
+  return sync_status(h);
 }
 
 cvr_status cvr_score_debug(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids,

@@ -78,7 +78,9 @@ struct FwdArgs {
   __nv_bfloat16* Q;       // [B][384]
   __nv_bfloat16* Ex;      // [B][768] expert outputs (after ReLU)
   float* gates;           // [B][8] task gate probabilities (2 x 3, padded)
-  int* err;
+  int* err;               // device error word (bits below), reset by the last kernel of each call
+  unsigned* done;         // CTA counter of the last kernel (finds the CTA that publishes the error word)
+  int* err_host;          // device view of a pinned host word: the call's error bits are OR-ed into it
   // packed weights (device)
   const __nv_bfloat16* tokU;   // [1664][256]
   const float* tok_b;          // [1664]
@@ -330,6 +332,7 @@ inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, 
 // kernel launchers (each returns the launch's error code)
 cudaError_t prepare_gemm_kernels();  // shared-memory attributes; once per device before any launch
 cudaError_t prepare_mlp_kernels();
+cudaError_t prepare_attention_kernel();
 cudaError_t launch_sparse(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_seq_colsum(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_request_side(const FwdArgs& a, cudaStream_t s);

@@ -321,6 +321,20 @@ __global__ void __launch_bounds__(kThreads, 1) heads_kernel(const __grid_constan
     tc_fence_after();
     tmem_dealloc(tbase, 128);
   }
+  // This is the last kernel of a call: every earlier kernel has completed (programmatic dependencies chain),
+  // so the last of its CTAs to finish publishes the call's error bits to the host word and resets the
+  // device word for the next call.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.done, 1u) == gridDim.x * gridDim.y - 1) {
+      __threadfence();
+      const int e = atomicExch(a.err, 0);
+      volatile int* hw = a.err_host;
+      *hw = *hw | e;
+      atomicExch(a.done, 0u);
+      __threadfence_system();
+    }
+  }
 }
 
 template <int BN, int STAGES, int EPI, int NEPI>
@@ -338,8 +352,8 @@ cudaError_t launch_gemm(const FwdArgs& a, const CUtensorMap& tmA, const CUtensor
                        s, a.pdl != 0, a, tmA, tmB, M, N, K, layer);
 }
 
-constexpr int kTokBN = 128, kTokStages = 4, kTokEpi = 4;
-constexpr int kQryBN = 96, kQryStages = 6, kQryEpi = 4;
+constexpr int kTokBN = 128, kTokStages = 4, kTokEpi = 8;
+constexpr int kQryBN = 96, kQryStages = 6, kQryEpi = 8;
 constexpr int kPleBN = 208, kPleStages = 5, kPleEpi = 8;
 static_assert(kPleCols % kPleBN == 0, "PLE columns are a whole number of tiles");
 

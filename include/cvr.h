@@ -125,6 +125,17 @@ cvr_status cvr_create(const cvr_weights* weights, const cvr_config* cfg, void* c
 cvr_status cvr_score(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids, const int64_t* bag_ids,
                      const int64_t* bag_offsets, const int64_t* seq_ids, float* out);
 
+/* As cvr_score, but only enqueues the work on the handle's stream and returns CVR_OK (or a host-side
+ * error: CVR_E_ARG / CVR_E_SHAPE / CVR_E_OOM / CVR_E_CUDA) without waiting. The input and output buffers
+ * must stay valid until cvr_sync returns. Several calls may be in flight; their device-side error bits
+ * accumulate until the next cvr_sync. */
+cvr_status cvr_score_async(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids,
+                           const int64_t* bag_ids, const int64_t* bag_offsets, const int64_t* seq_ids, float* out);
+
+/* Waits for every call enqueued on the handle's stream and returns the status of the device-side checks
+ * of all calls since the previous cvr_sync (CVR_E_ID_RANGE, CVR_E_INPUT, CVR_E_TIMEOUT) or CVR_E_CUDA. */
+cvr_status cvr_sync(cvr_handle* h);
+
 /* As cvr_score, and also writes the exact pooled embeddings and the rows read (DEVICE pointers, each
  * may be NULL): pooled_fp32 [n_req*8 + n_cand*8][32] -- the clamped fp32 means of every bag, in
  * bag_offsets order, before the bf16 cast; rows [bag_offsets[last]] -- the row each id read (the id

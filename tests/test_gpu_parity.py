@@ -217,3 +217,27 @@ def test_embheavy_sampled():
 @pytest.mark.parametrize("c", [64, 512, 2048])
 def test_deep_sampled(c):
     _full("deep", requests=[0, 31] if c < 2048 else [5], n_cand=c)
+
+
+def test_async_calls_match_sync_and_report_errors():
+    wl = synth.make_workload("tiny", n_req=3, n_cand=20)
+    w = synth.make_weights(wl.n_layers, wl.seed)
+    g = GpuRun(wl, w, debug=False)
+    g.run()
+    ref = g.out()
+    r, b, o, s, out = g.dw.ptrs()
+    g.dw.out.zero_()
+    for _ in range(3):
+        g.sc.score_async(wl.n_req, wl.n_cand, r, b, o, s, out)
+    assert g.sc.sync(check=False) == 0
+    assert np.array_equal(g.out(), ref)
+    # a bad id in one of several in-flight calls is reported by the next sync, then cleared
+    import torch
+    bad = g.dw.bag_ids.clone()
+    bad[3] = 10 ** 10
+    g.sc.score_async(wl.n_req, wl.n_cand, r, bad.data_ptr(), o, s, out)
+    g.sc.score_async(wl.n_req, wl.n_cand, r, b, o, s, out)
+    assert g.sc.sync(check=False) == 3
+    g.sc.score_async(wl.n_req, wl.n_cand, r, b, o, s, out)
+    assert g.sc.sync(check=False) == 0
+    torch.cuda.synchronize()
