@@ -17,6 +17,7 @@ from . import _build
 MAX_LAYERS, N_USER_FIELDS, N_ITEM_FIELDS, N_GROUPS, N_EXPERTS, N_TASKS = 4, 8, 8, 3, 3, 2
 STAGE_H, STAGE_Z, STAGE_Q, STAGE_Y, STAGE_EXPERTS, STAGE_GATES = range(6)
 OPT_PROFILE, OPT_CUDA_GRAPH, OPT_PDL = 0, 1, 2
+NOALLOC_MAX_CAND = 1024  # CVR_NOALLOC_MAX_CAND
 
 STATUS = {0: "CVR_OK", 1: "CVR_E_ARG", 2: "CVR_E_SHAPE", 3: "CVR_E_ID_RANGE", 4: "CVR_E_OOM", 5: "CVR_E_CUDA",
           6: "CVR_E_INPUT", 7: "CVR_E_TIMEOUT"}
@@ -85,6 +86,8 @@ def lib() -> ctypes.CDLL:
         L.cvr_last_error.restype = ctypes.c_char_p
         L.cvr_status_string.argtypes = [ctypes.c_int]
         L.cvr_status_string.restype = ctypes.c_char_p
+        L.cvr_predict_noalloc.argtypes = [V, i32, V, V]
+        L.cvr_predict_noalloc.restype = ctypes.c_int
         L.cvr_destroy.argtypes = [V]
         L.cvr_destroy.restype = None
         _lib = L
@@ -193,6 +196,14 @@ class Scorer:
             assert a.dtype == dt and a.flags["C_CONTIGUOUS"], "host arrays must be C-contiguous with the C ABI dtypes"
         st = self._lib.cvr_score_host(self._h, n_req, n_cand, req_ids.ctypes.data, bag_ids.ctypes.data,
                                       bag_ids.size, bag_offsets.ctypes.data, seq_ids.ctypes.data, out.ctypes.data)
+        if check:
+            self._check(st)
+        return st
+
+    def predict_noalloc(self, n_cand: int, y: int, out: int, check: bool = True) -> int:
+        """cvr_predict_noalloc: PLE + heads on a device bf16 [n_cand][16][128] Token Mixer output, with
+        no device allocation (n_cand <= NOALLOC_MAX_CAND)."""
+        st = self._lib.cvr_predict_noalloc(self._h, n_cand, y, out)
         if check:
             self._check(st)
         return st

@@ -10,6 +10,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -823,6 +824,81 @@ void cvr_destroy(cvr_handle* h) {
   for (auto ev : h->events) cudaEventDestroy(ev);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   delete h;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------------------------------
+// Prediction step without allocation: the PLE expert GEMM and the heads kernel on a caller's Token
+// Mixer output, their intermediates (expert outputs, gates) and the error word in one fixed
+// file-scope device array instead of the handle's growable workspace.
+namespace {
+
+constexpr int kNoAllocMaxCand = CVR_NOALLOC_MAX_CAND;
+constexpr size_t kNaGatesOff = (size_t)kNoAllocMaxCand * kPleN * 2;       // expert outputs, bf16 [n][768]
+constexpr size_t kNaErrOff = kNaGatesOff + (size_t)kNoAllocMaxCand * 8 * 4;  // gates, fp32 [n][8]
+constexpr size_t kNaBytes = kNaErrOff + 512;                                 // error word (+0), CTA counter (+256)
+constexpr int kNaMaxDevices = 64;
+
+std::mutex g_na_mu;
+uint8_t* g_na_addr[kNaMaxDevices] = {};
+
+}  // namespace
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNaBytes];
+
+namespace {
+
+// Device address of the scratch array, looked up once per device.
+cvr_status noalloc_scratch(cvr_handle* h, uint8_t** p) {
+  std::lock_guard<std::mutex> lock(g_na_mu);
+  if (h->device < 0 || h->device >= kNaMaxDevices) return fail(h, CVR_E_ARG, "device index out of range");
+  if (!g_na_addr[h->device]) {
+    void* addr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaGetSymbolAddress of the prediction scratch");
+    g_na_addr[h->device] = static_cast<uint8_t*>(addr);
+  }
+  *p = g_na_addr[h->device];
+  return CVR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+cvr_status cvr_predict_noalloc(cvr_handle* h, int32_t n_cand, const void* y, float* out) {
+  if (!h) return CVR_E_ARG;
+  if (!y || !out) return fail(h, CVR_E_ARG, "null Y or output pointer");
+  if (n_cand < 0 || n_cand > kNoAllocMaxCand)
+    return fail(h, CVR_E_SHAPE, "cvr_predict_noalloc takes 0 <= n_cand <= " + std::to_string(kNoAllocMaxCand) +
+                                    " (its scratch is a fixed device array); got " + std::to_string(n_cand));
+  if (reinterpret_cast<uintptr_t>(y) % 16 != 0) return fail(h, CVR_E_ARG, "Y must be 16-byte aligned");
+  int cur = -1;
+  cudaError_t ce = cudaGetDevice(&cur);
+  if (ce == cudaSuccess && cur != h->device) ce = cudaSetDevice(h->device);
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaSetDevice");
+  uint8_t* sc = nullptr;
+  cvr_status st = noalloc_scratch(h, &sc);
+  if (st != CVR_OK) return st;
+  if (n_cand == 0) return CVR_OK;
+  CUtensorMap tmY;
+  if (!encode_2d(&tmY, y, kYD, (uint64_t)n_cand, kYD, 64, 128))
+    return fail(h, CVR_E_CUDA, "cuTensorMapEncodeTiled failed for Y");
+  FwdArgs a = make_args(h, 1, n_cand, nullptr, nullptr, nullptr, nullptr, out, nullptr, nullptr);
+  // nothing but the two prediction kernels' own buffers is reachable from these arguments
+  a.U = a.I = a.Xs = a.H = a.Z = a.Y = a.Q = nullptr;
+  a.colsum = a.xu = a.qb = nullptr;
+  a.Ex = reinterpret_cast<bf16*>(sc);
+  a.gates = reinterpret_cast<float*>(sc + kNaGatesOff);
+  a.err = reinterpret_cast<int*>(sc + kNaErrOff);
+  a.done = reinterpret_cast<unsigned*>(sc + kNaErrOff + 256);
+  cudaStream_t s = h->stream;
+  ce = cudaMemsetAsync(sc + kNaErrOff, 0, 512, s);  // the error word and the CTA counter start at zero
+  if (ce == cudaSuccess) ce = launch_ple(a, tmY, h->tm_pleW, s);
+  if (ce == cudaSuccess) ce = launch_heads(a, h->tm_headW1, s);
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "prediction kernels");
+  return sync_status(h);
 }
 
 }  // extern "C"

@@ -181,6 +181,23 @@ int32_t cvr_last_launch_count(const cvr_handle* h);
 const char* cvr_last_error(const cvr_handle* h);
 const char* cvr_status_string(cvr_status s);
 
+/* The prediction step alone -- PLE experts and gates, task towers and sigmoid -- on a caller's Token Mixer
+ * output, without allocating device memory. The papers have no counterpart: it serves callers that
+ * cannot allocate mid-flight (a serving loop whose device memory is all pre-reserved by its own pool, or
+ * one that cannot afford the device-wide synchronisation of cudaMalloc / cudaFree that a growing
+ * cvr_score workspace would cost). Its intermediates (expert outputs, gates, error word) live in one
+ * fixed device array of CVR_NOALLOC_MAX_CAND x 1,568 + 512 bytes (1.6 MB) inside this library.
+ *   y    DEVICE bf16 [n_cand][16][128]: the last Token Mixer's output (the layout of CVR_STAGE_Y), 16-byte
+ *        aligned; read only.
+ *   out  DEVICE fp32 [n_cand][2]: pCVR per task, written by the call (caller-owned).
+ * 0 <= n_cand <= CVR_NOALLOC_MAX_CAND (0 does nothing); larger batches return CVR_E_SHAPE. Runs on the
+ * handle's stream and waits for it, returning CVR_E_TIMEOUT / CVR_E_CUDA like cvr_score.
+ * The first call on a device looks up the array's address (setup: make it before any stream capture).
+ * The array is shared by every handle of the process on that device: calls whose execution overlaps
+ * (on two streams, two handles or two threads) race on it. */
+#define CVR_NOALLOC_MAX_CAND 1024
+cvr_status cvr_predict_noalloc(cvr_handle* h, int32_t n_cand, const void* y, float* out);
+
 /* Frees the handle's device memory, graphs and events. NULL is ignored. */
 void cvr_destroy(cvr_handle* h);
 
