@@ -69,6 +69,56 @@ def algorithmic_work(wl, nnz: int):
     return flops, total_bytes, sparse_bytes
 
 
+def source_digest(rel_path: str) -> str:
+    import hashlib
+    p = os.path.join(ROOT, rel_path)
+    if not os.path.exists(p):
+        return ""
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------------------------
+# multi-rank host logic (one process per GPU; every rank scores its own batch, no data-path collective)
+def workload_for_rank(cfg_name: str, rank: int, **over):
+    """Rank 0 scores the configuration's own batch; rank r > 0 an independent batch of the same shape
+    (the configuration's seed + 7919 r)."""
+    import synth
+    if rank == 0:
+        return synth.make_workload(cfg_name, **over)
+    return synth.make_workload(cfg_name, seed=synth.default_seed(cfg_name) + 7919 * rank, **over)
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    import torch
+    on = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=on)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, batch: int, steps: int, total_ms: float) -> float:
+    """Candidates per second of the whole job: every rank's batches over the slowest rank's time."""
+    return world * batch * steps / (total_ms / 1e3)
+
+
+def measured_traffic(config: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when there is none for this kernel
+    and workload or the kernel's source has changed since the counters were taken."""
+    tr = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(tr):
+        return None
+    with open(tr) as f:
+        ent = json.load(f).get(f"{config}:{kernel}")
+    if ent and source_digest(ent["source"]) == ent["source_sha256_16"]:
+        return ent["bytes_per_launch"]
+    return None
+
+
 # ---------------------------------------------------------------------------------------------
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
@@ -86,15 +136,18 @@ class ClockSampler:
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu=timestamp,{self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
         time.sleep(0.3)
+        self.t0 = time.time()
         return self
 
     def __exit__(self, *exc):
+        self.t1 = time.time()
+        time.sleep(0.1)
         if self.proc:
             self.proc.terminate()
             try:
@@ -103,46 +156,53 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        """Median SM clock and the throttle reasons seen among the samples taken inside the timed region
+        (all samples if none falls inside it)."""
+        from datetime import datetime
         if not self.proc or not self.path or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
+        rows, inside = [], []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                row = (float(parts[2]), float(parts[3]), parts[6:10])
+                ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
             except ValueError:
                 continue
+            rows.append(row)
+            if self.t0 <= ts <= self.t1:
+                inside.append(row)
         os.unlink(self.path)
-        if not rows:
+        use = inside or rows
+        if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        reasons = sorted({names[i] for _, _, r in use for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in use), "sm_max_mhz": max(r[1] for r in use),
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside),
+                "timed_region_s": round(self.t1 - self.t0, 3)}
 
 
 # ---------------------------------------------------------------------------------------------
-def oracle_baseline(cfg_name: str, budget_s: float = 15.0):
-    """The CPU oracle, as it stands, on a bounded sample of the workload: candidates of one request."""
+def oracle_baseline(cfg_name: str, budget_s: float = 10.0):
+    """The CPU oracle, as it stands, on a bounded sample of the workload: the benchmark's own batch,
+    scored again until about budget_s seconds of CPU work have been spent."""
     import oracle
     import synth
     threads = oracle.threads_used(0)
-    n = 16
-    t = 0.0
-    while True:
-        wl = synth.make_workload(cfg_name, n_req=1, n_cand=n)
-        w = synth.make_weights(wl.n_layers, wl.seed)
+    wl = synth.make_workload(cfg_name)
+    w = synth.make_weights(wl.n_layers, wl.seed)
+    reps, t = 0, 0.0
+    while t < budget_s and reps < 100:
         t0 = time.perf_counter()
         oracle.score(wl, w)
-        t = time.perf_counter() - t0
-        if t * 2 > budget_s or n >= 4096:
-            break
-        n = min(4096, n * max(2, int(budget_s / max(t, 1e-3) / 2)))
-    return {"value": n / t, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{cfg_name} shapes, 1 request x {n} candidates (fp64 loop-nest oracle, OpenMP over "
-                      f"candidates), {t:.1f} s wall"}
+        t += time.perf_counter() - t0
+        reps += 1
+    return {"value": reps * wl.n_cand / t, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"the {cfg_name} batch ({wl.n_req} requests x {wl.n_cand // wl.n_req} candidates) scored "
+                      f"{reps} times by the fp64 loop-nest oracle (OpenMP over candidates), {t:.1f} s wall"}
 
 
 def run_reference(args):
@@ -187,7 +247,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="prod", choices=["tiny", "prod", "longseq", "embheavy", "deep"])
     ap.add_argument("--n-cand", type=int, default=None, help="candidates per request (deep sweep)")
@@ -216,8 +276,8 @@ def main():
     dev = f"cuda:{local}"
     stream = torch.cuda.Stream(device=dev)
 
-    wl = synth.make_workload(args.config, n_cand=args.n_cand)
-    w = synth.make_weights(wl.n_layers, wl.seed)
+    wl = workload_for_rank(args.config, rank, n_cand=args.n_cand)
+    w = synth.make_weights(wl.n_layers, synth.default_seed(args.config))  # one model, every replica
     with torch.cuda.stream(stream):
         dw = DeviceWorkload(wl, device=dev)
     torch.cuda.synchronize(dev)
@@ -236,7 +296,7 @@ def main():
             step()
     torch.cuda.synchronize(dev)
 
-    def timed_region(profile: bool):
+    def timed_region(profile: bool, n_steps: int):
         """K steps, L2 flushed before each, each step bracketed by CUDA events on the scorer's stream.
 
         Without profiling the steps are enqueued back to back through cvr_score_async (the host runs ahead;
@@ -248,14 +308,14 @@ def main():
             for _ in range(3):
                 flush.zero_()
                 step()
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
         stages, n_launch = {}, 0
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
         with torch.cuda.stream(stream):
-            for i in range(args.steps):
+            for i in range(n_steps):
                 flush.zero_()
                 starts[i].record(stream)
                 if profile:
@@ -271,18 +331,16 @@ def main():
         torch.cuda.synchronize(dev)
         if world > 1:
             dist.barrier()
-        return [starts[i].elapsed_time(ends[i]) for i in range(args.steps)], stages, n_launch
+        return [starts[i].elapsed_time(ends[i]) for i in range(n_steps)], stages, n_launch
 
     # timed region: the scoring calls alone (no per-kernel events inside the graph)
     with ClockSampler(local) as clocks:
-        step_ms, _, launches = timed_region(profile=False)
+        step_ms, _, launches = timed_region(profile=False, n_steps=args.steps)
     total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     # second timed region, same steps, with an event recorded after every kernel: per-kernel durations
-    prof_ms, stage_sum, _ = timed_region(profile=True)
+    n_prof = min(args.steps, 1000)
+    prof_ms, stage_sum, _ = timed_region(profile=True, n_steps=n_prof)
     # latency of the synchronous call as a caller sees it (host wall clock, L2 flushed before each call)
     call_ms = []
     with torch.cuda.stream(stream):
@@ -292,13 +350,13 @@ def main():
             t0 = time.perf_counter()
             step()
             call_ms.append((time.perf_counter() - t0) * 1e3)
-    value = world * B * args.steps / (total_ms / 1e3)
+    value = job_throughput(world, B, args.steps, total_ms)
 
     # per-kernel times (events recorded between the kernels, on the scorer's stream, every timed step)
     per_kernel = {}
     for name, lst in stage_sum.items():
         # a name repeats once per layer; stage_list already returns every launch -> group per step
-        per_kernel[name] = sum(lst) / args.steps
+        per_kernel[name] = sum(lst) / n_prof
     nnz = int(wl.bag_offsets[-1])
     flops, total_bytes, sparse_bytes = algorithmic_work(wl, nnz)
     peaks, peak_src = load_peaks()
@@ -316,18 +374,13 @@ def main():
                     "frac": ach / peak_tf, "traffic": None,
                     "peak_source": f"{peak_src} bf16 dense burst (cuBLAS)",
                     "flop_per_launch": flops[dom] / n_l, "launch_ms": avg_launch_ms}
-        tr = os.path.join(ROOT, "profiles", "traffic.json")
-        if os.path.exists(tr):
-            with open(tr) as f:
-                td = json.load(f)
-            ent = td.get(f"{args.config}:{dom}")
-            if ent and ent.get("valid", True):
-                roofline["traffic"] = ent["bytes_per_launch"]
+        roofline["traffic"] = measured_traffic(args.config, dom)
     sparse = None
     if "sparse" in per_kernel:
         gbs = sparse_bytes / (per_kernel["sparse"] / 1e3) / 1e9
         sparse = {"kernel": "sparse", "bound": "hbm", "achieved": gbs, "peak": peak_bw, "unit": "GB/s",
-                  "frac": gbs / peak_bw, "bytes_per_launch": sparse_bytes}
+                  "frac": gbs / peak_bw, "bytes_per_launch": sparse_bytes,
+                  "traffic": measured_traffic(args.config, "sparse")}
     p50 = statistics.median(step_ms)
     p99 = float(np.percentile(step_ms, 99))
     total_flop = sum(flops.values())
@@ -358,11 +411,8 @@ def main():
                 e_ms.append(ev0.elapsed_time(ev1))
         h2d = h_req.nbytes + h_ids.nbytes + h_off.nbytes + h_seq.nbytes
         e_tot = sum(e_ms)
-        if world > 1:
-            t = torch.tensor([e_tot], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_tot = float(t.item())
-        e2e = {"value": world * B * args.steps / (e_tot / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        e_tot = max_over_ranks(e_tot, dev)
+        e2e = {"value": job_throughput(world, B, args.steps, e_tot), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(h_out.nbytes), "p50_ms": statistics.median(e_ms),
                "api": "cvr_score_host (pinned host buffers)"}
 

@@ -142,6 +142,11 @@ class Workload:
         return out
 
 
+def default_seed(name: str) -> int:
+    """Seed of a named workload's inputs and weights."""
+    return 0xC0FFEE + CONFIGS[name]["index"]
+
+
 def make_workload(name: str, n_req: Optional[int] = None, n_cand: Optional[int] = None,
                   cand_per_req: Optional[Sequence[int]] = None, seq_len: Optional[Sequence[int]] = None,
                   seed: Optional[int] = None, table_scale: float = TABLE_SCALE, **over) -> Workload:
@@ -157,7 +162,7 @@ def make_workload(name: str, n_req: Optional[int] = None, n_cand: Optional[int] 
     assert len(cpr) == R
     B = int(cpr.sum())
     L = tuple(int(x) for x in (seq_len if seq_len is not None else c["seq_len"]))
-    sd = int(seed if seed is not None else 0xC0FFEE + c["index"])
+    sd = int(seed if seed is not None else default_seed(name))
     Fu, Fi = DIMS["n_user_fields"], DIMS["n_item_fields"]
     n_bags = R * Fu + B * Fi
     field = np.empty(n_bags, dtype=np.int32)
