@@ -658,10 +658,10 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
   h->head_b1 = wf + f_hb1;
   h->head_w2 = wf + f_hw2;
   h->head_b2 = wf + f_hb2;
-  ok = encode_2d(&h->tm_seqW13, h->seqW13, kD, kG * 512, kD, 64, 128) &&
+  ok = encode_2d(&h->tm_seqW13, h->seqW13, kD, kG * 512, kD, 64, 256) &&
        encode_2d(&h->tm_seqW2, h->seqW2, kHid, kG * kD, kHid, 64, 128) &&
        encode_2d(&h->tm_tokI, h->tokI, kID, kXD, kID, 64, 128) &&
-       encode_2d(&h->tm_tmW13, h->tmW13, kD, (uint64_t)NL * 512, kD, 64, 128) &&
+       encode_2d(&h->tm_tmW13, h->tmW13, kD, (uint64_t)NL * 512, kD, 64, 256) &&
        encode_2d(&h->tm_tmW2, h->tmW2, kHid, (uint64_t)NL * kD, kHid, 64, 128) &&
        encode_2d(&h->tm_pleW, h->pleW, kYD, kPleCols, kYD, 64, 208) &&
        encode_2d(&h->tm_headW1, h->headW1, kDE, kNT * kHH, kDE, 64, 128);
