@@ -46,14 +46,21 @@ uint16_t f32_to_bf16_bits(float x) {
   return (uint16_t)(u >> 16);
 }
 
+float bf16_round(float x) {
+  const uint32_t u = (uint32_t)f32_to_bf16_bits(x) << 16;
+  float r;
+  std::memcpy(&r, &u, 4);
+  return r;
+}
+
 struct GraphEntry {
   cudaGraphExec_t exec = nullptr;
   std::vector<const void*> key;
   int launches = 0;
 };
 
-const char* kStageNames[] = {"sparse", "seq_mlp", "seq_colsum", "request_side", "tokenizer", "query", "attention",
-                             "token_mixer", "ple", "heads"};
+const char* kStageNames[] = {"sparse", "seq_mlp", "seq_colsum", "tokenizer", "query", "attention", "token_mixer", "ple",
+                             "heads"};
 
 }  // namespace
 
@@ -81,6 +88,7 @@ struct cvr_handle {
   float *colsum = nullptr, *xu = nullptr, *qb = nullptr, *gates = nullptr;
   int* err = nullptr;
   unsigned* done = nullptr;
+  unsigned* cs_count = nullptr;
   int* err_host = nullptr;      // pinned, mapped: the call's error bits
   int* err_host_dev = nullptr;  // its device address
   // host-input staging
@@ -224,11 +232,11 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   };
   const size_t oU = take((size_t)R_cap * kUD * 2), oI = take((size_t)B_cap * kID * 2);
   const size_t oXs = take((size_t)seq_rows * kD * 2), oH = take((size_t)seq_rows * kD * 2);
-  const size_t oCs = take((size_t)R_cap * kG * max_chunks * kD * 4), oXu = take((size_t)R_cap * kXD * 4);
+  const size_t oCs = take((size_t)R_cap * kG * max_chunks * kD * 4), oXu = take((size_t)R_cap * kTokN * 4);
   const size_t oQb = take((size_t)h->n_layers * R_cap * kG * kD * 4);
   const size_t oZ = take((size_t)B_cap * kYD * 2), oY = take((size_t)B_cap * kYD * 2);
   const size_t oQ = take((size_t)B_cap * kG * kD * 2), oEx = take((size_t)B_cap * kPleN * 2);
-  const size_t oG = take((size_t)B_cap * 8 * 4), oErr = take(1024);
+  const size_t oG = take((size_t)B_cap * 8 * 4), oErr = take(1024), oCnt = take((size_t)R_cap * kG * 4);
   cudaError_t e = cudaMalloc(&h->ws, off);
   if (e != cudaSuccess) {
     h->ws = nullptr;
@@ -250,7 +258,9 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   h->gates = (float*)(b + oG);
   h->err = (int*)(b + oErr);
   h->done = (unsigned*)(b + oErr + 256);
+  h->cs_count = (unsigned*)(b + oCnt);
   e = cudaMemset(h->err, 0, 1024);  // error word and CTA counter start at zero; the last kernel resets them
+  if (e == cudaSuccess) e = cudaMemset(h->cs_count, 0, (size_t)R_cap * kG * 4);  // reset by their last block
   if (e != cudaSuccess) {
     free_workspace(h);
     return fail(h, CVR_E_CUDA, "workspace initialisation failed");
@@ -307,6 +317,7 @@ FwdArgs make_args(cvr_handle* h, int R, int B, const int32_t* req_ids, const int
   a.Xs = h->Xs;
   a.H = h->H;
   a.colsum = h->colsum;
+  a.cs_count = h->cs_count;
   a.max_chunks = h->max_chunks;
   a.xu = h->xu;
   a.qb = h->qb;
@@ -361,19 +372,19 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
   for (int g = 0; g < kG; ++g) seq_tiles += (int)(((int64_t)a.R * a.L[g] + 127) / 128);
   run(launch_seq_mlp(a, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, s), kStageNames[1]);
   run(launch_seq_colsum(a, s), kStageNames[2]);
-  run(launch_request_side(a, s), kStageNames[3]);
-  run(launch_tokenizer(a, h->tm_I, h->tm_tokI, s), kStageNames[4]);
+  run(launch_tokenizer(a, h->tm_I, h->tm_tokI, s), kStageNames[3]);
   bf16* zin = h->Z;
   bf16* zout = h->Y;
   for (int l = 0; l < a.n_layers; ++l) {
     if (l > 0) std::swap(zin, zout);  // layer l reads the previous output (its first 13 tokens) in place
     const bool in_is_Z = zin == h->Z;
-    run(launch_query(a, l, in_is_Z ? h->tm_x_Z : h->tm_x_Y, h->tm_qW[l], s), kStageNames[5]);
-    run(launch_attention(a, zin, s), kStageNames[6]);
-    run(launch_tm_mlp(a, l, zin, zout, in_is_Z ? h->tm_5_Z : h->tm_5_Y, h->tm_tmW13, h->tm_tmW2, s), kStageNames[7]);
+    // the first layer's queries come out of the tokeniser
+    if (l > 0) run(launch_query(a, l, in_is_Z ? h->tm_x_Z : h->tm_x_Y, h->tm_qW[l], s), kStageNames[4]);
+    run(launch_attention(a, zin, s), kStageNames[5]);
+    run(launch_tm_mlp(a, l, zin, zout, in_is_Z ? h->tm_5_Z : h->tm_5_Y, h->tm_tmW13, h->tm_tmW2, s), kStageNames[6]);
   }
-  run(launch_ple(a, zout == h->Z ? h->tm_full_Z : h->tm_full_Y, h->tm_pleW, s), kStageNames[8]);
-  run(launch_heads(a, h->tm_headW1, s), kStageNames[9]);
+  run(launch_ple(a, zout == h->Z ? h->tm_full_Z : h->tm_full_Y, h->tm_pleW, s), kStageNames[7]);
+  run(launch_heads(a, h->tm_headW1, s), kStageNames[8]);
   h->last_zin = zin;
   h->last_zout = zout;
   if (launches) *launches = n;
@@ -558,12 +569,12 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
 
   // ---- pack dense weights ----
   Packer P;
-  const size_t o_tokI = P.add_bf((size_t)kXD * kID), o_tokU = P.add_bf((size_t)kXD * kUD);
+  const size_t o_tokI = P.add_bf((size_t)kTokN * kID), o_tokU = P.add_bf((size_t)kTokN * kUD);
   const size_t o_seqW13 = P.add_bf((size_t)kG * 512 * kD), o_seqW2 = P.add_bf((size_t)kG * kD * kHid);
   const size_t o_qX = P.add_bf((size_t)NL * kG * kD * kXD), o_qm = P.add_bf((size_t)NL * kG * kD * kD);
   const size_t o_tmW13 = P.add_bf((size_t)NL * 512 * kD), o_tmW2 = P.add_bf((size_t)NL * kD * kHid);
   const size_t o_pleW = P.add_bf((size_t)kPleCols * kYD), o_headW1 = P.add_bf((size_t)kNT * kHH * kDE);
-  const size_t f_tok_b = P.add_f(kXD), f_seq_b13 = P.add_f(kG * 512), f_seq_b2 = P.add_f(kG * kD);
+  const size_t f_tok_b = P.add_f(kTokN), f_seq_b13 = P.add_f(kG * 512), f_seq_b2 = P.add_f(kG * kD);
   const size_t f_q_b = P.add_f((size_t)NL * kG * kD), f_tm_b13 = P.add_f((size_t)NL * 512);
   const size_t f_tm_b2 = P.add_f((size_t)NL * kD), f_gain = P.add_f((size_t)NL * kD), f_ple_b = P.add_f(kPleCols + 32);
   const size_t f_hb1 = P.add_f(kNT * kHH), f_hw2 = P.add_f(kNT * kHH), f_hb2 = P.add_f(32);
@@ -576,6 +587,32 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
       B[o_tokI + (size_t)n * kID + k] = f32_to_bf16_bits(w->tok_w[(size_t)n * IN + kUD + k]);
     }
   std::memcpy(F + f_tok_b, w->tok_b, sizeof(float) * kXD);
+  // The first layer's query FFN is linear in the tokens, so its token part folds into the tokeniser:
+  // Wq_x (Wt_u u + Wt_i i + bt) = (Wq_x Wt_u) u + (Wq_x Wt_i) i + Wq_x bt. Rows 1664.. of the packed
+  // tokeniser hold Wq_x Wt (from the bf16 weights, summed in double, rounded once to bf16) and Wq_x bt.
+  {
+    const int QIN0 = kXD + kD;
+    std::vector<double> acc(IN);
+    std::vector<float> wt_bf((size_t)kXD * IN);
+    for (size_t i = 0; i < wt_bf.size(); ++i) wt_bf[i] = bf16_round(w->tok_w[i]);
+    for (int g = 0; g < kG; ++g)
+      for (int n = 0; n < kD; ++n) {
+        const float* qrow = w->q_w[0][g] + (size_t)n * QIN0;
+        std::fill(acc.begin(), acc.end(), 0.0);
+        double bacc = 0.0;
+        for (int c = 0; c < kXD; ++c) {
+          const double qc = bf16_round(qrow[c]);
+          if (qc == 0.0) continue;
+          const float* wrow = wt_bf.data() + (size_t)c * IN;
+          for (int k = 0; k < IN; ++k) acc[k] += qc * wrow[k];
+          bacc += qc * w->tok_b[c];
+        }
+        const size_t row = (size_t)kXD + g * kD + n;
+        for (int k = 0; k < kUD; ++k) B[o_tokU + row * kUD + k] = f32_to_bf16_bits((float)acc[k]);
+        for (int k = 0; k < kID; ++k) B[o_tokI + row * kID + k] = f32_to_bf16_bits((float)acc[kUD + k]);
+        F[f_tok_b + row] = (float)bacc;
+      }
+  }
   for (int g = 0; g < kG; ++g) {
     pack_w13(B + o_seqW13 + (size_t)g * 512 * kD, w->seq_w1[g], w->seq_w3[g], kD);
     for (size_t i = 0; i < (size_t)kD * kHid; ++i) B[o_seqW2 + (size_t)g * kD * kHid + i] = f32_to_bf16_bits(w->seq_w2[g][i]);
@@ -660,7 +697,7 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
   h->head_b2 = wf + f_hb2;
   ok = encode_2d(&h->tm_seqW13, h->seqW13, kD, kG * 512, kD, 64, 256) &&
        encode_2d(&h->tm_seqW2, h->seqW2, kHid, kG * kD, kHid, 64, 128) &&
-       encode_2d(&h->tm_tokI, h->tokI, kID, kXD, kID, 64, 128) &&
+       encode_2d(&h->tm_tokI, h->tokI, kID, kTokN, kID, 64, 128) &&
        encode_2d(&h->tm_tmW13, h->tmW13, kD, (uint64_t)NL * 512, kD, 64, 256) &&
        encode_2d(&h->tm_tmW2, h->tmW2, kHid, (uint64_t)NL * kD, kHid, 64, 128) &&
        encode_2d(&h->tm_pleW, h->pleW, kYD, kPleCols, kYD, 64, 208) &&
@@ -889,6 +926,7 @@ cvr_status cvr_predict_noalloc(cvr_handle* h, int32_t n_cand, const void* y, flo
   // nothing but the two prediction kernels' own buffers is reachable from these arguments
   a.U = a.I = a.Xs = a.H = a.Z = a.Y = a.Q = nullptr;
   a.colsum = a.xu = a.qb = nullptr;
+  a.cs_count = nullptr;
   a.Ex = reinterpret_cast<bf16*>(sc);
   a.gates = reinterpret_cast<float*>(sc + kNaGatesOff);
   a.err = reinterpret_cast<int*>(sc + kNaErrOff);

@@ -22,6 +22,7 @@ constexpr int kG = 3;             // behaviour-sequence groups (= decoded tokens
 constexpr int kT = kN + kG;       // 16 tokens into the Token Mixer
 constexpr int kXD = kN * kD;      // 1664
 constexpr int kYD = kT * kD;      // 2048
+constexpr int kTokN = kXD + kG * kD;  // 2048 tokeniser outputs: the 13 tokens + the first layer's 3 queries
 constexpr int kCols = 4;          // id columns per sequence event
 constexpr int kHid = 256;         // SwiGLU hidden width
 constexpr int kHeads = 4;         // cross-attention heads
@@ -70,6 +71,7 @@ struct FwdArgs {
   __nv_bfloat16* Xs;      // [sum_g R*L_g][128] sequence rows, group-major
   __nv_bfloat16* H;       // same layout: encoded sequence states
   float* colsum;          // [R][G][max_chunks][128] partial column sums of H
+  unsigned* cs_count;     // [R][G] blocks of the column-sum kernel done (zero between calls)
   int max_chunks;
   float* xu;              // [R][1664] user half of the tokeniser (+ bias)
   float* qb;              // [layers][R][384] per-request query term (+ bias)
@@ -349,7 +351,6 @@ cudaError_t prepare_mlp_kernels();
 cudaError_t prepare_attention_kernel();
 cudaError_t launch_sparse(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_seq_colsum(const FwdArgs& a, cudaStream_t s);
-cudaError_t launch_request_side(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_seq_mlp(const FwdArgs& a, const CUtensorMap& tmXs, const CUtensorMap& tmW13,
                            const CUtensorMap& tmW2, int n_tiles, cudaStream_t s);
 cudaError_t launch_tm_mlp(const FwdArgs& a, int layer, const __nv_bfloat16* zin, __nv_bfloat16* yout,

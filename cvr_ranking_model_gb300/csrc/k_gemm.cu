@@ -4,9 +4,13 @@
 //                    shared memory loaded by TMA through a STAGES-deep mbarrier ring; one elected thread
 //                    issues tcgen05.mma into a TMEM accumulator; four epilogue warps drain TMEM with
 //                    tcgen05.ld (one accumulator row per thread) and apply:
-//    EPI_TOKENIZE    Z[:, 0:1664] = bf16(I . Wtok_item^T + xu[request])        (iQIYI 3.2.2; the user half
-//                    xu, bias included, is computed once per request: iQIYI 3.4.5)
-//    EPI_QUERY       Q = bf16(flat(X) . Wq_x^T + qb[request])                   (iQIYI 3.2.3, item 1)
+//    EPI_TOKENIZE    [Z[:, 0:1664] | Q] = bf16(I . [Wtok_item ; Wq_x Wtok_item]^T + [xu | qu + qb][request])
+//                    (iQIYI 3.2.2 and 3.2.3 item 1): the tokens and, since the first layer's query FFN is
+//                    linear in them, that layer's queries, with the query weights folded into the tokeniser
+//                    (Wq_x Wtok precomputed); the per-request terms -- user half of the tokeniser and of
+//                    the folded query, biases, mean-pool term qb -- are computed once per request
+//                    (iQIYI 3.4.5)
+//    EPI_QUERY       Q = bf16(flat(X) . Wq_x^T + qb[request]) for stacked layers (iQIYI 3.2.3, item 1)
 //    EPI_PLE         Ex = bf16(ReLU(Y . We^T + be)); the 6 gate logits of the last tile become per-task
 //                    softmax weights over the 3 experts                          (iQIYI 3.2.4)
 //  heads_kernel      per task t: r_t = sum_k gate_t[k] e_k built in shared memory, ReLU(W1_t r_t + b1)
@@ -142,14 +146,24 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
         float v[32], add[32];
         const int nb = n0 + c * 32;
         if (live) {
-          if (EPI == EPI_TOKENIZE) ldg32(a.xu + (int64_t)req * kXD + nb, add);
+          if (EPI == EPI_TOKENIZE) {
+            ldg32(a.xu + (int64_t)req * kTokN + nb, add);
+            if (nb >= kXD) {  // first-layer query columns: + the mean-pool term of the request
+              float qadd[32];
+              ldg32(a.qb + (int64_t)req * (kG * kD) + (nb - kXD), qadd);
+#pragma unroll
+              for (int x = 0; x < 32; ++x) add[x] += qadd[x];
+            }
+          }
           else if (EPI == EPI_QUERY) ldg32(a.qb + ((int64_t)layer * a.R + req) * (kG * kD) + nb, add);
           else ldg32(a.ple_b + nb, add);
         }
         tmem_ld32(tbase + lane_off + buf * TC + c * 32, v);
         if (!live) continue;
         if (EPI == EPI_TOKENIZE || EPI == EPI_QUERY) {
-          __nv_bfloat16* out = EPI == EPI_TOKENIZE ? a.Z + (int64_t)row * kYD + nb : a.Q + (int64_t)row * (kG * kD) + nb;
+          __nv_bfloat16* out = EPI == EPI_TOKENIZE ? (nb < kXD ? a.Z + (int64_t)row * kYD + nb
+                                                              : a.Q + (int64_t)row * (kG * kD) + (nb - kXD))
+                                                 : a.Q + (int64_t)row * (kG * kD) + nb;
           uint4* dst = reinterpret_cast<uint4*>(out);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -368,7 +382,8 @@ cudaError_t prepare_gemm_kernels() {
 }
 
 cudaError_t launch_tokenizer(const FwdArgs& a, const CUtensorMap& tmI, const CUtensorMap& tmW, cudaStream_t s) {
-  return launch_gemm<kTokBN, kTokStages, EPI_TOKENIZE, kTokEpi>(a, tmI, tmW, a.B, kXD, kID, 0, s);
+  static_assert(kXD % kTokBN == 0 && kTokN % kTokBN == 0, "token and query columns fall in separate tiles");
+  return launch_gemm<kTokBN, kTokStages, EPI_TOKENIZE, kTokEpi>(a, tmI, tmW, a.B, kTokN, kID, 0, s);
 }
 
 cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, const CUtensorMap& tmW, cudaStream_t s) {

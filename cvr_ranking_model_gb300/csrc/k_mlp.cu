@@ -19,6 +19,7 @@
 // chunk keep the single issuing thread ahead of the tensor pipe.
 // TMEM: up 256, down 128, hidden 64, mixed activations 64 columns.
 #include "cvr_internal.cuh"
+#include "request_gemv.cuh"
 
 namespace cvr {
 
@@ -81,8 +82,13 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     swiglu_mlp_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmW13, const __grid_constant__ CUtensorMap tmW2, int layer,
-                      int n_tiles, const __nv_bfloat16* __restrict__ zin, __nv_bfloat16* __restrict__ yout) {
+                      int n_tiles, int n_cta, const __nv_bfloat16* __restrict__ zin, __nv_bfloat16* __restrict__ yout) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  if (MODE == MODE_SEQ && (int)blockIdx.x >= n_cta) {  // CTAs past the encoder tiles: the user-side GEMV
+    pdl_trigger();
+    xu_block(a, (int)blockIdx.x - n_cta, smem);
+    return;
+  }
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) atomicOr(a.err, kErrLayout);
     return;
@@ -130,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tslot;
   pdl_trigger();
-  const int n_my = blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int n_my = (int)blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / n_cta + 1 : 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -139,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int w_group = -1, w_loads = 0;
     bool waited = false;
     for (int i = 0; i < (MODE == MODE_TM ? (n_my > 0 ? 1 : 0) : n_my); ++i) {
-      const TileInfo ti = tile_info<MODE>(a, blockIdx.x + i * gridDim.x);
+      const TileInfo ti = tile_info<MODE>(a, blockIdx.x + i * n_cta);
       if (ti.g != w_group) {  // (TM: once)
         if (w_loads > 0 && !mbar_wait(w_empty, (w_loads - 1) & 1, abort_flag, a.err)) break;
         const int wsel = MODE == MODE_SEQ ? ti.g : layer;
@@ -177,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_up = [&](int cc) -> bool {
       const int i = cc / kChunks, c = cc % kChunks;
       if (c == 0) {
-        const int g = tile_info<MODE>(a, blockIdx.x + i * gridDim.x).g;
+        const int g = tile_info<MODE>(a, blockIdx.x + i * n_cta).g;
         if (g != w_group) {
           if (!mbar_wait(w_full, w_loads & 1, abort_flag, a.err)) return false;
           w_group = g;
@@ -223,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c == kChunks - 1) {
           tc_commit(dn_full);
           // the weights may be replaced once this tile's MMAs are done, if the next tile needs another group
-          const int tile = blockIdx.x + i * gridDim.x, next = tile + gridDim.x;
+          const int tile = blockIdx.x + i * n_cta, next = tile + n_cta;
           if (MODE == MODE_SEQ && next < n_tiles && tile_info<MODE>(a, next).g != tile_info<MODE>(a, tile).g)
             tc_commit(w_empty);
         }
@@ -237,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a sequence tile of another group needs the weights reloaded, which needs every MMA of the previous
         // tile done: issue the pending down projection first
         const bool reload = MODE == MODE_SEQ && k % kChunks == 0 &&
-                            tile_info<MODE>(a, blockIdx.x + (k / kChunks) * gridDim.x).g !=
-                                tile_info<MODE>(a, blockIdx.x + (k / kChunks - 1) * gridDim.x).g;
+                            tile_info<MODE>(a, blockIdx.x + (k / kChunks) * n_cta).g !=
+                                tile_info<MODE>(a, blockIdx.x + (k / kChunks - 1) * n_cta).g;
         if (reload) {
           ok = issue_down(k - 1) && issue_up(k);
           continue;
@@ -352,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // output epilogue of tile i: columns [32 grp, 32 grp + 32) of the down accumulator
     auto finish = [&](int i) -> bool {
-      const TileInfo ti = tile_info<MODE>(a, blockIdx.x + i * gridDim.x);
+      const TileInfo ti = tile_info<MODE>(a, blockIdx.x + i * n_cta);
       if (!mbar_wait(dn_full, i & 1, abort_flag, a.err)) return false;
       tc_fence_after();
       uint32_t rv[32];
@@ -442,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // finishes each tile before the next).
     constexpr bool kDefer = MODE == MODE_TM;
     for (int i = 0; i < n_my && ok; ++i) {
-      const TileInfo ti = tile_info<MODE>(a, blockIdx.x + i * gridDim.x);
+      const TileInfo ti = tile_info<MODE>(a, blockIdx.x + i * n_cta);
       if (ti.g != bias_group) {  // stage this group's biases (TM: once)
         if (bias_group >= 0) epi_sync();
         const int wsel = MODE == MODE_SEQ ? ti.g : layer;
@@ -455,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bias_group = ti.g;
       }
       const bool has_next = i + 1 < n_my;
-      if (MODE == MODE_TM && has_next) load_z(znext, blockIdx.x + (i + 1) * gridDim.x);
+      if (MODE == MODE_TM && has_next) load_z(znext, blockIdx.x + (i + 1) * n_cta);
       ok = chunk(i, 0, has_next);
       if (ok && kDefer && i >= 1) ok = finish(i - 1);
       if (ok) ok = chunk(i, 1, has_next);
@@ -483,8 +489,9 @@ cudaError_t prepare_mlp_kernels() {
 cudaError_t launch_seq_mlp(const FwdArgs& a, const CUtensorMap& tmXs, const CUtensorMap& tmW13, const CUtensorMap& tmW2,
                            int n_tiles, cudaStream_t s) {
   const int grid = n_tiles < a.num_sms ? n_tiles : a.num_sms;
-  return launch_kernel(swiglu_mlp_kernel<MODE_SEQ>, dim3(grid), dim3(kThreads), kSmemBytes, s, a.pdl != 0, a, tmXs,
-                       tmW13, tmW2, 0, n_tiles, (const __nv_bfloat16*)nullptr, (__nv_bfloat16*)nullptr);
+  static_assert(kXuSmemBytes <= kSmemBytes && kXuThreads <= kThreads, "the user-side GEMV fits the CTA");
+  return launch_kernel(swiglu_mlp_kernel<MODE_SEQ>, dim3(grid + kXuBlocks), dim3(kThreads), kSmemBytes, s, a.pdl != 0,
+                       a, tmXs, tmW13, tmW2, 0, n_tiles, grid, (const __nv_bfloat16*)nullptr, (__nv_bfloat16*)nullptr);
 }
 
 cudaError_t launch_tm_mlp(const FwdArgs& a, int layer, const __nv_bfloat16* zin, __nv_bfloat16* yout,
@@ -492,7 +499,7 @@ cudaError_t launch_tm_mlp(const FwdArgs& a, int layer, const __nv_bfloat16* zin,
   const int n_tiles = (a.B + 7) / 8;  // 8 candidates x 16 mixed rows per tile
   const int grid = n_tiles < a.num_sms ? n_tiles : a.num_sms;
   return launch_kernel(swiglu_mlp_kernel<MODE_TM>, dim3(grid), dim3(kThreads), kSmemBytes, s, a.pdl != 0, a, tmZ, tmW13,
-                       tmW2, layer, n_tiles, zin, yout);
+                       tmW2, layer, n_tiles, grid, zin, yout);
 }
 
 }  // namespace cvr

@@ -5,10 +5,9 @@
 //                      clamp and bf16 cast after the lookup (GPU CTR inference article, section 三),
 //                      plus the sequence-event gather from the shared id table (iQIYI 3.2.1): one launch
 //                      for every lookup of the batch (iQIYI 3.4.2).
-//  seq_colsum_kernel   partial column sums of the encoded sequences (for the mean-pooled sequence vector
-//                      of Query Decoding, iQIYI 3.2.3).
-//  request_side_kernel the work done once per request: the user half of the tokeniser and the
-//                      mean-pool half of each group's query FFN (the "lazy user repeat" of iQIYI 3.4.5).
+//  seq_colsum_kernel   partial column sums of the encoded sequences; the last block of each (request, group)
+//                      forms the mean-pooled sequence vector and the mean-pool half of that group's query
+//                      FFN, once per request (Query Decoding, iQIYI 3.2.3; the lazy user repeat of 3.4.5).
 #include "cvr_internal.cuh"
 
 namespace cvr {
@@ -145,13 +144,18 @@ __global__ void __launch_bounds__(256) sparse_kernel(const __grid_constant__ Fwd
   }
 }
 
-// Partial column sums of H over chunks of 64 positions; grid (max_chunks, G, R), 128 threads.
+// Partial column sums of H over chunks of 64 positions; grid (max_chunks, G, R), 128 threads. The last
+// block of each (request, group) to finish -- found with a counter, nobody waits -- adds the partials up into
+// the mean-pooled sequence vector m_g (iQIYI 3.2.3, Query Decoding item 1: mean over positions of the encoded
+// states) and computes that group's per-request query term for every layer,
+// qb[l][r][g*128 + n] = q_b[l][g*128 + n] + sum_k Wq[l][g][n][1664 + k] * m_g[k], then resets the counter.
 __global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__ FwdArgs a) {
   const int chunk = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
   const int L = a.L[g];
+  const int chunks = (L + 63) / 64;
   pdl_trigger();
   pdl_wait();
-  if (chunk * 64 >= L) return;
+  if (chunk >= chunks) return;
   const int t = threadIdx.x, cp = t & 63, half = t >> 6;
   const __nv_bfloat16* base = a.H + (a.goff[g] + (int64_t)r * L) * kD;
   const int l_end = min(L, chunk * 64 + 64);
@@ -163,121 +167,42 @@ __global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__
     s1 += __high2float(v);
   }
   __shared__ float part[2][128];
+  __shared__ float m[128];
+  __shared__ int last;
   part[half][2 * cp] = s0;
   part[half][2 * cp + 1] = s1;
   __syncthreads();
-  float* dst = a.colsum + (((int64_t)r * kG + g) * a.max_chunks + chunk) * kD;
-  dst[t] = part[0][t] + part[1][t];
-}
-
-constexpr int kXuCols = 32;                 // tokeniser outputs per block
-constexpr int kXuBlocks = kXD / kXuCols;    // 52
-constexpr int kXuReq = 16;                  // requests staged per pass
-constexpr int kQbReqPerBlock = 8;
-constexpr int kXuWStride = kXuCols + 2;     // bf16 elements per staged k-row
-constexpr int kQbWStride = kD + 2;
-
-// Blocks [0, kXuBlocks): xu[r][n] = tok_b[n] + sum_k Wtok[n][k] * U[r][k] (user half of the tokeniser), for
-// 32 columns n per block: the weight slice is staged transposed in shared memory (conflict-free column
-// reads), the users 16 at a time, and every thread finishes whole dot products (no cross-lane reductions).
-// Blocks after: qb[l][r][g*128+n] = q_b[l][g*128+n] + sum_k Wq[l][g][n][1664+k] * m_g[r][k], m_g the mean
-// over positions of the encoded sequence of group g (from the partial column sums).
-__global__ void __launch_bounds__(256) request_side_kernel(const __grid_constant__ FwdArgs a) {
-  __shared__ __align__(16) unsigned char smem[40 * 1024];
-  const int tid = threadIdx.x;
-  pdl_trigger();
-  pdl_wait();
-  if ((int)blockIdx.x < kXuBlocks) {
-    __nv_bfloat16* w = reinterpret_cast<__nv_bfloat16*>(smem);                     // [256][34]: w[k][nn]
-    float* act = reinterpret_cast<float*>(smem + kUD * kXuWStride * 2);            // [16][256]
-    const int n0 = blockIdx.x * kXuCols;
-    // 32 rows x 256 bf16 = 1024 16-byte vectors: 4 per thread, all loads issued before any store
-    {
-      uint4 raw[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int v = tid + t * 256, nn = v >> 5, k8 = v & 31;
-        raw[t] = __ldg(reinterpret_cast<const uint4*>(a.tokU + (int64_t)(n0 + nn) * kUD) + k8);
-      }
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int v = tid + t * 256, nn = v >> 5, k8 = v & 31;
-        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[t]);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) w[(k8 * 8 + q) * kXuWStride + nn] = e[q];
-      }
-    }
-    const int nn = tid & (kXuCols - 1), rs = tid >> 5;  // 8 request slots per pass
-    const float bias = a.tok_b[n0 + nn];
-    for (int r0 = 0; r0 < a.R; r0 += kXuReq) {
-      const int nr = min(kXuReq, a.R - r0);
-      __syncthreads();
-      for (int v = tid; v < nr * (kUD / 8); v += blockDim.x) {   // 16-byte vectors of U
-        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(a.U + (int64_t)r0 * kUD) + v);
-        const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          act[v * 8 + 2 * q] = __low2float(e[q]);
-          act[v * 8 + 2 * q + 1] = __high2float(e[q]);
-        }
-      }
-      __syncthreads();
-      for (int rr = rs; rr < nr; rr += 8) {
-        float acc = 0.f;
-#pragma unroll 8
-        for (int k = 0; k < kUD; ++k) acc += __bfloat162float(w[k * kXuWStride + nn]) * act[rr * kUD + k];
-        a.xu[(int64_t)(r0 + rr) * kXD + n0 + nn] = acc + bias;
-      }
-    }
-    return;
-  }
-  __nv_bfloat16* wt = reinterpret_cast<__nv_bfloat16*>(smem);                       // [128][130]: wt[k][n]
-  float* m = reinterpret_cast<float*>(smem + kD * kQbWStride * 2);                  // [8][128]
-  const int nrc = (a.R + kQbReqPerBlock - 1) / kQbReqPerBlock;
-  const int idx = blockIdx.x - kXuBlocks;
-  const int rc = idx % nrc, g = (idx / nrc) % kG, layer = idx / (nrc * kG);
-  const int L = a.L[g];
-  const int chunks = (L + 63) / 64;
-  const __nv_bfloat16* W = a.qm + ((int64_t)layer * kG + g) * kD * kD;
-  {  // wt[k][n] = W[n][k]: 2048 16-byte vectors, 8 per thread, loads issued before the stores
-    uint4 raw[8];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) raw[t] = __ldg(reinterpret_cast<const uint4*>(W) + tid + t * 256);
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const int v = tid + t * 256, n = v >> 4, k8 = v & 15;
-      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[t]);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) wt[(k8 * 8 + q) * kQbWStride + n] = e[q];
-    }
-  }
-  for (int i = tid; i < kQbReqPerBlock * kD; i += blockDim.x) {
-    const int rr = i / kD, k = i % kD, r = rc * kQbReqPerBlock + rr;
-    float s = 0.f;
-    if (r < a.R) {
-      const float* src = a.colsum + ((int64_t)r * kG + g) * a.max_chunks * kD + k;
-#pragma unroll 8
-      for (int c = 0; c < chunks; ++c) s += __ldg(src + (int64_t)c * kD);
-      s /= (float)L;
-    }
-    m[i] = s;
-  }
+  float* rg = a.colsum + ((int64_t)r * kG + g) * a.max_chunks * kD;
+  rg[chunk * kD + t] = part[0][t] + part[1][t];
+  __threadfence();
   __syncthreads();
-  const int n = tid & (kD - 1), half = tid >> 7;
-  const float bias = a.q_b[layer * kG * kD + g * kD + n];
-  float acc[kQbReqPerBlock / 2];
+  unsigned* cnt = a.cs_count + r * kG + g;
+  if (t == 0) last = atomicAdd(cnt, 1u) == (unsigned)(chunks - 1);
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  float sum = 0.f;
+  for (int c = 0; c < chunks; ++c) sum += __ldcg(rg + c * kD + t);  // in chunk order, as written by the others
+  m[t] = sum / (float)L;
+  if (t == 0) *cnt = 0u;
+  __syncthreads();
+  for (int l = 0; l < a.n_layers; ++l) {
+    const uint4* wrow = reinterpret_cast<const uint4*>(a.qm + (((int64_t)l * kG + g) * kD + t) * kD);
+    uint4 wv[16];
 #pragma unroll
-  for (int j = 0; j < kQbReqPerBlock / 2; ++j) acc[j] = 0.f;
-#pragma unroll 4
-  for (int k = 0; k < kD; ++k) {
-    const float wk = __bfloat162float(wt[k * kQbWStride + n]);
+    for (int v = 0; v < 16; ++v) wv[v] = __ldg(wrow + v);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < kQbReqPerBlock / 2; ++j) acc[j] += wk * m[(half + 2 * j) * kD + k];
-  }
+    for (int v = 0; v < 16; ++v) {
+      const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&wv[v]);
 #pragma unroll
-  for (int j = 0; j < kQbReqPerBlock / 2; ++j) {
-    const int r = rc * kQbReqPerBlock + half + 2 * j;
-    if (r < a.R) a.qb[((int64_t)layer * a.R + r) * (kG * kD) + g * kD + n] = acc[j] + bias;
+      for (int q = 0; q < 4; ++q) {
+        acc[q] += __low2float(e[q]) * m[v * 8 + 2 * q];
+        acc[q] += __high2float(e[q]) * m[v * 8 + 2 * q + 1];
+      }
+    }
+    a.qb[((int64_t)l * a.R + r) * (kG * kD) + g * kD + t] =
+        a.q_b[l * kG * kD + g * kD + t] + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
   }
 }
 
@@ -295,9 +220,5 @@ cudaError_t launch_seq_colsum(const FwdArgs& a, cudaStream_t s) {
   return launch_kernel(seq_colsum_kernel, dim3(a.max_chunks, kG, a.R), dim3(128), 0, s, a.pdl != 0, a);
 }
 
-cudaError_t launch_request_side(const FwdArgs& a, cudaStream_t s) {
-  const int nrc = (a.R + kQbReqPerBlock - 1) / kQbReqPerBlock;
-  return launch_kernel(request_side_kernel, dim3(kXuBlocks + a.n_layers * kG * nrc), dim3(256), 0, s, a.pdl != 0, a);
-}
 
 }  // namespace cvr
