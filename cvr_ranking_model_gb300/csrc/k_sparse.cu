@@ -153,10 +153,19 @@ __global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__
   const int chunk = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
   const int L = a.L[g];
   const int chunks = (L + 63) / 64;
+  const int t = threadIdx.x, cp = t & 63, half = t >> 6;
+  // constants of the query term, loaded before waiting for the encoder (only the last block uses them):
+  // row t of the first layer's mean-pool weights and its bias
+  uint4 w0[16];
+  {
+    const uint4* wrow = reinterpret_cast<const uint4*>(a.qm + ((int64_t)g * kD + t) * kD);
+#pragma unroll
+    for (int v = 0; v < 16; ++v) w0[v] = __ldg(wrow + v);
+  }
+  const float qb0 = __ldg(a.q_b + g * kD + t);
   pdl_trigger();
   pdl_wait();
   if (chunk >= chunks) return;
-  const int t = threadIdx.x, cp = t & 63, half = t >> 6;
   const __nv_bfloat16* base = a.H + (a.goff[g] + (int64_t)r * L) * kD;
   const int l_end = min(L, chunk * 64 + 64);
   float s0 = 0.f, s1 = 0.f;
@@ -180,17 +189,28 @@ __global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__
   if (t == 0) last = atomicAdd(cnt, 1u) == (unsigned)(chunks - 1);
   __syncthreads();
   if (!last) return;
-  __threadfence();
   float sum = 0.f;
-  for (int c = 0; c < chunks; ++c) sum += __ldcg(rg + c * kD + t);  // in chunk order, as written by the others
+  for (int c0 = 0; c0 < chunks; c0 += 4) {  // four loads in flight, summed in chunk order
+    float v[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) v[c] = c0 + c < chunks ? __ldcg(rg + (c0 + c) * kD + t) : 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (c0 + c < chunks) sum += v[c];
+  }
   m[t] = sum / (float)L;
   if (t == 0) *cnt = 0u;
   __syncthreads();
   for (int l = 0; l < a.n_layers; ++l) {
-    const uint4* wrow = reinterpret_cast<const uint4*>(a.qm + (((int64_t)l * kG + g) * kD + t) * kD);
     uint4 wv[16];
+    if (l == 0) {
 #pragma unroll
-    for (int v = 0; v < 16; ++v) wv[v] = __ldg(wrow + v);
+      for (int v = 0; v < 16; ++v) wv[v] = w0[v];
+    } else {
+      const uint4* wrow = reinterpret_cast<const uint4*>(a.qm + (((int64_t)l * kG + g) * kD + t) * kD);
+#pragma unroll
+      for (int v = 0; v < 16; ++v) wv[v] = __ldg(wrow + v);
+    }
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int v = 0; v < 16; ++v) {
@@ -202,7 +222,7 @@ __global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__
       }
     }
     a.qb[((int64_t)l * a.R + r) * (kG * kD) + g * kD + t] =
-        a.q_b[l * kG * kD + g * kD + t] + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+        (l == 0 ? qb0 : a.q_b[l * kG * kD + g * kD + t]) + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
   }
 }
 

@@ -37,6 +37,12 @@ __device__ __forceinline__ void xu_block(const FwdArgs& a, int blk, uint8_t* sme
   }
   const int nn = tid & (kXuCols - 1), rs = tid >> 5;
   const float bias = __ldg(a.tok_b + n0 + nn);
+  // warm L2 with the mean-pool query weights, which the column-sum kernel reads next
+  {
+    const int64_t lines = (int64_t)a.n_layers * kG * kD * kD * 2 / 128;
+    const int64_t line = (int64_t)blk * kXuThreads + tid;
+    if (line < lines) asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(a.qm) + line * 128));
+  }
   pdl_wait();  // U comes from the sparse kernel
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
