@@ -22,7 +22,9 @@ namespace cvr {
 namespace {
 
 enum { EPI_TOKENIZE = 0, EPI_QUERY = 1, EPI_PLE = 2 };
-constexpr int kThreads = 192;  // heads kernel: warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
+constexpr int kThreads = 576;  // heads kernel: warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..17 build r_t,
+                               // warps 2..5 then drain TMEM (one per lane quarter)
+constexpr int kBuildWarps = kThreads / 32 - 2;
 constexpr int kBM = 128, kBK = 64;
 constexpr int kATile = kBM * kBK * 2;  // 16 KB
 
@@ -190,8 +192,11 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
               dst[j] = p;
             }
           }
-          if (nb <= kPleN && kPleN < nb + 32 && kPleN + kNT * kNE <= n0 + BN) {
-            const int o = kPleN - nb;  // gate logits sit in columns [768, 774)
+          // gate logits sit in columns [768, 774): 16 columns into the chunk that starts at 752 (tiles of
+          // 208 start at 624, chunks every 32 columns), a compile-time offset so v and add stay in registers
+          constexpr int o = 16;
+          static_assert(EPI != EPI_PLE || ((kPleN - o) % BN) % 32 == 0, "gate logits 16 columns into a chunk");
+          if (nb + o == kPleN) {
 #pragma unroll
             for (int t = 0; t < kNT; ++t) {
               float l0 = v[o + 3 * t] + add[o + 3 * t];
@@ -241,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) heads_kernel(const __grid_constan
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * kBM, t = blockIdx.y;
   if (threadIdx.x == 0) {
-    mbar_init(barA, 128);
+    mbar_init(barA, kBuildWarps * 32);
     mbar_init(barW, 1);
     mbar_init(barD, 1);
     *abort_flag = 0;
@@ -253,12 +258,12 @@ __global__ void __launch_bounds__(kThreads, 1) heads_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tbase = *tslot;
   pdl_trigger();
+  if (warp == 0 && lane == 0) {  // W1_t is constant: its load overlaps the previous kernel
+    mbar_expect_tx(barW, 4 * kATile);
+    for (int kb = 0; kb < 4; ++kb) tma_load_2d(sW + kb * kATile, &tmW1, barW, kb * kBK, t * kHH);
+  }
   pdl_wait();
   if (warp == 0) {
-    if (lane == 0) {
-      mbar_expect_tx(barW, 4 * kATile);
-      for (int kb = 0; kb < 4; ++kb) tma_load_2d(sW + kb * kATile, &tmW1, barW, kb * kBK, t * kHH);
-    }
   } else if (warp == 1) {
     if (lane == 0) {
       if (mbar_wait(barA, 0, abort_flag, a.err) && mbar_wait(barW, 0, abort_flag, a.err)) {
@@ -277,16 +282,16 @@ __global__ void __launch_bounds__(kThreads, 1) heads_kernel(const __grid_constan
     const int rl = q * 32 + lane;
     const int row = m0 + rl;
     const bool live = row < a.B;
-    // r_t = sum_k gate_t[k] e_k for the tile's 128 rows: warp w builds rows w, w+4, ...; lane l covers
-    // hidden units [8l, 8l+8) (a 16-byte vector of each expert), four rows' loads in flight at once.
+    // r_t = sum_k gate_t[k] e_k for the tile's 128 rows: build warp w builds rows w, w + 16, ...; lane l
+    // covers hidden units [8l, 8l+8) (a 16-byte vector of each expert), four rows' loads in flight at once.
     const int ew = warp - 2;
 #pragma unroll 1
-    for (int r0 = ew; r0 < kBM; r0 += 16) {
+    for (int r0 = ew; r0 < kBM; r0 += 4 * kBuildWarps) {
       uint4 u[4][3];
       float g[4][3];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int rr = r0 + 4 * k, grow = m0 + rr;
+        const int rr = r0 + kBuildWarps * k, grow = m0 + rr;
         const bool ok = grow < a.B;
         const uint4* e = reinterpret_cast<const uint4*>(a.Ex + (int64_t)(ok ? grow : 0) * kPleN);
 #pragma unroll
@@ -297,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) heads_kernel(const __grid_constan
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int rr = r0 + 4 * k;
+        const int rr = r0 + kBuildWarps * k;
         const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&u[k][0]);
         const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&u[k][1]);
         const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u[k][2]);
@@ -314,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) heads_kernel(const __grid_constan
     }
     fence_proxy_async_smem();
     mbar_arrive(barA);
-    if (mbar_wait(barD, 0, abort_flag, a.err)) {
+    if (warp < 6 && mbar_wait(barD, 0, abort_flag, a.err)) {
       tc_fence_after();
       float logit = 0.f;
 #pragma unroll 1
