@@ -34,7 +34,7 @@ __host__ __device__ constexpr uint32_t tmem_cols() {
 }
 template <int BN, int STAGES>
 __host__ __device__ constexpr int gemm_smem_bytes() {
-  return 1024 + STAGES * (kATile + BN * kBK * 2) + 256;
+  return 1024 + STAGES * (kATile + BN * kBK * 2) + 256 + (kPleCols + 32) * 4;  // + PLE biases
 }
 
 // Persistent GEMM: CTAs loop over 128 x BN output tiles (n fastest, so co-running CTAs share A rows in L2).
@@ -59,8 +59,11 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  float* sbias = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 256);  // PLE: biases of all columns
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (EPI == EPI_PLE)  // constant: staged before waiting for the previous kernel
+    for (int k = threadIdx.x; k < kPleCols + 32; k += blockDim.x) sbias[k] = __ldg(a.ple_b + k);
   const int tiles_n = N / BN;
   const int n_tiles = ((M + kBM - 1) / kBM) * tiles_n;
   const int nk = K / kBK;
@@ -141,25 +144,35 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
       const bool live = row < M;
       int req = 0;
       if (EPI != EPI_PLE && live) req = min(max(a.req_ids[row], 0), a.R - 1);
+      // the addends of this warp's chunks (per-request terms or biases) are loaded before waiting for the
+      // accumulator, so their latency hides under the tile's MMAs
+      constexpr int NMY = (NCHUNK + NGRP - 1) / NGRP;
+      float addv[NMY][32];
+#pragma unroll
+      for (int m = 0; m < NMY; ++m) {
+        const int c = grp + m * NGRP, nb = n0 + c * 32;
+        if (c >= NCHUNK || !live) continue;
+        if (EPI == EPI_TOKENIZE) {
+          ldg32(a.xu + (int64_t)req * kTokN + nb, addv[m]);
+          if (nb >= kXD) {  // first-layer query columns: + the mean-pool term of the request
+            float qadd[32];
+            ldg32(a.qb + (int64_t)req * (kG * kD) + (nb - kXD), qadd);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) addv[m][x] += qadd[x];
+          }
+        } else if (EPI == EPI_QUERY) {
+          ldg32(a.qb + ((int64_t)layer * a.R + req) * (kG * kD) + nb, addv[m]);
+        }
+      }
       if (!mbar_wait(&acc_full[buf], (i >> 1) & 1, abort_flag, a.err)) break;
       tc_fence_after();
-#pragma unroll 1
-      for (int c = grp; c < NCHUNK; c += NGRP) {
-        float v[32], add[32];
-        const int nb = n0 + c * 32;
-        if (live) {
-          if (EPI == EPI_TOKENIZE) {
-            ldg32(a.xu + (int64_t)req * kTokN + nb, add);
-            if (nb >= kXD) {  // first-layer query columns: + the mean-pool term of the request
-              float qadd[32];
-              ldg32(a.qb + (int64_t)req * (kG * kD) + (nb - kXD), qadd);
 #pragma unroll
-              for (int x = 0; x < 32; ++x) add[x] += qadd[x];
-            }
-          }
-          else if (EPI == EPI_QUERY) ldg32(a.qb + ((int64_t)layer * a.R + req) * (kG * kD) + nb, add);
-          else ldg32(a.ple_b + nb, add);
-        }
+      for (int m = 0; m < NMY; ++m) {
+        const int c = grp + m * NGRP;
+        if (c >= NCHUNK) continue;
+        float v[32];
+        const float* add = EPI == EPI_PLE ? sbias + n0 + c * 32 : addv[m];
+        const int nb = n0 + c * 32;
         tmem_ld32(tbase + lane_off + buf * TC + c * 32, v);
         if (!live) continue;
         if (EPI == EPI_TOKENIZE || EPI == EPI_QUERY) {
