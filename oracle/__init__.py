@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
         V, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
         L.oracle_score.argtypes = [V, V, V, i32, i32, V, V, V, V, V, i32, V, V, i32]
         L.oracle_score.restype = ctypes.c_int
+        L.oracle_score_lens.argtypes = [V, V, V, i32, i32, V, V, V, V, V, V, i32, V, V, i32]
+        L.oracle_score_lens.restype = ctypes.c_int
         L.oracle_pool_bag.argtypes = [V, V, i64, i32, dbl, V, V]
         L.oracle_pool_bag.restype = ctypes.c_int
         L.oracle_bf16.argtypes = [ctypes.c_float]
@@ -172,9 +174,10 @@ class Result:
 
 def score(wl: "synth.Workload", w: Dict[str, np.ndarray], requests: Optional[Sequence[int]] = None,
           dumps: bool = False, threads: int = 0, host_tables: Optional[Dict[int, np.ndarray]] = None,
-          **model_over) -> Result:
+          seq_lens: Optional[np.ndarray] = None, **model_over) -> Result:
     """Runs the oracle over ``requests`` (default: all). ``out`` is [n_cand][n_tasks] fp64 (NaN for the
-    candidates of requests not scored). ``model_over`` overrides tau, clamp or rms_eps."""
+    candidates of requests not scored). ``seq_lens`` [n_req][3]: events each request really has per group
+    (variable-length sequences; None = every slot). ``model_over`` overrides tau, clamp or rms_eps."""
     d = synth.DIMS
     m = model_struct(wl, **model_over)
     ws = weights_struct(w, wl.n_layers)
@@ -194,9 +197,11 @@ def score(wl: "synth.Workload", w: Dict[str, np.ndarray], requests: Optional[Seq
         dstruct = Dumps(*[_p(dm[k]) for k in ("pooled", "rows", "H", "Q", "Z", "Y", "R")])
     sub = None if requests is None else np.ascontiguousarray(requests, dtype=np.int32)
     req_ids = np.ascontiguousarray(wl.req_ids, dtype=np.int32)
-    st = lib().oracle_score(ctypes.byref(m), ctypes.addressof(tabs), ctypes.byref(ws), R, B, _p(req_ids), _p(wl.bag_offsets),
-                            _p(wl.bag_ids), _p(wl.seq_ids), _p(sub), 0 if sub is None else len(sub), _p(out),
-                            ctypes.byref(dstruct) if dstruct is not None else None, threads)
+    lens = None if seq_lens is None else np.ascontiguousarray(seq_lens, dtype=np.int32)
+    st = lib().oracle_score_lens(ctypes.byref(m), ctypes.addressof(tabs), ctypes.byref(ws), R, B, _p(req_ids),
+                                 _p(wl.bag_offsets), _p(wl.bag_ids), _p(wl.seq_ids), _p(lens), _p(sub),
+                                 0 if sub is None else len(sub), _p(out),
+                                 ctypes.byref(dstruct) if dstruct is not None else None, threads)
     return Result(out, st, dm)
 
 

@@ -281,9 +281,14 @@ static int check_model(const oracle_model* m) {
 }
 
 /* One request: its user bags, its sequences and every one of its candidates. */
+/* lens[g]: events of group g that this request really has (the first lens[g] of its seq_len[g] slots);
+ * the remaining slots are padding: never read, left out of the mean and masked out of the attention
+ * (sequence lengths are a dynamic input, iQIYI CVR 3.3; sequences are padded, 3.4.2). A group with no
+ * event decodes to a zero token and has a zero mean, as an empty bag pools to zero. */
 static int score_request(const oracle_model* m, const oracle_table* tables, const oracle_weights* w, int32_t n_req,
                          int32_t r, int32_t n_cand, const int32_t* req_ids, const int64_t* bag_offsets,
-                         const int64_t* bag_ids, const int64_t* seq_ids, double* out, const oracle_dumps* dumps) {
+                         const int64_t* bag_ids, const int64_t* seq_ids, const int32_t* lens, double* out,
+                         const oracle_dumps* dumps) {
   const int32_t Fu = m->n_user_fields, Fi = m->n_item_fields, E = m->emb_dim, D = m->token_dim;
   const int32_t N = m->n_tokens, G = m->n_groups, T = N + G;
   int32_t SL = 0;
@@ -311,7 +316,7 @@ static int score_request(const oracle_model* m, const oracle_table* tables, cons
   for (int32_t g = 0; g < G; ++g) {
     int bad = 0;
 #pragma omp parallel for schedule(static) reduction(| : bad)
-    for (int32_t l = 0; l < m->seq_len[g]; ++l) {
+    for (int32_t l = 0; l < lens[g]; ++l) {
       double x[1024];
       float row[512];
       const int64_t* ids = seq_ids + ((int64_t)r * SL + base + l) * m->seq_cols;
@@ -344,8 +349,8 @@ static int score_request(const oracle_model* m, const oracle_table* tables, cons
   for (int32_t g = 0; g < G; ++g) {
     for (int32_t i = 0; i < D; ++i) {
       double acc = 0.0;
-      for (int32_t l = 0; l < m->seq_len[g]; ++l) acc += H[(size_t)(base + l) * D + i];
-      mg[g * D + i] = m->seq_len[g] > 0 ? acc / m->seq_len[g] : 0.0;
+      for (int32_t l = 0; l < lens[g]; ++l) acc += H[(size_t)(base + l) * D + i];
+      mg[g * D + i] = lens[g] > 0 ? acc / lens[g] : 0.0;
     }
     base += m->seq_len[g];
   }
@@ -376,8 +381,11 @@ static int score_request(const oracle_model* m, const oracle_table* tables, cons
         double q[1024];
         oracle_query(z, N, D, mg + g * D, w->q_w[layer][g], w->q_b[layer][g], q);
         if (dumps && dumps->Q) memcpy(dumps->Q + (((size_t)layer * n_cand + b) * G + g) * D, q, sizeof(double) * D);
-        oracle_cross_attention(q, H + (size_t)gbase * D, m->seq_len[g], D, m->heads, m->tau, z + (size_t)(N + g) * D,
-                               NULL);
+        if (lens[g] > 0)
+          oracle_cross_attention(q, H + (size_t)gbase * D, lens[g], D, m->heads, m->tau, z + (size_t)(N + g) * D,
+                                 NULL);
+        else
+          for (int32_t i = 0; i < D; ++i) z[(size_t)(N + g) * D + i] = 0.0;
         gbase += m->seq_len[g];
       }
       if (dumps && dumps->Z)
@@ -407,7 +415,18 @@ int oracle_score(const oracle_model* m, const oracle_table* tables, const oracle
                  int32_t n_cand, const int32_t* req_ids, const int64_t* bag_offsets, const int64_t* bag_ids,
                  const int64_t* seq_ids, const int32_t* req_subset, int32_t n_subset, double* out,
                  const oracle_dumps* dumps, int32_t threads) {
+  return oracle_score_lens(m, tables, w, n_req, n_cand, req_ids, bag_offsets, bag_ids, seq_ids, NULL, req_subset,
+                           n_subset, out, dumps, threads);
+}
+
+int oracle_score_lens(const oracle_model* m, const oracle_table* tables, const oracle_weights* w, int32_t n_req,
+                      int32_t n_cand, const int32_t* req_ids, const int64_t* bag_offsets, const int64_t* bag_ids,
+                      const int64_t* seq_ids, const int32_t* seq_lens, const int32_t* req_subset, int32_t n_subset,
+                      double* out, const oracle_dumps* dumps, int32_t threads) {
   if (check_model(m) || n_req < 0 || n_cand < 0) return ORACLE_E_ARG;
+  if (seq_lens)
+    for (int64_t i = 0; i < (int64_t)n_req * m->n_groups; ++i)
+      if (seq_lens[i] < 0 || seq_lens[i] > m->seq_len[i % m->n_groups]) return ORACLE_E_ARG;
 #ifdef _OPENMP
   const int saved = omp_get_max_threads();
   if (threads > 0) omp_set_num_threads(threads);
@@ -422,7 +441,8 @@ int oracle_score(const oracle_model* m, const oracle_table* tables, const oracle
       status = ORACLE_E_ARG;
       break;
     }
-    int st = score_request(m, tables, w, n_req, r, n_cand, req_ids, bag_offsets, bag_ids, seq_ids, out, dumps);
+    const int32_t* lens = seq_lens ? seq_lens + (int64_t)r * m->n_groups : m->seq_len;
+    int st = score_request(m, tables, w, n_req, r, n_cand, req_ids, bag_offsets, bag_ids, seq_ids, lens, out, dumps);
     if (st) status = st;
   }
 #ifdef _OPENMP

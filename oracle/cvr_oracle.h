@@ -87,6 +87,14 @@ int oracle_score(const oracle_model* m, const oracle_table* tables, const oracle
                  const int64_t* seq_ids, const int32_t* req_subset, int32_t n_subset, double* out,
                  const oracle_dumps* dumps, int32_t threads);
 
+/* As oracle_score with variable-length sequences: seq_lens[n_req][n_groups] gives the events each request
+ * really has in each group, 0 <= seq_lens <= seq_len[g] (else ORACLE_E_ARG); the slots past it are padding,
+ * never read, out of the mean and masked out of the attention; a group with no event decodes to zero. */
+int oracle_score_lens(const oracle_model* m, const oracle_table* tables, const oracle_weights* w, int32_t n_req,
+                      int32_t n_cand, const int32_t* req_ids, const int64_t* bag_offsets, const int64_t* bag_ids,
+                      const int64_t* seq_ids, const int32_t* seq_lens, const int32_t* req_subset, int32_t n_subset,
+                      double* out, const oracle_dumps* dumps, int32_t threads);
+
 /* ---- single stages, exposed so that each can be pinned on its own ---- */
 int oracle_pool_bag(const oracle_table* t, const int64_t* ids, int64_t n, int32_t dim, double clamp, float* out,
                     int64_t* rows_out);

@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
         L.synth_rank_to_row.restype = i64
         L.synth_bags.argtypes = [u64, i64, P, P, i32, i32, dbl, P, P]
         L.synth_seq_ids.argtypes = [u64, i64, i64, i32, i64, dbl, P]
+        L.synth_seq_lens.argtypes = [u64, i64, i32, P, i32, P]
         _lib = L
     return _lib
 
@@ -183,6 +184,27 @@ def make_workload(name: str, n_req: Optional[int] = None, n_cand: Optional[int] 
                     user_rows=int(c["user_rows"]), item_rows=int(c["item_rows"]), seq_rows=int(c["seq_rows"]),
                     zipf_s=float(c["zipf_s"]), table_scale=float(table_scale), cand_per_req=cpr, req_ids=req_ids,
                     bag_offsets=offsets, bag_ids=ids, seq_ids=seq)
+
+
+def make_seq_lens(wl: Workload, min_len: int = 0, seed: Optional[int] = None) -> np.ndarray:
+    """Variable sequence lengths [n_req][3] int32: the events each request really has in each group,
+    uniform in [min_len, seq_len[g]]."""
+    L = np.ascontiguousarray(wl.seq_len, dtype=np.int32)
+    out = np.empty((wl.n_req, DIMS["n_groups"]), dtype=np.int32)
+    lib().synth_seq_lens(int(seed if seed is not None else wl.seed), wl.n_req, DIMS["n_groups"], _ptr(L), int(min_len),
+                         _ptr(out))
+    return out
+
+
+def pad_seq_ids(wl: Workload, lens: np.ndarray, fill: int) -> np.ndarray:
+    """seq_ids with every padding slot (past a request's length) set to ``fill``."""
+    ids = wl.seq_ids.copy()
+    base = 0
+    for g, L in enumerate(wl.seq_len):
+        for r in range(wl.n_req):
+            ids[r, base + int(lens[r, g]): base + L, :] = fill
+        base += L
+    return ids
 
 
 # ----------------------------------------------------------------------------------------------

@@ -92,3 +92,13 @@ void synth_seq_ids(uint64_t seed, int64_t n_req, int64_t sum_len, int32_t cols, 
     ids[i] = synth_rank_to_row(seed, 16u, rank, rows);
   }
 }
+
+void synth_seq_lens(uint64_t seed, int64_t n_req, int32_t n_groups, const int32_t* seq_len, int32_t min_len,
+                    int32_t* lens) {
+  for (int64_t r = 0; r < n_req; ++r)
+    for (int32_t g = 0; g < n_groups; ++g) {
+      const int32_t lo = min_len < seq_len[g] ? min_len : seq_len[g];
+      const uint64_t span = (uint64_t)(seq_len[g] - lo) + 1u;
+      lens[r * n_groups + g] = lo + (int32_t)(synth_hash(seed, SYNTH_STREAM_LENS, (uint64_t)(r * n_groups + g)) % span);
+    }
+}

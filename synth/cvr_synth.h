@@ -35,6 +35,7 @@ extern "C" {
 #define SYNTH_STREAM_IDS 0x3000u    /* + field index */
 #define SYNTH_STREAM_SEQ 0x4000u
 #define SYNTH_STREAM_PERM 0x5000u   /* + table index: offset of the rank->row bijection */
+#define SYNTH_STREAM_LENS 0x6000u   /* variable sequence lengths */
 
 #define SYNTH_GAMMA 0x9E3779B97F4A7C15ull
 
@@ -83,6 +84,10 @@ void synth_bags(uint64_t seed, int64_t n_bags, const int32_t* field_of_bag, cons
 
 /* Sequence ids [n_req][sum_len][cols], every id a Zipf(s) row of the shared table (table index 16). */
 void synth_seq_ids(uint64_t seed, int64_t n_req, int64_t sum_len, int32_t cols, int64_t rows, double s, int64_t* ids);
+
+/* Variable sequence lengths [n_req][n_groups]: lens[r][g] uniform in [min_len, seq_len[g]]. */
+void synth_seq_lens(uint64_t seed, int64_t n_req, int32_t n_groups, const int32_t* seq_len, int32_t min_len,
+                    int32_t* lens);
 
 #ifdef __cplusplus
 }
