@@ -46,9 +46,12 @@ def load_peaks():
 
 # ---------------------------------------------------------------------------------------------
 # algorithmic work (user side once per request, K/V and mean-pool once per request)
-def algorithmic_work(wl, nnz: int):
+def algorithmic_work(wl, nnz: int, seq_events=None):
+    """FLOPs per step and bytes; ``seq_events`` = the real sequence events of the batch per request (variable
+    lengths), default every slot."""
     D, H = 128, 256
-    R, B, SL, NL = wl.n_req, wl.n_cand, wl.sum_len, wl.n_layers
+    R, B, NL = wl.n_req, wl.n_cand, wl.n_layers
+    SL = wl.sum_len if seq_events is None else seq_events
     swiglu_row = 2 * D * 2 * H + 2 * H * D                       # 196,608 FLOP per row
     flops = {
         "seq_mlp": R * SL * swiglu_row,
@@ -254,6 +257,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--varlen", action="store_true",
+                    help="variable-length sequences: every request's length per group uniform in [1, L_g]")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
@@ -286,9 +291,16 @@ def main():
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     r, b, o, s, out = dw.ptrs()
     B = wl.n_cand
+    lens = d_lens = None
+    if args.varlen:
+        lens = synth.make_seq_lens(wl, min_len=1)
+        d_lens = torch.from_numpy(lens).to(dev)
 
     def step():
-        sc.score(wl.n_req, B, r, b, o, s, out)
+        if args.varlen:
+            sc.score_varlen(wl.n_req, B, r, b, o, s, d_lens.data_ptr(), out)
+        else:
+            sc.score(wl.n_req, B, r, b, o, s, out)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -322,6 +334,8 @@ def main():
                     step()
                     for name, ms in sc.stage_list():
                         stages.setdefault(name, []).append(ms)
+                elif args.varlen:
+                    sc.score_varlen_async(wl.n_req, B, r, b, o, s, d_lens.data_ptr(), out)
                 else:
                     sc.score_async(wl.n_req, B, r, b, o, s, out)
                 ends[i].record(stream)
@@ -358,7 +372,8 @@ def main():
         # a name repeats once per layer; stage_list already returns every launch -> group per step
         per_kernel[name] = sum(lst) / n_prof
     nnz = int(wl.bag_offsets[-1])
-    flops, total_bytes, sparse_bytes = algorithmic_work(wl, nnz)
+    seq_events = None if lens is None else float(lens.sum()) / wl.n_req
+    flops, total_bytes, sparse_bytes = algorithmic_work(wl, nnz, seq_events)
     peaks, peak_src = load_peaks()
     peak_tf = float(peaks["bf16_tflops"])
     peak_bw = float(peaks["hbm_gbs"])
@@ -391,7 +406,7 @@ def main():
 
     # ---- end to end through the host-buffer entry point (pinned buffers, copies inside the timed region)
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.varlen:  # the host-buffer entry point has fixed lengths
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory().numpy()
         h_req, h_ids, h_off, h_seq = pin(wl.req_ids), pin(wl.bag_ids), pin(wl.bag_offsets), pin(wl.seq_ids)
         h_out = torch.empty((B, 2), dtype=torch.float32).pin_memory().numpy()
@@ -429,7 +444,10 @@ def main():
                                    f"L={Lstr}, {wl.n_layers} interaction layer(s), tables {wl.user_rows}/"
                                    f"{wl.item_rows}/{wl.seq_rows} rows x 32 fp32, bags 1-8, Zipf({wl.zipf_s})",
                        "global_batch": B * world, "parallelism": f"replicas x{world}",
-                       "l2": "flushed (256 MB write) before every timed step"},
+                       "l2": "flushed (256 MB write) before every timed step",
+                       **({"seq_lens": f"variable: uniform in [1, L_g] per request and group, "
+                                       f"{float(lens.sum()) / wl.n_req:.1f} of {wl.sum_len} events per request"}
+                          if args.varlen else {})},
             "p50_ms": p50, "p99_ms": p99, "call_p50_ms": statistics.median(call_ms),
             "call_p99_ms": float(np.percentile(call_ms, 99)), "profiled_p50_ms": statistics.median(prof_ms),
             "roofline": roofline, "sparse_roofline": sparse, "path_roofline": path,

@@ -86,6 +86,10 @@ def lib() -> ctypes.CDLL:
         L.cvr_last_error.restype = ctypes.c_char_p
         L.cvr_status_string.argtypes = [ctypes.c_int]
         L.cvr_status_string.restype = ctypes.c_char_p
+        L.cvr_score_varlen.argtypes = [V, i32, i32, V, V, V, V, V, V]
+        L.cvr_score_varlen.restype = ctypes.c_int
+        L.cvr_score_varlen_async.argtypes = [V, i32, i32, V, V, V, V, V, V]
+        L.cvr_score_varlen_async.restype = ctypes.c_int
         L.cvr_predict_noalloc.argtypes = [V, i32, V, V]
         L.cvr_predict_noalloc.restype = ctypes.c_int
         L.cvr_destroy.argtypes = [V]
@@ -169,6 +173,19 @@ class Scorer:
         if check:
             self._check(st)
         return st
+
+    def score_varlen(self, n_req: int, n_cand: int, req_ids: int, bag_ids: int, bag_offsets: int, seq_ids: int,
+                     seq_lens: int, out: int, check: bool = True) -> int:
+        """cvr_score_varlen: seq_lens is a device int32 [n_req][3] of real sequence lengths."""
+        st = self._lib.cvr_score_varlen(self._h, n_req, n_cand, req_ids, bag_ids, bag_offsets, seq_ids, seq_lens, out)
+        if check:
+            self._check(st)
+        return st
+
+    def score_varlen_async(self, n_req: int, n_cand: int, req_ids: int, bag_ids: int, bag_offsets: int,
+                           seq_ids: int, seq_lens: int, out: int) -> None:
+        self._check(self._lib.cvr_score_varlen_async(self._h, n_req, n_cand, req_ids, bag_ids, bag_offsets, seq_ids,
+                                                     seq_lens, out))
 
     def score_async(self, n_req: int, n_cand: int, req_ids: int, bag_ids: int, bag_offsets: int, seq_ids: int,
                     out: int) -> None:

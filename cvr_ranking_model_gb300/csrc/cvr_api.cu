@@ -396,7 +396,7 @@ cvr_status sync_status(cvr_handle* h);
 
 cvr_status run_forward(cvr_handle* h, int32_t R, int32_t B, const int32_t* req_ids, const int64_t* bag_ids,
                        const int64_t* bag_offsets, const int64_t* seq_ids, float* out, float* dbg_pooled,
-                       int64_t* dbg_rows, bool sync = true) {
+                       int64_t* dbg_rows, bool sync = true, const int32_t* seq_lens = nullptr) {
   if (!h) return CVR_E_ARG;
   if (!req_ids || !bag_ids || !bag_offsets || !seq_ids || !out) return fail(h, CVR_E_ARG, "null input or output pointer");
   if (R < 1 || B < 1 || R > 65535 || B > (1 << 20)) return fail(h, CVR_E_SHAPE, "need 1 <= n_req <= 65535, 1 <= n_cand <= 2^20");
@@ -406,10 +406,11 @@ cvr_status run_forward(cvr_handle* h, int32_t R, int32_t B, const int32_t* req_i
   if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaSetDevice");
   cvr_status st = ensure_workspace(h, R, B);
   if (st != CVR_OK) return st;
-  const FwdArgs a = make_args(h, R, B, req_ids, bag_ids, bag_offsets, seq_ids, out, dbg_pooled, dbg_rows);
+  FwdArgs a = make_args(h, R, B, req_ids, bag_ids, bag_offsets, seq_ids, out, dbg_pooled, dbg_rows);
+  a.seq_lens = seq_lens;
   cudaStream_t s = h->stream;
   if (h->use_graph) {
-    std::vector<const void*> key = {req_ids, bag_ids, bag_offsets, seq_ids, out, dbg_pooled, dbg_rows,
+    std::vector<const void*> key = {req_ids, bag_ids, bag_offsets, seq_ids, seq_lens, out, dbg_pooled, dbg_rows,
                                     reinterpret_cast<const void*>((intptr_t)h->profile)};
     GraphEntry& ge = h->graphs[std::make_pair(R, B)];
     if (!ge.exec || ge.key != key) {
@@ -474,6 +475,7 @@ cvr_status sync_status(cvr_handle* h) {
   *hw = 0;
   if (ew & kErrTimeout) return fail(h, CVR_E_TIMEOUT, "a bounded device-side wait gave up");
   if (ew & kErrLayout) return fail(h, CVR_E_CUDA, "a kernel's shared-memory window was not 1024-byte aligned");
+  if (ew & kErrSeqLens) return fail(h, CVR_E_INPUT, "a sequence length is outside [0, seq_len[g]]");
   if (ew & (kErrOffsets | kErrReqIds))
     return fail(h, CVR_E_INPUT, (ew & kErrOffsets) ? "bag offsets decrease" : "request ids out of range or decreasing");
   if (ew & kErrIdRange) return fail(h, CVR_E_ID_RANGE, "an id is outside its table (row 0 was read)");
@@ -720,6 +722,18 @@ cvr_status cvr_score(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t
 cvr_status cvr_score_async(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids, const int64_t* bag_ids,
                            const int64_t* bag_offsets, const int64_t* seq_ids, float* out) {
   return run_forward(h, n_req, n_cand, req_ids, bag_ids, bag_offsets, seq_ids, out, nullptr, nullptr, false);
+}
+cvr_status cvr_score_varlen(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids,
+                            const int64_t* bag_ids, const int64_t* bag_offsets, const int64_t* seq_ids,
+                            const int32_t* seq_lens, float* out) {
+  if (!seq_lens) return fail(h, CVR_E_ARG, "null seq_lens");
+  return run_forward(h, n_req, n_cand, req_ids, bag_ids, bag_offsets, seq_ids, out, nullptr, nullptr, true, seq_lens);
+}
+cvr_status cvr_score_varlen_async(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids,
+                                  const int64_t* bag_ids, const int64_t* bag_offsets, const int64_t* seq_ids,
+                                  const int32_t* seq_lens, float* out) {
+  if (!seq_lens) return fail(h, CVR_E_ARG, "null seq_lens");
+  return run_forward(h, n_req, n_cand, req_ids, bag_ids, bag_offsets, seq_ids, out, nullptr, nullptr, false, seq_lens);
 }
 
 cvr_status cvr_sync(cvr_handle* h) {

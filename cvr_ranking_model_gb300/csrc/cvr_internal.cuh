@@ -41,7 +41,8 @@ constexpr int kErrOffsets = 2;      // bag offsets not non-decreasing
 constexpr int kErrReqIds = 4;       // request ids out of range or decreasing
 constexpr int kErrTimeout = 8;      // a bounded wait in a tensor-core kernel gave up
 constexpr int kErrDebugCap = 16;
-constexpr int kErrLayout = 32;      // a kernel found its shared-memory window misaligned and did nothing
+constexpr int kErrLayout = 32;
+constexpr int kErrSeqLens = 64;     // a sequence length outside [0, L[g]]      // a kernel found its shared-memory window misaligned and did nothing
 
 // ---- arguments of the forward pass, one copy per call ----
 struct FwdArgs {
@@ -72,6 +73,7 @@ struct FwdArgs {
   __nv_bfloat16* H;       // same layout: encoded sequence states
   float* colsum;          // [R][G][max_chunks][128] partial column sums of H
   unsigned* cs_count;     // [R][G] blocks of the column-sum kernel done (zero between calls)
+  const int32_t* seq_lens;  // [R][G] events each request really has per group, or null (all L[g])
   int max_chunks;
   float* xu;              // [R][1664] user half of the tokeniser (+ bias)
   float* qb;              // [layers][R][384] per-request query term (+ bias)
@@ -142,6 +144,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       return false;
     }
   }
+}
+// Events that request r really has in group g (variable-length sequences); kept in [0, L[g]] so that no
+// access ever leaves the padded layout (the sparse kernel reports a value outside that range).
+__device__ __forceinline__ int seq_len_of(const FwdArgs& a, int64_t r, int g) {
+  if (!a.seq_lens) return a.L[g];
+  const int v = a.seq_lens[r * kG + g];
+  return v < 0 ? 0 : (v > a.L[g] ? a.L[g] : v);
 }
 // Programmatic dependent launch: let the next kernel in the stream launch (its prologue overlaps this
 // kernel), and wait until the previous kernel has completed and its writes are visible. Every kernel of

@@ -84,10 +84,12 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
   }
   // logits * log2(e) / (tau * sqrt(head_dim)) so that the softmax runs on exp2
   const float sl2 = 1.4426950408889634f / (a.tau * sqrtf((float)kHD));
-  const int nchunks = (L + kChunk - 1) / kChunk;
 
   for (int r = r_first; r <= r_last; ++r) {
     const __nv_bfloat16* Hb = a.H + (a.goff[g] + (int64_t)r * L) * kD;
+    // keys: the request's real events (variable-length sequences mask the padding out); none -> zero token
+    const int Lr = seq_len_of(a, r, g);
+    const int nchunks = (Lr + kChunk - 1) / kChunk;
     // one chunk = 64 rows x 16 pieces of 16 bytes, 4 per thread; rows past L are zero-filled
     auto load_chunk = [&](int ch, int slot) {
       __nv_bfloat16* dst = buf + slot * (kChunk * kKStride);
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
       for (int i = 0; i < kChunk * (kD / 8) / (kWarps * 32); ++i) {
         const int v = tid + i * kWarps * 32, row = v >> 4, c16 = v & 15;
         const int l = ch * kChunk + row;
-        const bool ok = l < L;
+        const bool ok = l < Lr;
         cp_async16(dst + row * kKStride + c16 * 8, Hb + (int64_t)(ok ? l : 0) * kD + c16 * 8, ok ? 16 : 0);
       }
     };
@@ -106,7 +108,7 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
 #pragma unroll
       for (int i = 0; i < 4; ++i) o[j][i] = 0.f;
     __syncthreads();  // the previous request's chunks have been read by every warp
-    load_chunk(0, 0);
+    if (nchunks > 0) load_chunk(0, 0);
     cp_async_commit();
     for (int ch = 0; ch < nchunks; ++ch) {
       if (ch + 1 < nchunks) load_chunk(ch + 1, (ch + 1) & 1);
@@ -131,7 +133,7 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int key = ch * kChunk + nt * 8 + 2 * tig + (i & 1);
-          s[nt][i] = key < L ? s[nt][i] * sl2 : -INFINITY;
+          s[nt][i] = key < Lr ? s[nt][i] * sl2 : -INFINITY;
           if (i < 2)
             cA = fmaxf(cA, s[nt][i]);
           else
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
     lA += __shfl_xor_sync(0xffffffffu, lA, 2);
     lB += __shfl_xor_sync(0xffffffffu, lB, 1);
     lB += __shfl_xor_sync(0xffffffffu, lB, 2);
-    const float iA = 1.f / lA, iB = 1.f / lB;
+    const float iA = Lr > 0 ? 1.f / lA : 0.f, iB = Lr > 0 ? 1.f / lB : 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int col = kXD + g * kD + h * kHD + j * 8 + 2 * tig;

@@ -130,6 +130,14 @@ __global__ void __launch_bounds__(256) sparse_kernel(const __grid_constant__ Fwd
       ++g;
     }
     const int64_t row = a.goff[g] + r * a.L[g] + l;
+    if (a.seq_lens) {
+      const int raw = a.seq_lens[r * kG + g];
+      if (l == 0 && lane == 0 && (raw < 0 || raw > a.L[g])) atomicOr(a.err, kErrSeqLens);
+      if (l >= seq_len_of(a, r, g)) {  // padding: never read, encoded from zeros and never used
+        store_bf16x4(a.Xs + row * kD + c * kE + part * 4, make_float4(0.f, 0.f, 0.f, 0.f));
+        return;
+      }
+    }
     int64_t id = a.seq_ids[ev * kCols + c];
     if (id < 0 || id >= a.table_rows[kFu + kFi]) {
       atomicOr(a.err, kErrIdRange);
@@ -152,7 +160,6 @@ __global__ void __launch_bounds__(256) sparse_kernel(const __grid_constant__ Fwd
 __global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__ FwdArgs a) {
   const int chunk = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
   const int L = a.L[g];
-  const int chunks = (L + 63) / 64;
   const int t = threadIdx.x, cp = t & 63, half = t >> 6;
   // constants of the query term, loaded before waiting for the encoder (only the last block uses them):
   // row t of the first layer's mean-pool weights and its bias
@@ -165,9 +172,13 @@ __global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__
   const float qb0 = __ldg(a.q_b + g * kD + t);
   pdl_trigger();
   pdl_wait();
+  // positions that count: the request's real events (all L without variable lengths); an empty group still
+  // has one block, which writes a zero mean
+  const int len = seq_len_of(a, r, g);
+  const int chunks = len > 0 ? (len + 63) / 64 : 1;
   if (chunk >= chunks) return;
   const __nv_bfloat16* base = a.H + (a.goff[g] + (int64_t)r * L) * kD;
-  const int l_end = min(L, chunk * 64 + 64);
+  const int l_end = min(len, chunk * 64 + 64);
   float s0 = 0.f, s1 = 0.f;
 #pragma unroll 8
   for (int l = chunk * 64 + half; l < l_end; l += 2) {
@@ -198,7 +209,7 @@ __global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__
     for (int c = 0; c < 4; ++c)
       if (c0 + c < chunks) sum += v[c];
   }
-  m[t] = sum / (float)L;
+  m[t] = len > 0 ? sum / (float)len : 0.f;
   if (t == 0) *cnt = 0u;
   __syncthreads();
   for (int l = 0; l < a.n_layers; ++l) {

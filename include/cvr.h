@@ -132,6 +132,21 @@ cvr_status cvr_score(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t
 cvr_status cvr_score_async(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids,
                            const int64_t* bag_ids, const int64_t* bag_offsets, const int64_t* seq_ids, float* out);
 
+/* As cvr_score with variable-length sequences (sequence lengths are a dynamic input, iQIYI ad-CVR article
+ * 3.3; sequences are padded, 3.4.2): seq_lens [n_req][3] int32 (DEVICE) gives the events each request
+ * really has in each group, 0 <= seq_lens[r][g] <= seq_len[g]; seq_ids keeps its padded layout and the
+ * slots past a request's length are padding -- never read (any value is accepted there), left out of the
+ * mean-pooled sequence vector and masked out of the cross-attention. A group with no event decodes to a
+ * zero token and has a zero mean. A length outside the range returns CVR_E_INPUT (it is used clamped, so
+ * nothing is read out of bounds). */
+cvr_status cvr_score_varlen(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids,
+                            const int64_t* bag_ids, const int64_t* bag_offsets, const int64_t* seq_ids,
+                            const int32_t* seq_lens, float* out);
+/* cvr_score_varlen, enqueued only (as cvr_score_async; collect the status with cvr_sync). */
+cvr_status cvr_score_varlen_async(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids,
+                                  const int64_t* bag_ids, const int64_t* bag_offsets, const int64_t* seq_ids,
+                                  const int32_t* seq_lens, float* out);
+
 /* Waits for every call enqueued on the handle's stream and returns the status of the device-side checks
  * of all calls since the previous cvr_sync (CVR_E_ID_RANGE, CVR_E_INPUT, CVR_E_TIMEOUT) or CVR_E_CUDA. */
 cvr_status cvr_sync(cvr_handle* h);
