@@ -90,6 +90,8 @@ def lib() -> ctypes.CDLL:
         L.cvr_score_varlen.restype = ctypes.c_int
         L.cvr_score_varlen_async.argtypes = [V, i32, i32, V, V, V, V, V, V]
         L.cvr_score_varlen_async.restype = ctypes.c_int
+        L.cvr_selftest_wait_timeout.argtypes = [V]
+        L.cvr_selftest_wait_timeout.restype = ctypes.c_int
         L.cvr_predict_noalloc.argtypes = [V, i32, V, V]
         L.cvr_predict_noalloc.restype = ctypes.c_int
         L.cvr_destroy.argtypes = [V]
@@ -216,6 +218,10 @@ class Scorer:
         if check:
             self._check(st)
         return st
+
+    def selftest_wait_timeout(self) -> int:
+        """cvr_selftest_wait_timeout: a wait that nothing ends; returns the status (7 = CVR_E_TIMEOUT)."""
+        return int(self._lib.cvr_selftest_wait_timeout(self._h))
 
     def predict_noalloc(self, n_cand: int, y: int, out: int, check: bool = True) -> int:
         """cvr_predict_noalloc: PLE + heads on a device bf16 [n_cand][16][128] Token Mixer output, with

@@ -880,6 +880,46 @@ void cvr_destroy(cvr_handle* h) {
 }  // extern "C"
 
 // ------------------------------------------------------------------------------------------
+// Self-test of the bounded waits: one CTA waits on an mbarrier that nothing arrives at, with the same wait
+// the tensor-core kernels use; after its ~1 s limit the wait gives up, raises the timeout bit and the kernel
+// publishes it like the last kernel of a call does. Nothing faults, traps or hangs.
+namespace {
+__global__ void selftest_wait_kernel(int* err, int* err_host) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait(&bar, 0, &abort_flag, err);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int e = atomicExch(err, 0);
+    volatile int* hw = err_host;
+    *hw = *hw | e;
+    __threadfence_system();
+  }
+}
+}  // namespace
+
+extern "C" cvr_status cvr_selftest_wait_timeout(cvr_handle* h) {
+  if (!h) return CVR_E_ARG;
+  int cur = -1;
+  cudaError_t ce = cudaGetDevice(&cur);
+  if (ce == cudaSuccess && cur != h->device) ce = cudaSetDevice(h->device);
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaSetDevice");
+  cvr_status st = ensure_workspace(h, 1, 1);  // the device error word
+  if (st != CVR_OK) return st;
+  selftest_wait_kernel<<<1, 32, 0, h->stream>>>(h->err, h->err_host_dev);
+  ce = cudaGetLastError();
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "self-test launch");
+  return sync_status(h);
+}
+
+// ------------------------------------------------------------------------------------------
 // Prediction step without allocation: the PLE expert GEMM and the heads kernel on a caller's Token
 // Mixer output, their intermediates (expert outputs, gates) and the error word in one fixed
 // file-scope device array instead of the handle's growable workspace.

@@ -196,6 +196,12 @@ int32_t cvr_last_launch_count(const cvr_handle* h);
 const char* cvr_last_error(const cvr_handle* h);
 const char* cvr_status_string(cvr_status s);
 
+/* Diagnostic (the pages have no counterpart): launches one CTA that waits on a barrier nothing arrives at,
+ * through the same bounded wait as the scoring kernels, and returns what a call would report when a wait
+ * gives up: CVR_E_TIMEOUT after about 1 s, the handle staying usable. Shows that a stuck wait ends as a
+ * status instead of a hung GPU. */
+cvr_status cvr_selftest_wait_timeout(cvr_handle* h);
+
 /* The prediction step alone -- PLE experts and gates, task towers and sigmoid -- on a caller's Token Mixer
  * output, without allocating device memory. The papers have no counterpart: it serves callers that
  * cannot allocate mid-flight (a serving loop whose device memory is all pre-reserved by its own pool, or
