@@ -14,8 +14,8 @@ namespace cvr {
 
 namespace {
 
-constexpr int kBagsPerBlock = 32;     // 8 lanes per bag, 256 threads
-constexpr int kEventsPerBlock = 8;    // one warp per sequence event
+constexpr int kSparseThreads = 256;   // 8 warps
+constexpr int kSparseBlocksPerSm = 3;  // persistent grid
 
 __device__ __forceinline__ float clampf(float v, float c) { return fminf(fmaxf(v, -c), c); }
 
@@ -26,130 +26,184 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float4 v) {
   *reinterpret_cast<uint2*>(dst) = p;
 }
 
-__global__ void __launch_bounds__(256) sparse_kernel(const __grid_constant__ FwdArgs a, int n_bag_blocks) {
-  const int tid = threadIdx.x;
+// Persistent and software-pipelined: every warp walks units with a grid stride -- units of 4 bags (8 lanes
+// per bag, each lane 4 of the 32 columns), then single sequence events -- and while the table rows of unit k
+// are in flight it already loads the ids of unit k+1 and the offsets of unit k+2, so the three dependent
+// round trips of a lookup (offsets -> ids -> rows) overlap instead of adding up.
+__global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_kernel(const __grid_constant__ FwdArgs a) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t gw = (int64_t)blockIdx.x * (kSparseThreads / 32) + (tid >> 5);
+  const int64_t nw = (int64_t)gridDim.x * (kSparseThreads / 32);
   pdl_trigger();
   pdl_wait();
-  if ((int)blockIdx.x < n_bag_blocks) {
-    // request ids: in range and non-decreasing (checked once per candidate)
-    const int64_t cand = (int64_t)blockIdx.x * 256 + tid;
-    if (cand < a.B) {
-      const int r = a.req_ids[cand];
-      bool bad = r < 0 || r >= a.R;
-      if (cand + 1 < a.B && a.req_ids[cand + 1] < r) bad = true;
-      if (bad) atomicOr(a.err, kErrReqIds);
-    }
+  // request ids: in range and non-decreasing (checked once per candidate)
+  for (int64_t cand = (int64_t)blockIdx.x * kSparseThreads + tid; cand < a.B;
+       cand += (int64_t)gridDim.x * kSparseThreads) {
+    const int r = a.req_ids[cand];
+    bool bad = r < 0 || r >= a.R;
+    if (cand + 1 < a.B && a.req_ids[cand + 1] < r) bad = true;
+    if (bad) atomicOr(a.err, kErrReqIds);
+  }
+  int errbits = 0;
+
+  // ---------------------------------------------------------------- embedding bags
+  {
     const int64_t n_user_bags = (int64_t)a.R * kFu;
     const int64_t n_bags = n_user_bags + (int64_t)a.B * kFi;
-    const int64_t bag_raw = (int64_t)blockIdx.x * kBagsPerBlock + (tid >> 3);
-    const bool live = bag_raw < n_bags;             // dead lanes still take part in the shuffles
-    const int64_t bag = live ? bag_raw : n_bags - 1;
-    const int sub = tid & 7;  // this lane's 4 of the 32 columns
-    int field;
-    __nv_bfloat16* dst;
-    if (bag < n_user_bags) {
-      field = (int)(bag % kFu);
-      dst = a.U + (bag / kFu) * kUD + field * kE;
-    } else {
-      const int64_t ib = bag - n_user_bags;
-      const int f = (int)(ib % kFi);
-      field = kFu + f;
-      dst = a.I + (ib / kFi) * kID + f * kE;
+    const int64_t n_units = (n_bags + 3) / 4;
+    const int grp = lane >> 3, sub = lane & 7;  // bag of this lane within the unit, its 4 columns
+    auto bag_of = [&](int64_t u) { return min(u * 4 + grp, n_bags - 1); };
+    int64_t u0 = gw, s0 = 0, e0 = 0, id0 = 0, s1 = 0, e1 = 0;
+    if (u0 < n_units) {
+      const int64_t b = bag_of(u0);
+      s0 = a.bag_offsets[b];
+      e0 = a.bag_offsets[b + 1];
     }
-    const float* table = a.tables[field];
-    const int64_t rows = a.table_rows[field];
-    const int64_t s = a.bag_offsets[bag];
-    int64_t e = a.bag_offsets[bag + 1];
-    int errbits = 0;
-    if (e < s) {
-      errbits |= kErrOffsets;
-      e = s;
+    if (u0 + nw < n_units) {
+      const int64_t b = bag_of(u0 + nw);
+      s1 = a.bag_offsets[b];
+      e1 = a.bag_offsets[b + 1];
     }
-    // The 8 lanes of a bag load 8 ids at once (one each), share them by shuffle, then have all 8 rows in
-    // flight; the fp32 sum still runs in bag order from 0 (bit-exact with the definition). The loop count
-    // is the warp's largest bag, so every lane reaches every shuffle.
-    int64_t nmax = e - s;
-    nmax = max(nmax, (int64_t)__shfl_xor_sync(0xffffffffu, (long long)nmax, 8));
-    nmax = max(nmax, (int64_t)__shfl_xor_sync(0xffffffffu, (long long)nmax, 16));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t base = 0; base < nmax; base += 8) {
-      const int64_t j = s + base + sub;
-      int64_t mine = 0;
-      if (j < e) {
-        mine = a.bag_ids[j];
-        if (mine < 0 || mine >= rows) {
-          errbits |= kErrIdRange;
-          mine = 0;
+    if (u0 < n_units && s0 + sub < e0) id0 = a.bag_ids[s0 + sub];
+    while (u0 < n_units) {  // warp-uniform
+      const int64_t u1 = u0 + nw, u2 = u1 + nw;
+      // stage A: offsets of unit k+2; stage B: first ids of unit k+1 (raw; checked when used)
+      int64_t s2 = 0, e2 = 0, id1 = 0;
+      if (u2 < n_units) {
+        const int64_t b = bag_of(u2);
+        s2 = a.bag_offsets[b];
+        e2 = a.bag_offsets[b + 1];
+      }
+      if (u1 < n_units && s1 + sub < e1) id1 = a.bag_ids[s1 + sub];
+      // stage C: the rows of unit k
+      const int64_t bag_raw = u0 * 4 + grp;
+      const bool live = bag_raw < n_bags;  // dead lanes still take part in the shuffles
+      const int64_t bag = live ? bag_raw : n_bags - 1;
+      int field;
+      __nv_bfloat16* dst;
+      if (bag < n_user_bags) {
+        field = (int)(bag % kFu);
+        dst = a.U + (bag / kFu) * kUD + field * kE;
+      } else {
+        const int64_t ib = bag - n_user_bags;
+        const int f = (int)(ib % kFi);
+        field = kFu + f;
+        dst = a.I + (ib / kFi) * kID + f * kE;
+      }
+      const float* table = a.tables[field];
+      const int64_t rows = a.table_rows[field];
+      const int64_t s = s0;
+      int64_t e = e0;
+      if (e < s) {
+        if (live) errbits |= kErrOffsets;
+        e = s;
+      }
+      // The 8 lanes of a bag hold 8 ids at once (one each), share them by shuffle, then have all 8 rows in
+      // flight; the fp32 sum still runs in bag order from 0 (bit-exact with the definition). The loop count
+      // is the warp's largest bag, so every lane reaches every shuffle.
+      int64_t nmax = e - s;
+      nmax = max(nmax, (int64_t)__shfl_xor_sync(0xffffffffu, (long long)nmax, 8));
+      nmax = max(nmax, (int64_t)__shfl_xor_sync(0xffffffffu, (long long)nmax, 16));
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int64_t base = 0; base < nmax; base += 8) {
+        const int64_t j = s + base + sub;
+        int64_t mine = 0;
+        if (j < e) {
+          mine = base == 0 ? id0 : a.bag_ids[j];
+          if (mine < 0 || mine >= rows) {
+            if (live) errbits |= kErrIdRange;
+            mine = 0;
+          }
+          if (a.dbg_rows && live) a.dbg_rows[j] = mine;
         }
-        if (a.dbg_rows && live) a.dbg_rows[j] = mine;
-      }
-      float4 v[8];
+        float4 v[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int64_t id = __shfl_sync(0xffffffffu, (long long)mine, u, 8);
-        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (s + base + u < e) v[u] = __ldg(reinterpret_cast<const float4*>(table + id * kE) + sub);
-      }
+        for (int u = 0; u < 8; ++u) {
+          const int64_t id = __shfl_sync(0xffffffffu, (long long)mine, u, 8);
+          v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (s + base + u < e) v[u] = __ldg(reinterpret_cast<const float4*>(table + id * kE) + sub);
+        }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (s + base + u < e) {
-          acc.x = __fadd_rn(acc.x, v[u].x);
-          acc.y = __fadd_rn(acc.y, v[u].y);
-          acc.z = __fadd_rn(acc.z, v[u].z);
-          acc.w = __fadd_rn(acc.w, v[u].w);
+        for (int u = 0; u < 8; ++u) {
+          if (s + base + u < e) {
+            acc.x = __fadd_rn(acc.x, v[u].x);
+            acc.y = __fadd_rn(acc.y, v[u].y);
+            acc.z = __fadd_rn(acc.z, v[u].z);
+            acc.w = __fadd_rn(acc.w, v[u].w);
+          }
         }
       }
-    }
-    const int64_t n = e - s;
-    float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (n > 0) {
-      const float fn = (float)n;
-      m.x = __fdiv_rn(acc.x, fn);
-      m.y = __fdiv_rn(acc.y, fn);
-      m.z = __fdiv_rn(acc.z, fn);
-      m.w = __fdiv_rn(acc.w, fn);
-    }
-    m.x = clampf(m.x, a.clamp);
-    m.y = clampf(m.y, a.clamp);
-    m.z = clampf(m.z, a.clamp);
-    m.w = clampf(m.w, a.clamp);
-    if (!live) return;
-    store_bf16x4(dst + sub * 4, m);
-    if (a.dbg_pooled) reinterpret_cast<float4*>(a.dbg_pooled + bag * kE)[sub] = m;
-    if (errbits) atomicOr(a.err, errbits);
-  } else {
-    // sequence events: 4 id columns -> 4 rows of the shared table -> one 128-wide row
-    const int64_t ev = (int64_t)(blockIdx.x - n_bag_blocks) * kEventsPerBlock + (tid >> 5);
-    if (ev >= (int64_t)a.R * a.SL) return;
-    const int lane = tid & 31, c = lane >> 3, part = lane & 7;
-    const int64_t r = ev / a.SL;
-    int l = (int)(ev - r * a.SL);
-    int g = 0;
-    while (g < kG - 1 && l >= a.L[g]) {
-      l -= a.L[g];
-      ++g;
-    }
-    const int64_t row = a.goff[g] + r * a.L[g] + l;
-    if (a.seq_lens) {
-      const int raw = a.seq_lens[r * kG + g];
-      if (l == 0 && lane == 0 && (raw < 0 || raw > a.L[g])) atomicOr(a.err, kErrSeqLens);
-      if (l >= seq_len_of(a, r, g)) {  // padding: never read, encoded from zeros and never used
-        store_bf16x4(a.Xs + row * kD + c * kE + part * 4, make_float4(0.f, 0.f, 0.f, 0.f));
-        return;
+      const int64_t n = e - s;
+      float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (n > 0) {
+        const float fn = (float)n;
+        m.x = __fdiv_rn(acc.x, fn);
+        m.y = __fdiv_rn(acc.y, fn);
+        m.z = __fdiv_rn(acc.z, fn);
+        m.w = __fdiv_rn(acc.w, fn);
       }
+      m.x = clampf(m.x, a.clamp);
+      m.y = clampf(m.y, a.clamp);
+      m.z = clampf(m.z, a.clamp);
+      m.w = clampf(m.w, a.clamp);
+      if (live) {
+        store_bf16x4(dst + sub * 4, m);
+        if (a.dbg_pooled) reinterpret_cast<float4*>(a.dbg_pooled + bag * kE)[sub] = m;
+      }
+      u0 = u1;
+      s0 = s1;
+      e0 = e1;
+      id0 = id1;
+      s1 = s2;
+      e1 = e2;
     }
-    int64_t id = a.seq_ids[ev * kCols + c];
-    if (id < 0 || id >= a.table_rows[kFu + kFi]) {
-      atomicOr(a.err, kErrIdRange);
-      id = 0;
-    }
-    float4 v = __ldg(reinterpret_cast<const float4*>(a.tables[kFu + kFi] + id * kE) + part);
-    v.x = clampf(v.x, a.clamp);
-    v.y = clampf(v.y, a.clamp);
-    v.z = clampf(v.z, a.clamp);
-    v.w = clampf(v.w, a.clamp);
-    store_bf16x4(a.Xs + row * kD + c * kE + part * 4, v);
   }
+
+  // ---------------------------------------------------------------- sequence events
+  // one warp per event: 4 id columns -> 4 rows of the shared table -> one 128-wide row; the ids of the next
+  // event load while this event's rows are in flight
+  {
+    const int64_t n_events = (int64_t)a.R * a.SL;
+    const int c = lane >> 3, part = lane & 7;
+    int64_t ev = gw;
+    int64_t id_next = ev < n_events ? a.seq_ids[ev * kCols + c] : 0;
+    while (ev < n_events) {  // warp-uniform
+      const int64_t ev1 = ev + nw;
+      int64_t id = id_next;
+      id_next = ev1 < n_events ? a.seq_ids[ev1 * kCols + c] : 0;
+      const int64_t r = ev / a.SL;
+      int l = (int)(ev - r * a.SL);
+      int g = 0;
+      while (g < kG - 1 && l >= a.L[g]) {
+        l -= a.L[g];
+        ++g;
+      }
+      const int64_t row = a.goff[g] + r * a.L[g] + l;
+      __nv_bfloat16* out = a.Xs + row * kD + c * kE + part * 4;
+      bool pad = false;
+      if (a.seq_lens) {
+        const int raw = a.seq_lens[r * kG + g];
+        if (l == 0 && lane == 0 && (raw < 0 || raw > a.L[g])) errbits |= kErrSeqLens;
+        pad = l >= seq_len_of(a, r, g);  // padding: its id is never looked up; encoded from zeros, never used
+      }
+      if (pad) {
+        store_bf16x4(out, make_float4(0.f, 0.f, 0.f, 0.f));
+      } else {
+        if (id < 0 || id >= a.table_rows[kFu + kFi]) {
+          errbits |= kErrIdRange;
+          id = 0;
+        }
+        float4 v = __ldg(reinterpret_cast<const float4*>(a.tables[kFu + kFi] + id * kE) + part);
+        v.x = clampf(v.x, a.clamp);
+        v.y = clampf(v.y, a.clamp);
+        v.z = clampf(v.z, a.clamp);
+        v.w = clampf(v.w, a.clamp);
+        store_bf16x4(out, v);
+      }
+      ev = ev1;
+    }
+  }
+  if (errbits) atomicOr(a.err, errbits);
 }
 
 // Partial column sums of H over chunks of 64 positions; grid (max_chunks, G, R), 128 threads. The last
@@ -240,11 +294,7 @@ __global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__
 }  // namespace
 
 cudaError_t launch_sparse(const FwdArgs& a, cudaStream_t s) {
-  const int64_t n_bags = (int64_t)a.R * kFu + (int64_t)a.B * kFi;
-  const int n_bag_blocks = (int)((n_bags + kBagsPerBlock - 1) / kBagsPerBlock);
-  const int64_t n_events = (int64_t)a.R * a.SL;
-  const int n_seq_blocks = (int)((n_events + kEventsPerBlock - 1) / kEventsPerBlock);
-  return launch_kernel(sparse_kernel, dim3(n_bag_blocks + n_seq_blocks), dim3(256), 0, s, false, a, n_bag_blocks);
+  return launch_kernel(sparse_kernel, dim3(a.num_sms * kSparseBlocksPerSm), dim3(kSparseThreads), 0, s, false, a);
 }
 
 cudaError_t launch_seq_colsum(const FwdArgs& a, cudaStream_t s) {
