@@ -89,6 +89,9 @@ struct cvr_handle {
   int* err = nullptr;
   unsigned* done = nullptr;
   unsigned* cs_count = nullptr;
+  float* attn_state = nullptr;
+  unsigned* attn_count = nullptr;
+  int attn_splits = 1;
   int* err_host = nullptr;      // pinned, mapped: the call's error bits
   int* err_host_dev = nullptr;  // its device address
   // host-input staging
@@ -237,6 +240,11 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   const size_t oZ = take((size_t)B_cap * kYD * 2), oY = take((size_t)B_cap * kYD * 2);
   const size_t oQ = take((size_t)B_cap * kG * kD * 2), oEx = take((size_t)B_cap * kPleN * 2);
   const size_t oG = take((size_t)B_cap * 8 * 4), oErr = take(1024), oCnt = take((size_t)R_cap * kG * 4);
+  int splits = 1;
+  for (int g = 0; g < kG; ++g) splits = std::max(splits, split_count(h->L[g]));
+  const size_t n_tiles32 = (size_t)(B_cap + 31) / 32;
+  const size_t oAst = splits > 1 ? take(n_tiles32 * kG * splits * 256 * 20 * 4) : 0;
+  const size_t oAcnt = take(n_tiles32 * kG * 4);
   cudaError_t e = cudaMalloc(&h->ws, off);
   if (e != cudaSuccess) {
     h->ws = nullptr;
@@ -259,8 +267,12 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   h->err = (int*)(b + oErr);
   h->done = (unsigned*)(b + oErr + 256);
   h->cs_count = (unsigned*)(b + oCnt);
+  h->attn_splits = splits;
+  h->attn_state = splits > 1 ? (float*)(b + oAst) : nullptr;
+  h->attn_count = (unsigned*)(b + oAcnt);
   e = cudaMemset(h->err, 0, 1024);  // error word and CTA counter start at zero; the last kernel resets them
   if (e == cudaSuccess) e = cudaMemset(h->cs_count, 0, (size_t)R_cap * kG * 4);  // reset by their last block
+  if (e == cudaSuccess) e = cudaMemset(h->attn_count, 0, n_tiles32 * kG * 4);  // reset by the merging CTA
   if (e != cudaSuccess) {
     free_workspace(h);
     return fail(h, CVR_E_CUDA, "workspace initialisation failed");
@@ -318,6 +330,9 @@ FwdArgs make_args(cvr_handle* h, int R, int B, const int32_t* req_ids, const int
   a.H = h->H;
   a.colsum = h->colsum;
   a.cs_count = h->cs_count;
+  a.attn_state = h->attn_state;
+  a.attn_count = h->attn_count;
+  a.attn_splits = h->attn_splits;
   a.max_chunks = h->max_chunks;
   a.xu = h->xu;
   a.qb = h->qb;
@@ -981,6 +996,8 @@ cvr_status cvr_predict_noalloc(cvr_handle* h, int32_t n_cand, const void* y, flo
   a.U = a.I = a.Xs = a.H = a.Z = a.Y = a.Q = nullptr;
   a.colsum = a.xu = a.qb = nullptr;
   a.cs_count = nullptr;
+  a.attn_state = nullptr;
+  a.attn_count = nullptr;
   a.Ex = reinterpret_cast<bf16*>(sc);
   a.gates = reinterpret_cast<float*>(sc + kNaGatesOff);
   a.err = reinterpret_cast<int*>(sc + kNaErrOff);

@@ -34,6 +34,15 @@ constexpr int kHH = 128;          // head hidden width
 constexpr int kPleN = kNE * kDE;  // 768 expert columns
 constexpr int kPleCols = 832;     // + 2x3 gate logits, zero-padded to 4 tiles of 208
 constexpr int kMaxLayers = 4;
+// cross-attention over long sequences: a CTA takes at most kChunksPerSplit chunks of 64 positions; a
+// group longer than that is split over up to kMaxSplits CTAs whose softmax states are merged
+constexpr int kAttnChunk = 64, kChunksPerSplit = 8, kMaxSplits = 8;
+__host__ __device__ constexpr int split_count(int L) {
+  return L <= kAttnChunk * kChunksPerSplit ? 1
+         : ((L + kAttnChunk * kChunksPerSplit - 1) / (kAttnChunk * kChunksPerSplit) < kMaxSplits
+                ? (L + kAttnChunk * kChunksPerSplit - 1) / (kAttnChunk * kChunksPerSplit)
+                : kMaxSplits);
+}
 
 // ---- device error word bits ----
 constexpr int kErrIdRange = 1;      // a bag or sequence id outside its table
@@ -74,6 +83,9 @@ struct FwdArgs {
   float* colsum;          // [R][G][max_chunks][128] partial column sums of H
   unsigned* cs_count;     // [R][G] blocks of the column-sum kernel done (zero between calls)
   const int32_t* seq_lens;  // [R][G] events each request really has per group, or null (all L[g])
+  float* attn_state;       // [B/32][G][attn_splits][256 threads][20] partial softmax states of split sequences
+  unsigned* attn_count;    // [B/32][G] split CTAs done (zero between calls)
+  int attn_splits;         // splits of the longest group (grid z of the attention kernel)
   int max_chunks;
   float* xu;              // [R][1664] user half of the tokeniser (+ bias)
   float* qb;              // [layers][R][384] per-request query term (+ bias)

@@ -3,7 +3,9 @@
 // both K and V; logits are scaled by 1/(tau*sqrt(32)) and normalised by a softmax over the sequence.
 //
 // One CTA = one group x 32 consecutive candidates (two m16 MMA tiles), 8 warps: warp w owns candidate tile
-// w / 4 and head w % 4 for the whole sequence, so its online-softmax state never needs merging. All warps
+// w / 4 and head w % 4 for the whole sequence, so its online-softmax state never needs merging within the
+// CTA. A group longer than 512 positions is split over several CTAs (when the tile holds one request); the
+// last of them to finish -- found with a counter, nobody waits -- merges their states. All warps
 // share the K/V chunks of 64 positions, staged by the whole CTA with cp.async into a double buffer; every
 // K/V row is read once per 32 candidates. Logits and P.V run on mma.sync m16n8k16 (bf16 in, fp32
 // accumulate) with the softmax on exp2, and the decoded tokens are written straight into slots 13..15 of
@@ -20,6 +22,7 @@ constexpr int kChunk = 64;                        // positions per step
 constexpr int kKStride = kD + 8;                  // padded smem row (272 B): conflict-free fragment loads
 constexpr int kBufBytes = kChunk * kKStride * 2;  // 17408 B
 constexpr int kSmemBytes = 2 * kBufBytes;         // 34816 B
+static_assert(kChunk == kAttnChunk, "split sizing uses the same chunk");
 
 __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -50,20 +53,26 @@ __device__ __forceinline__ float ex2(float x) {
 __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_constant__ FwdArgs a,
                                                                 __nv_bfloat16* __restrict__ zin) {
   extern __shared__ __align__(16) uint8_t smem[];
-  const int g = blockIdx.y;
+  const int g = blockIdx.y, sp = blockIdx.z;
   const int b0 = blockIdx.x * kCandPerCta;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int mt = warp >> 2, h = warp & 3;  // candidate tile and head of this warp
   const int L = a.L[g];
   const int R = a.R, B = a.B;
+  const int n_split = split_count(L);  // this group's splits of the sequence
   __nv_bfloat16* buf = reinterpret_cast<__nv_bfloat16*>(smem);  // 2 chunks of [64][136]
   pdl_trigger();
+  if (sp >= n_split) return;
   pdl_wait();
   const int b_last = min(b0 + kCandPerCta, B) - 1;
   // request ids are validated by the sparse kernel; here they are only kept in range
   const int r_first = min(max(a.req_ids[b0], 0), R - 1);
   const int r_last = min(max(a.req_ids[b_last], 0), R - 1);
+  // A long sequence is split over n_split CTAs when the tile holds one request; otherwise the first split's
+  // CTA takes every position of every request of its tile.
+  const bool split = n_split > 1 && r_first == r_last;
+  if (!split && sp > 0) return;
   const int rowA = b0 + mt * 16 + gid, rowB = rowA + 8;
   const int reqA = rowA < B ? a.req_ids[rowA] : -1;
   const int reqB = rowB < B ? a.req_ids[rowB] : -1;
@@ -85,12 +94,13 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
   // logits * log2(e) / (tau * sqrt(head_dim)) so that the softmax runs on exp2
   const float sl2 = 1.4426950408889634f / (a.tau * sqrtf((float)kHD));
 
-  for (int r = r_first; r <= r_last; ++r) {
+  // online-softmax state of this thread: rows A (gid) and B (gid + 8), 8 of head h's 32 output columns each
+  float o[4][4];
+  float mA, mB, lA, lB;
+  // positions [64 c_begin, 64 c_end) of request r's group-g sequence, of which Lr are real events
+  auto run_chunks = [&](int r, int Lr, int c_begin, int c_end) {
     const __nv_bfloat16* Hb = a.H + (a.goff[g] + (int64_t)r * L) * kD;
-    // keys: the request's real events (variable-length sequences mask the padding out); none -> zero token
-    const int Lr = seq_len_of(a, r, g);
-    const int nchunks = (Lr + kChunk - 1) / kChunk;
-    // one chunk = 64 rows x 16 pieces of 16 bytes, 4 per thread; rows past L are zero-filled
+    // one chunk = 64 rows x 16 pieces of 16 bytes, 4 per thread; rows past Lr are zero-filled
     auto load_chunk = [&](int ch, int slot) {
       __nv_bfloat16* dst = buf + slot * (kChunk * kKStride);
 #pragma unroll
@@ -101,21 +111,22 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
         cp_async16(dst + row * kKStride + c16 * 8, Hb + (int64_t)(ok ? l : 0) * kD + c16 * 8, ok ? 16 : 0);
       }
     };
-    float o[4][4];
-    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+    mA = mB = -INFINITY;
+    lA = lB = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
       for (int i = 0; i < 4; ++i) o[j][i] = 0.f;
     __syncthreads();  // the previous request's chunks have been read by every warp
-    if (nchunks > 0) load_chunk(0, 0);
+    if (c_begin < c_end) load_chunk(c_begin, 0);
     cp_async_commit();
-    for (int ch = 0; ch < nchunks; ++ch) {
-      if (ch + 1 < nchunks) load_chunk(ch + 1, (ch + 1) & 1);
+    for (int ch = c_begin; ch < c_end; ++ch) {
+      const int slot = (ch - c_begin) & 1;
+      if (ch + 1 < c_end) load_chunk(ch + 1, slot ^ 1);
       cp_async_commit();
       cp_async_wait1();
       __syncthreads();  // chunk ch has landed for every warp
-      const __nv_bfloat16* Ks = buf + (ch & 1) * (kChunk * kKStride);
+      const __nv_bfloat16* Ks = buf + slot * (kChunk * kKStride);
       float s[8][4];
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
@@ -185,7 +196,9 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
       }
       __syncthreads();  // every warp is done with chunk ch before it is refilled
     }
-    // row sums over the 4 threads of a row, then the decoded token of head h
+  };
+  // row sums over the 4 threads of a row, then the decoded token of head h for the rows of request r
+  auto finish = [&](int r, int Lr) {
     lA += __shfl_xor_sync(0xffffffffu, lA, 1);
     lA += __shfl_xor_sync(0xffffffffu, lA, 2);
     lB += __shfl_xor_sync(0xffffffffu, lB, 1);
@@ -199,7 +212,71 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
       if (reqB == r)
         *reinterpret_cast<uint32_t*>(zin + (int64_t)rowB * kYD + col) = pack_bf16(o[j][2] * iB, o[j][3] * iB);
     }
+  };
+
+  if (!split) {
+    for (int r = r_first; r <= r_last; ++r) {
+      // keys: the request's real events (variable-length sequences mask the padding out); none -> zero token
+      const int Lr = seq_len_of(a, r, g);
+      run_chunks(r, Lr, 0, (Lr + kChunk - 1) / kChunk);
+      finish(r, Lr);
+    }
+    return;
   }
+  // ---- split: this CTA's positions, its state to the workspace, the last split of the tile merges them
+  const int r = r_first;
+  const int Lr = seq_len_of(a, r, g);
+  const int nch = (Lr + kChunk - 1) / kChunk;
+  const int per = ((L + kChunk - 1) / kChunk + n_split - 1) / n_split;  // chunks per split (of the padded length)
+  run_chunks(r, Lr, min(sp * per, nch), min((sp + 1) * per, nch));
+  const int64_t slot = (int64_t)blockIdx.x * kG + g;
+  float4* st = reinterpret_cast<float4*>(a.attn_state) + ((slot * a.attn_splits + sp) * (kWarps * 32) + tid) * 5;
+  st[0] = make_float4(mA, mB, lA, lB);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) st[1 + j] = make_float4(o[j][0], o[j][1], o[j][2], o[j][3]);
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last = atomicAdd(a.attn_count + slot, 1u) == (unsigned)(n_split - 1);
+  __syncthreads();
+  if (!last) return;
+  // merge in split order: M = max m_s, l = sum l_s 2^(m_s - M), o = sum o_s 2^(m_s - M)
+  float4 hd[kMaxSplits];
+#pragma unroll
+  for (int q = 0; q < kMaxSplits; ++q)
+    if (q < n_split)
+      hd[q] = __ldcg(reinterpret_cast<const float4*>(a.attn_state) + ((slot * a.attn_splits + q) * (kWarps * 32) + tid) * 5);
+  float MA = -INFINITY, MB = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < kMaxSplits; ++q)
+    if (q < n_split) {
+      MA = fmaxf(MA, hd[q].x);
+      MB = fmaxf(MB, hd[q].y);
+    }
+  lA = lB = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[j][i] = 0.f;
+#pragma unroll
+  for (int q = 0; q < kMaxSplits; ++q) {
+    if (q >= n_split) break;
+    const float wA = hd[q].x == -INFINITY ? 0.f : ex2(hd[q].x - MA);
+    const float wB = hd[q].y == -INFINITY ? 0.f : ex2(hd[q].y - MB);
+    lA += hd[q].z * wA;
+    lB += hd[q].w * wB;
+    const float4* so = reinterpret_cast<const float4*>(a.attn_state) + ((slot * a.attn_splits + q) * (kWarps * 32) + tid) * 5 + 1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 v = __ldcg(so + j);
+      o[j][0] += v.x * wA;
+      o[j][1] += v.y * wA;
+      o[j][2] += v.z * wB;
+      o[j][3] += v.w * wB;
+    }
+  }
+  if (tid == 0) a.attn_count[slot] = 0u;  // ready for the next call
+  finish(r, Lr);
 }
 
 }  // namespace
@@ -210,7 +287,8 @@ cudaError_t prepare_attention_kernel() {
 
 cudaError_t launch_attention(const FwdArgs& a, __nv_bfloat16* zin, cudaStream_t s) {
   const int nblk = (a.B + kCandPerCta - 1) / kCandPerCta;
-  return launch_kernel(attention_kernel, dim3(nblk, kG), dim3(kWarps * 32), kSmemBytes, s, a.pdl != 0, a, zin);
+  return launch_kernel(attention_kernel, dim3(nblk, kG, a.attn_splits), dim3(kWarps * 32), kSmemBytes, s, a.pdl != 0,
+                       a, zin);
 }
 
 }  // namespace cvr
