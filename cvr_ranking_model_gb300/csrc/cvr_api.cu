@@ -99,7 +99,7 @@ struct cvr_handle {
   size_t stage_bytes = 0;
   // tensor maps
   CUtensorMap tm_seqW13, tm_seqW2, tm_tokI, tm_qW[kMaxLayers], tm_tmW13, tm_tmW2, tm_pleW, tm_headW1;
-  CUtensorMap tm_Xs, tm_I, tm_x_Z, tm_x_Y, tm_5_Z, tm_5_Y, tm_full_Z, tm_full_Y;
+  CUtensorMap tm_Xs, tm_I, tm_x_Z, tm_x_Y, tm_5_Z, tm_5_Y, tm_full_Z, tm_full_Y, tm_Q;
   // graphs, profiling
   bool use_graph = true, profile = false, pdl = true;
   std::map<std::pair<int, int>, GraphEntry> graphs;
@@ -285,7 +285,8 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
             encode_2d(&h->tm_x_Z, h->Z, kXD, B_cap, kYD, 64, 128) &&
             encode_2d(&h->tm_x_Y, h->Y, kXD, B_cap, kYD, 64, 128) && encode_mix5d(&h->tm_5_Z, h->Z, B_cap) &&
             encode_mix5d(&h->tm_5_Y, h->Y, B_cap) && encode_2d(&h->tm_full_Z, h->Z, kYD, B_cap, kYD, 64, 128) &&
-            encode_2d(&h->tm_full_Y, h->Y, kYD, B_cap, kYD, 64, 128);
+            encode_2d(&h->tm_full_Y, h->Y, kYD, B_cap, kYD, 64, 128) &&
+            encode_2d(&h->tm_Q, h->Q, kG * kD, B_cap, kG * kD, 64, 128);
   if (!ok) {
     free_workspace(h);
     return fail(h, CVR_E_CUDA, "cuTensorMapEncodeTiled failed for a workspace tensor");
@@ -387,7 +388,7 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
   for (int g = 0; g < kG; ++g) seq_tiles += (int)(((int64_t)a.R * a.L[g] + 127) / 128);
   run(launch_seq_mlp(a, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, s), kStageNames[1]);
   run(launch_seq_colsum(a, s), kStageNames[2]);
-  run(launch_tokenizer(a, h->tm_I, h->tm_tokI, s), kStageNames[3]);
+  run(launch_tokenizer(a, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, s), kStageNames[3]);
   bf16* zin = h->Z;
   bf16* zout = h->Y;
   for (int l = 0; l < a.n_layers; ++l) {

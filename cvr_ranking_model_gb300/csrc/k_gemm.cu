@@ -28,13 +28,20 @@ constexpr int kBuildWarps = kThreads / 32 - 2;
 constexpr int kBM = 128, kBK = 64;
 constexpr int kATile = kBM * kBK * 2;  // 16 KB
 
+// named barrier of the NEPI epilogue warps (the producer and MMA warps never take part)
+template <int NEPI>
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NEPI * 32) : "memory");
+}
+
 template <int BN>
 __host__ __device__ constexpr uint32_t tmem_cols() {
   return BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
 }
-template <int BN, int STAGES>
+template <int BN, int STAGES, int EPI>
 __host__ __device__ constexpr int gemm_smem_bytes() {
-  return 1024 + STAGES * (kATile + BN * kBK * 2) + 256 + (kPleCols + 32) * 4;  // + PLE biases
+  return 1024 + STAGES * (kATile + BN * kBK * 2) + 256 + (kPleCols + 32) * 4 +  // + PLE biases
+         (EPI == EPI_TOKENIZE ? 1024 + 2 * kBM * BN * 2 : 0);                         // + output staging (aligned)
 }
 
 // Persistent GEMM: CTAs loop over 128 x BN output tiles (n fastest, so co-running CTAs share A rows in L2).
@@ -44,7 +51,8 @@ __host__ __device__ constexpr int gemm_smem_bytes() {
 template <int BN, int STAGES, int EPI, int NEPI>
 __global__ void __launch_bounds__(64 + NEPI * 32, 1)
     gemm_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap tmA,
-                const __grid_constant__ CUtensorMap tmB, int M, int N, int K, int layer) {
+                const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmZo,
+                const __grid_constant__ CUtensorMap tmQo, int M, int N, int K, int layer) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int B_TILE = BN * kBK * 2;
@@ -60,6 +68,9 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   float* sbias = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 256);  // PLE: biases of all columns
+  // tokeniser: two output tiles [128][BN] bf16 staged for TMA stores, as boxes of [128 rows][64 columns]
+  // with the 128-byte swizzle (1024-byte aligned)
+  uint8_t* sOut = reinterpret_cast<uint8_t*>(((reinterpret_cast<uintptr_t>(sbias + kPleCols + 32)) + 1023) & ~uintptr_t(1023));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (EPI == EPI_PLE)  // constant: staged before waiting for the previous kernel
@@ -166,6 +177,12 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
       }
       if (!mbar_wait(&acc_full[buf], (i >> 1) & 1, abort_flag, a.err)) break;
       tc_fence_after();
+      uint8_t* sb = sOut + (i & 1) * (kBM * BN * 2);
+      if (EPI == EPI_TOKENIZE) {
+        // the TMA store issued from this staging buffer two tiles ago must have finished reading it
+        if (threadIdx.x == 64) bulk_wait_read<1>();
+        epi_bar<NEPI>();
+      }
 #pragma unroll
       for (int m = 0; m < NMY; ++m) {
         const int c = grp + m * NGRP;
@@ -175,10 +192,21 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
         const int nb = n0 + c * 32;
         tmem_ld32(tbase + lane_off + buf * TC + c * 32, v);
         if (!live) continue;
-        if (EPI == EPI_TOKENIZE || EPI == EPI_QUERY) {
-          __nv_bfloat16* out = EPI == EPI_TOKENIZE ? (nb < kXD ? a.Z + (int64_t)row * kYD + nb
-                                                              : a.Q + (int64_t)row * (kG * kD) + (nb - kXD))
-                                                 : a.Q + (int64_t)row * (kG * kD) + nb;
+        if (EPI == EPI_TOKENIZE) {
+          // columns [32c, 32c + 32) of row rl into the staging tile: box c/2, 16-byte chunks 4 (c%2) + j, swizzled
+          const int rl = q * 32 + lane;
+          uint8_t* rowp = sb + (c >> 1) * (kBM * 128) + rl * 128;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 p;
+            p.x = pack_bf16(v[8 * j + 0] + add[8 * j + 0], v[8 * j + 1] + add[8 * j + 1]);
+            p.y = pack_bf16(v[8 * j + 2] + add[8 * j + 2], v[8 * j + 3] + add[8 * j + 3]);
+            p.z = pack_bf16(v[8 * j + 4] + add[8 * j + 4], v[8 * j + 5] + add[8 * j + 5]);
+            p.w = pack_bf16(v[8 * j + 6] + add[8 * j + 6], v[8 * j + 7] + add[8 * j + 7]);
+            *reinterpret_cast<uint4*>(rowp + ((((c & 1) * 4 + j) ^ (rl & 7)) << 4)) = p;
+          }
+        } else if (EPI == EPI_QUERY) {
+          __nv_bfloat16* out = a.Q + (int64_t)row * (kG * kD) + nb;
           uint4* dst = reinterpret_cast<uint4*>(out);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -228,10 +256,24 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
           }
         }
       }
+      if (EPI == EPI_TOKENIZE) {
+        // the whole tile is staged: one thread stores it as boxes of 64 columns (tokens into Z, the first
+        // layer's queries into Q)
+        fence_proxy_async_smem();
+        epi_bar<NEPI>();
+        if (threadIdx.x == 64) {
+          const bool qcols = n0 >= kXD;
+#pragma unroll
+          for (int bx = 0; bx < BN / 64; ++bx)
+            tma_store_2d(qcols ? &tmQo : &tmZo, sb + bx * (kBM * 128), (qcols ? n0 - kXD : n0) + bx * 64, m0);
+          bulk_commit();
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
+    if (EPI == EPI_TOKENIZE && threadIdx.x == 64) bulk_wait_all();  // the stores have landed before exit
   }
   tc_fence_before();
   __syncthreads();
@@ -372,16 +414,16 @@ __global__ void __launch_bounds__(kThreads, 1) heads_kernel(const __grid_constan
 template <int BN, int STAGES, int EPI, int NEPI>
 cudaError_t prepare_gemm() {
   return cudaFuncSetAttribute(gemm_kernel<BN, STAGES, EPI, NEPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              gemm_smem_bytes<BN, STAGES>());
+                              gemm_smem_bytes<BN, STAGES, EPI>());
 }
 
 template <int BN, int STAGES, int EPI, int NEPI>
-cudaError_t launch_gemm(const FwdArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
-                        int layer, cudaStream_t s) {
+cudaError_t launch_gemm(const FwdArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmZo,
+                        const CUtensorMap& tmQo, int M, int N, int K, int layer, cudaStream_t s) {
   const int tiles = ((M + kBM - 1) / kBM) * (N / BN);
   const int grid = tiles < a.num_sms ? tiles : a.num_sms;
-  return launch_kernel(gemm_kernel<BN, STAGES, EPI, NEPI>, dim3(grid), dim3(64 + NEPI * 32), gemm_smem_bytes<BN, STAGES>(),
-                       s, a.pdl != 0, a, tmA, tmB, M, N, K, layer);
+  return launch_kernel(gemm_kernel<BN, STAGES, EPI, NEPI>, dim3(grid), dim3(64 + NEPI * 32), gemm_smem_bytes<BN, STAGES, EPI>(),
+                       s, a.pdl != 0, a, tmA, tmB, tmZo, tmQo, M, N, K, layer);
 }
 
 constexpr int kTokBN = 128, kTokStages = 4, kTokEpi = 8;
@@ -399,17 +441,19 @@ cudaError_t prepare_gemm_kernels() {
   return e;
 }
 
-cudaError_t launch_tokenizer(const FwdArgs& a, const CUtensorMap& tmI, const CUtensorMap& tmW, cudaStream_t s) {
+cudaError_t launch_tokenizer(const FwdArgs& a, const CUtensorMap& tmI, const CUtensorMap& tmW, const CUtensorMap& tmZo,
+                             const CUtensorMap& tmQo, cudaStream_t s) {
   static_assert(kXD % kTokBN == 0 && kTokN % kTokBN == 0, "token and query columns fall in separate tiles");
-  return launch_gemm<kTokBN, kTokStages, EPI_TOKENIZE, kTokEpi>(a, tmI, tmW, a.B, kTokN, kID, 0, s);
+  static_assert(kTokBN % 64 == 0 && gemm_smem_bytes<kTokBN, kTokStages, EPI_TOKENIZE>() <= 232448, "staging fits");
+  return launch_gemm<kTokBN, kTokStages, EPI_TOKENIZE, kTokEpi>(a, tmI, tmW, tmZo, tmQo, a.B, kTokN, kID, 0, s);
 }
 
 cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, const CUtensorMap& tmW, cudaStream_t s) {
-  return launch_gemm<kQryBN, kQryStages, EPI_QUERY, kQryEpi>(a, tmX, tmW, a.B, kG * kD, kXD, layer, s);
+  return launch_gemm<kQryBN, kQryStages, EPI_QUERY, kQryEpi>(a, tmX, tmW, tmX, tmX, a.B, kG * kD, kXD, layer, s);
 }
 
 cudaError_t launch_ple(const FwdArgs& a, const CUtensorMap& tmY, const CUtensorMap& tmW, cudaStream_t s) {
-  return launch_gemm<kPleBN, kPleStages, EPI_PLE, kPleEpi>(a, tmY, tmW, a.B, kPleCols, kYD, 0, s);
+  return launch_gemm<kPleBN, kPleStages, EPI_PLE, kPleEpi>(a, tmY, tmW, tmY, tmY, a.B, kPleCols, kYD, 0, s);
 }
 
 cudaError_t launch_heads(const FwdArgs& a, const CUtensorMap& tmW1, cudaStream_t s) {
