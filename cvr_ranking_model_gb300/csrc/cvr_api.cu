@@ -99,7 +99,7 @@ struct cvr_handle {
   size_t stage_bytes = 0;
   // tensor maps
   CUtensorMap tm_seqW13, tm_seqW2, tm_tokI, tm_qW[kMaxLayers], tm_tmW13, tm_tmW2, tm_pleW, tm_headW1;
-  CUtensorMap tm_Xs, tm_I, tm_x_Z, tm_x_Y, tm_5_Z, tm_5_Y, tm_full_Z, tm_full_Y, tm_Q;
+  CUtensorMap tm_Xs, tm_I, tm_x_Z, tm_x_Y, tm_5_Z, tm_5_Y, tm_full_Z, tm_full_Y, tm_Q, tm_Ex;
   // graphs, profiling
   bool use_graph = true, profile = false, pdl = true;
   std::map<std::pair<int, int>, GraphEntry> graphs;
@@ -131,6 +131,20 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Expert outputs Ex[rows][768] (bf16), plain layout, boxes of [128 rows][208 columns]: the PLE epilogue's
+// TMA stores (columns past 768 are clipped)
+bool encode_ex(CUtensorMap* m, const void* base, uint64_t rows) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kPleN, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kPleN * 2};
+  cuuint32_t box[2] = {208, 128};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -286,7 +300,8 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
             encode_2d(&h->tm_x_Y, h->Y, kXD, B_cap, kYD, 64, 128) && encode_mix5d(&h->tm_5_Z, h->Z, B_cap) &&
             encode_mix5d(&h->tm_5_Y, h->Y, B_cap) && encode_2d(&h->tm_full_Z, h->Z, kYD, B_cap, kYD, 64, 128) &&
             encode_2d(&h->tm_full_Y, h->Y, kYD, B_cap, kYD, 64, 128) &&
-            encode_2d(&h->tm_Q, h->Q, kG * kD, B_cap, kG * kD, 64, 128);
+            encode_2d(&h->tm_Q, h->Q, kG * kD, B_cap, kG * kD, 64, 128) &&
+            encode_ex(&h->tm_Ex, h->Ex, B_cap);
   if (!ok) {
     free_workspace(h);
     return fail(h, CVR_E_CUDA, "cuTensorMapEncodeTiled failed for a workspace tensor");
@@ -399,7 +414,7 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
     run(launch_attention(a, zin, s), kStageNames[5]);
     run(launch_tm_mlp(a, l, zin, zout, in_is_Z ? h->tm_5_Z : h->tm_5_Y, h->tm_tmW13, h->tm_tmW2, s), kStageNames[6]);
   }
-  run(launch_ple(a, zout == h->Z ? h->tm_full_Z : h->tm_full_Y, h->tm_pleW, s), kStageNames[7]);
+  run(launch_ple(a, zout == h->Z ? h->tm_full_Z : h->tm_full_Y, h->tm_pleW, h->tm_Ex, s), kStageNames[7]);
   run(launch_heads(a, h->tm_headW1, s), kStageNames[8]);
   h->last_zin = zin;
   h->last_zout = zout;
@@ -1005,7 +1020,9 @@ cvr_status cvr_predict_noalloc(cvr_handle* h, int32_t n_cand, const void* y, flo
   a.done = reinterpret_cast<unsigned*>(sc + kNaErrOff + 256);
   cudaStream_t s = h->stream;
   ce = cudaMemsetAsync(sc + kNaErrOff, 0, 512, s);  // the error word and the CTA counter start at zero
-  if (ce == cudaSuccess) ce = launch_ple(a, tmY, h->tm_pleW, s);
+  CUtensorMap tmEx;
+  if (!encode_ex(&tmEx, a.Ex, (uint64_t)kNoAllocMaxCand)) return fail(h, CVR_E_CUDA, "cuTensorMapEncodeTiled failed for Ex");
+  if (ce == cudaSuccess) ce = launch_ple(a, tmY, h->tm_pleW, tmEx, s);
   if (ce == cudaSuccess) ce = launch_heads(a, h->tm_headW1, s);
   if (ce != cudaSuccess) return cuda_fail(h, ce, "prediction kernels");
   return sync_status(h);

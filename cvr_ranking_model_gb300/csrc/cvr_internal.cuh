@@ -395,7 +395,8 @@ cudaError_t launch_tokenizer(const FwdArgs& a, const CUtensorMap& tmI, const CUt
                              const CUtensorMap& tmQo, cudaStream_t s);
 cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, const CUtensorMap& tmW, cudaStream_t s);
 cudaError_t launch_attention(const FwdArgs& a, __nv_bfloat16* zin, cudaStream_t s);
-cudaError_t launch_ple(const FwdArgs& a, const CUtensorMap& tmY, const CUtensorMap& tmW, cudaStream_t s);
+cudaError_t launch_ple(const FwdArgs& a, const CUtensorMap& tmY, const CUtensorMap& tmW, const CUtensorMap& tmEx,
+                       cudaStream_t s);
 cudaError_t launch_heads(const FwdArgs& a, const CUtensorMap& tmW1, cudaStream_t s);
 
 }  // namespace cvr

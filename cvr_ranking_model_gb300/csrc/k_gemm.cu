@@ -41,7 +41,8 @@ __host__ __device__ constexpr uint32_t tmem_cols() {
 template <int BN, int STAGES, int EPI>
 __host__ __device__ constexpr int gemm_smem_bytes() {
   return 1024 + STAGES * (kATile + BN * kBK * 2) + 256 + (kPleCols + 32) * 4 +  // + PLE biases
-         (EPI == EPI_TOKENIZE ? 1024 + 2 * kBM * BN * 2 : 0);                         // + output staging (aligned)
+         (EPI == EPI_TOKENIZE ? 1024 + 2 * kBM * BN * 2                               // + output staging (aligned):
+                              : EPI == EPI_PLE ? 1024 + kBM * BN * 2 : 0);            //   two swizzled tiles / one plain
 }
 
 // Persistent GEMM: CTAs loop over 128 x BN output tiles (n fastest, so co-running CTAs share A rows in L2).
@@ -68,8 +69,8 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   float* sbias = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 256);  // PLE: biases of all columns
-  // tokeniser: two output tiles [128][BN] bf16 staged for TMA stores, as boxes of [128 rows][64 columns]
-  // with the 128-byte swizzle (1024-byte aligned)
+  // output staging for TMA stores (1024-byte aligned): tokeniser, two tiles [128][BN] bf16 as boxes of [128 rows]
+  // [64 columns] with the 128-byte swizzle; PLE, one plain [128][BN] tile
   uint8_t* sOut = reinterpret_cast<uint8_t*>(((reinterpret_cast<uintptr_t>(sbias + kPleCols + 32)) + 1023) & ~uintptr_t(1023));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -177,10 +178,15 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
       }
       if (!mbar_wait(&acc_full[buf], (i >> 1) & 1, abort_flag, a.err)) break;
       tc_fence_after();
-      uint8_t* sb = sOut + (i & 1) * (kBM * BN * 2);
-      if (EPI == EPI_TOKENIZE) {
-        // the TMA store issued from this staging buffer two tiles ago must have finished reading it
-        if (threadIdx.x == 64) bulk_wait_read<1>();
+      uint8_t* sb = sOut + (EPI == EPI_TOKENIZE ? (i & 1) * (kBM * BN * 2) : 0);
+      if (EPI == EPI_TOKENIZE || (EPI == EPI_PLE && i > 0)) {
+        // the TMA store issued from this staging buffer earlier must have finished reading it
+        if (threadIdx.x == 64) {
+          if (EPI == EPI_TOKENIZE)
+            bulk_wait_read<1>();
+          else
+            bulk_wait_read<0>();
+        }
         epi_bar<NEPI>();
       }
 #pragma unroll
@@ -219,19 +225,20 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
             dst[j] = p;
           }
         } else {  // EPI_PLE
-          if (nb < kPleN) {
-            uint4* dst = reinterpret_cast<uint4*>(a.Ex + (int64_t)row * kPleN + nb);
+          // ReLU(expert) columns of row rl into the plain [128][BN] staging tile (the TMA store clips the
+          // columns past the 768 expert outputs)
+          const int rl = q * 32 + lane;
+          uint4* rowp = reinterpret_cast<uint4*>(sb + rl * (BN * 2) + c * 64);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if (c * 32 + j * 8 >= BN || nb + j * 8 >= kPleN) break;
-              uint4 p;
-              uint32_t* pp = reinterpret_cast<uint32_t*>(&p);
+          for (int j = 0; j < 4; ++j) {
+            if (c * 32 + j * 8 >= BN) break;
+            uint4 p;
+            uint32_t* pp = reinterpret_cast<uint32_t*>(&p);
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                pp[e] = pack_bf16(fmaxf(v[8 * j + 2 * e] + add[8 * j + 2 * e], 0.f),
-                                  fmaxf(v[8 * j + 2 * e + 1] + add[8 * j + 2 * e + 1], 0.f));
-              dst[j] = p;
-            }
+            for (int e = 0; e < 4; ++e)
+              pp[e] = pack_bf16(fmaxf(v[8 * j + 2 * e] + add[8 * j + 2 * e], 0.f),
+                                fmaxf(v[8 * j + 2 * e + 1] + add[8 * j + 2 * e + 1], 0.f));
+            rowp[j] = p;
           }
           // gate logits sit in columns [768, 774): 16 columns into the chunk that starts at 752 (tiles of
           // 208 start at 624, chunks every 32 columns), a compile-time offset so v and add stay in registers
@@ -256,16 +263,20 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
           }
         }
       }
-      if (EPI == EPI_TOKENIZE) {
-        // the whole tile is staged: one thread stores it as boxes of 64 columns (tokens into Z, the first
-        // layer's queries into Q)
+      if (EPI == EPI_TOKENIZE || EPI == EPI_PLE) {
+        // the whole tile is staged: one thread stores it (tokeniser: boxes of 64 columns, tokens into Z and the
+        // first layer's queries into Q; PLE: one box of BN columns into the expert outputs)
         fence_proxy_async_smem();
         epi_bar<NEPI>();
         if (threadIdx.x == 64) {
-          const bool qcols = n0 >= kXD;
+          if (EPI == EPI_TOKENIZE) {
+            const bool qcols = n0 >= kXD;
 #pragma unroll
-          for (int bx = 0; bx < BN / 64; ++bx)
-            tma_store_2d(qcols ? &tmQo : &tmZo, sb + bx * (kBM * 128), (qcols ? n0 - kXD : n0) + bx * 64, m0);
+            for (int bx = 0; bx < BN / 64; ++bx)
+              tma_store_2d(qcols ? &tmQo : &tmZo, sb + bx * (kBM * 128), (qcols ? n0 - kXD : n0) + bx * 64, m0);
+          } else {
+            tma_store_2d(&tmZo, sb, n0, m0);
+          }
           bulk_commit();
         }
       }
@@ -273,7 +284,7 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
-    if (EPI == EPI_TOKENIZE && threadIdx.x == 64) bulk_wait_all();  // the stores have landed before exit
+    if ((EPI == EPI_TOKENIZE || EPI == EPI_PLE) && threadIdx.x == 64) bulk_wait_all();  // stores landed before exit
   }
   tc_fence_before();
   __syncthreads();
@@ -428,7 +439,7 @@ cudaError_t launch_gemm(const FwdArgs& a, const CUtensorMap& tmA, const CUtensor
 
 constexpr int kTokBN = 128, kTokStages = 4, kTokEpi = 8;
 constexpr int kQryBN = 96, kQryStages = 6, kQryEpi = 8;
-constexpr int kPleBN = 208, kPleStages = 5, kPleEpi = 8;
+constexpr int kPleBN = 208, kPleStages = 4, kPleEpi = 8;
 static_assert(kPleCols % kPleBN == 0, "PLE columns are a whole number of tiles");
 
 }  // namespace
@@ -452,8 +463,10 @@ cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, co
   return launch_gemm<kQryBN, kQryStages, EPI_QUERY, kQryEpi>(a, tmX, tmW, tmX, tmX, a.B, kG * kD, kXD, layer, s);
 }
 
-cudaError_t launch_ple(const FwdArgs& a, const CUtensorMap& tmY, const CUtensorMap& tmW, cudaStream_t s) {
-  return launch_gemm<kPleBN, kPleStages, EPI_PLE, kPleEpi>(a, tmY, tmW, tmY, tmY, a.B, kPleCols, kYD, 0, s);
+cudaError_t launch_ple(const FwdArgs& a, const CUtensorMap& tmY, const CUtensorMap& tmW, const CUtensorMap& tmEx,
+                       cudaStream_t s) {
+  static_assert(gemm_smem_bytes<kPleBN, kPleStages, EPI_PLE>() <= 232448, "PLE staging fits");
+  return launch_gemm<kPleBN, kPleStages, EPI_PLE, kPleEpi>(a, tmY, tmW, tmEx, tmEx, a.B, kPleCols, kYD, 0, s);
 }
 
 cudaError_t launch_heads(const FwdArgs& a, const CUtensorMap& tmW1, cudaStream_t s) {
