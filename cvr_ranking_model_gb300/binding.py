@@ -16,7 +16,7 @@ from . import _build
 
 MAX_LAYERS, N_USER_FIELDS, N_ITEM_FIELDS, N_GROUPS, N_EXPERTS, N_TASKS = 4, 8, 8, 3, 3, 2
 STAGE_H, STAGE_Z, STAGE_Q, STAGE_Y, STAGE_EXPERTS, STAGE_GATES = range(6)
-OPT_PROFILE, OPT_CUDA_GRAPH, OPT_PDL = 0, 1, 2
+OPT_PROFILE, OPT_CUDA_GRAPH, OPT_PDL, OPT_ATTENTION_TC = 0, 1, 2, 3
 NOALLOC_MAX_CAND = 1024  # CVR_NOALLOC_MAX_CAND
 
 STATUS = {0: "CVR_OK", 1: "CVR_E_ARG", 2: "CVR_E_SHAPE", 3: "CVR_E_ID_RANGE", 4: "CVR_E_OOM", 5: "CVR_E_CUDA",

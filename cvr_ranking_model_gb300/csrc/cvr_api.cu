@@ -99,9 +99,10 @@ struct cvr_handle {
   size_t stage_bytes = 0;
   // tensor maps
   CUtensorMap tm_seqW13, tm_seqW2, tm_tokI, tm_qW[kMaxLayers], tm_tmW13, tm_tmW2, tm_pleW, tm_headW1;
-  CUtensorMap tm_Xs, tm_I, tm_x_Z, tm_x_Y, tm_5_Z, tm_5_Y, tm_full_Z, tm_full_Y, tm_Q, tm_Ex;
+  CUtensorMap tm_Xs, tm_I, tm_x_Z, tm_x_Y, tm_5_Z, tm_5_Y, tm_full_Z, tm_full_Y, tm_Q, tm_H, tm_Ex;
   // graphs, profiling
   bool use_graph = true, profile = false, pdl = true;
+  bool attn_tc = false;  // cross-attention on the tcgen05 kernel instead of the register-tile one
   std::map<std::pair<int, int>, GraphEntry> graphs;
   std::vector<cudaEvent_t> events;
   std::vector<const char*> event_names;
@@ -233,6 +234,12 @@ cvr_status free_workspace(cvr_handle* h) {
   return CVR_OK;
 }
 
+// merge counters of either attention kernel: one per (32-candidate tile, group), or one per (128-candidate
+// tile, group, softmax warp)
+size_t attn_count_bytes(int B_cap) {
+  return std::max((size_t)(B_cap + 31) / 32 * kG, (size_t)(B_cap + 127) / 128 * kG * kAttnCounters) * 4;
+}
+
 cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   if (R <= h->R_cap && B <= h->B_cap) return CVR_OK;
   free_workspace(h);
@@ -256,9 +263,14 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   const size_t oG = take((size_t)B_cap * 8 * 4), oErr = take(1024), oCnt = take((size_t)R_cap * kG * 4);
   int splits = 1;
   for (int g = 0; g < kG; ++g) splits = std::max(splits, split_count(h->L[g]));
-  const size_t n_tiles32 = (size_t)(B_cap + 31) / 32;
-  const size_t oAst = splits > 1 ? take(n_tiles32 * kG * splits * 256 * 20 * 4) : 0;
-  const size_t oAcnt = take(n_tiles32 * kG * 4);
+  // attention split state and merge counters, sized for either attention kernel: the register-tile one keeps
+  // 20 floats per thread of 256 per 32-candidate tile, the tcgen05 one m[4], l[4], O[4][32] per row of a
+  // 128-candidate tile and one counter per softmax warp
+  const size_t st_bytes = std::max((size_t)(B_cap + 31) / 32 * kG * splits * 256 * 20 * 4,
+                                   (size_t)(B_cap + 127) / 128 * kG * splits * 128 * kAttnStateFloats * 4);
+  const size_t cnt_bytes = attn_count_bytes(B_cap);
+  const size_t oAst = splits > 1 ? take(st_bytes) : 0;
+  const size_t oAcnt = take(cnt_bytes);
   cudaError_t e = cudaMalloc(&h->ws, off);
   if (e != cudaSuccess) {
     h->ws = nullptr;
@@ -286,7 +298,7 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   h->attn_count = (unsigned*)(b + oAcnt);
   e = cudaMemset(h->err, 0, 1024);  // error word and CTA counter start at zero; the last kernel resets them
   if (e == cudaSuccess) e = cudaMemset(h->cs_count, 0, (size_t)R_cap * kG * 4);  // reset by their last block
-  if (e == cudaSuccess) e = cudaMemset(h->attn_count, 0, n_tiles32 * kG * 4);  // reset by the merging CTA
+  if (e == cudaSuccess) e = cudaMemset(h->attn_count, 0, cnt_bytes);  // reset by the merging CTA or warp
   if (e != cudaSuccess) {
     free_workspace(h);
     return fail(h, CVR_E_CUDA, "workspace initialisation failed");
@@ -301,6 +313,7 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
             encode_mix5d(&h->tm_5_Y, h->Y, B_cap) && encode_2d(&h->tm_full_Z, h->Z, kYD, B_cap, kYD, 64, 128) &&
             encode_2d(&h->tm_full_Y, h->Y, kYD, B_cap, kYD, 64, 128) &&
             encode_2d(&h->tm_Q, h->Q, kG * kD, B_cap, kG * kD, 64, 128) &&
+            encode_2d(&h->tm_H, h->H, kD, (uint64_t)seq_rows, kD, 64, 64) &&
             encode_ex(&h->tm_Ex, h->Ex, B_cap);
   if (!ok) {
     free_workspace(h);
@@ -411,7 +424,7 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
     const bool in_is_Z = zin == h->Z;
     // the first layer's queries come out of the tokeniser
     if (l > 0) run(launch_query(a, l, in_is_Z ? h->tm_x_Z : h->tm_x_Y, h->tm_qW[l], s), kStageNames[4]);
-    run(launch_attention(a, zin, s), kStageNames[5]);
+    run(h->attn_tc ? launch_attention_tc(a, h->tm_Q, h->tm_H, zin, s) : launch_attention(a, zin, s), kStageNames[5]);
     run(launch_tm_mlp(a, l, zin, zout, in_is_Z ? h->tm_5_Z : h->tm_5_Y, h->tm_tmW13, h->tm_tmW2, s), kStageNames[6]);
   }
   run(launch_ple(a, zout == h->Z ? h->tm_full_Z : h->tm_full_Y, h->tm_pleW, h->tm_Ex, s), kStageNames[7]);
@@ -504,7 +517,12 @@ cvr_status sync_status(cvr_handle* h) {
   volatile int* hw = h->err_host;
   const int ew = *hw;
   *hw = 0;
-  if (ew & kErrTimeout) return fail(h, CVR_E_TIMEOUT, "a bounded device-side wait gave up");
+  if (ew & kErrTimeout) {
+    // a CTA that gave up may have left a group or split counter part-way; the next call starts from zero
+    if (h->cs_count) cudaMemset(h->cs_count, 0, (size_t)h->R_cap * kG * 4);
+    if (h->attn_count) cudaMemset(h->attn_count, 0, attn_count_bytes(h->B_cap));
+    return fail(h, CVR_E_TIMEOUT, "a bounded device-side wait gave up");
+  }
   if (ew & kErrLayout) return fail(h, CVR_E_CUDA, "a kernel's shared-memory window was not 1024-byte aligned");
   if (ew & kErrSeqLens) return fail(h, CVR_E_INPUT, "a sequence length is outside [0, seq_len[g]]");
   if (ew & (kErrOffsets | kErrReqIds))
@@ -571,6 +589,7 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
     cudaError_t pe = prepare_gemm_kernels();
     if (pe == cudaSuccess) pe = prepare_mlp_kernels();
     if (pe == cudaSuccess) pe = prepare_attention_kernel();
+    if (pe == cudaSuccess) pe = prepare_attention_tc_kernel();
     if (pe != cudaSuccess) {
       fprintf(stderr, "cvr_create: kernel attribute setup failed: %s\n", cudaGetErrorString(pe));
       cudaGetLastError();
@@ -869,8 +888,9 @@ cvr_status cvr_set_option(cvr_handle* h, int32_t option, int64_t value) {
     h->use_graph = value != 0;
     return CVR_OK;
   }
-  if (option == CVR_OPT_PDL) {
-    h->pdl = value != 0;
+  if (option == CVR_OPT_PDL || option == CVR_OPT_ATTENTION_TC) {
+    if (option == CVR_OPT_PDL) h->pdl = value != 0;
+    else h->attn_tc = value != 0;
     for (auto& kv : h->graphs)
       if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
     h->graphs.clear();

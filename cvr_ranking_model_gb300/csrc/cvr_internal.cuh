@@ -37,6 +37,8 @@ constexpr int kMaxLayers = 4;
 // cross-attention over long sequences: a CTA takes at most kChunksPerSplit chunks of 64 positions; a
 // group longer than that is split over up to kMaxSplits CTAs whose softmax states are merged
 constexpr int kAttnChunk = 64, kChunksPerSplit = 8, kMaxSplits = 8;
+constexpr int kAttnStateFloats = 2 * kHeads + kHeads * kHD;  // split state of one candidate row: m, l, O
+constexpr int kAttnCounters = 8;  // merge counters per (128-candidate tile, group): one per softmax warp
 __host__ __device__ constexpr int split_count(int L) {
   return L <= kAttnChunk * kChunksPerSplit ? 1
          : ((L + kAttnChunk * kChunksPerSplit - 1) / (kAttnChunk * kChunksPerSplit) < kMaxSplits
@@ -83,8 +85,11 @@ struct FwdArgs {
   float* colsum;          // [R][G][max_chunks][128] partial column sums of H
   unsigned* cs_count;     // [R][G] blocks of the column-sum kernel done (zero between calls)
   const int32_t* seq_lens;  // [R][G] events each request really has per group, or null (all L[g])
-  float* attn_state;       // [B/32][G][attn_splits][256 threads][20] partial softmax states of split sequences
-  unsigned* attn_count;    // [B/32][G] split CTAs done (zero between calls)
+  // partial softmax states of split sequences and the merge counters (zero between calls), laid out by the
+  // attention kernel in use: register-tile kernel [B/32][G][splits][256 threads][20] and [B/32][G];
+  // tcgen05 kernel [B/128][G][splits][128 rows][m 4, l 4, O 4x32] and [B/128][G][8 softmax warps]
+  float* attn_state;
+  unsigned* attn_count;
   int attn_splits;         // splits of the longest group (grid z of the attention kernel)
   int max_chunks;
   float* xu;              // [R][1664] user half of the tokeniser (+ bias)
@@ -156,6 +161,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       return false;
     }
   }
+}
+// The same wait taken by a whole warp, with one answer for all of its lanes: code that follows it with
+// warp-collective instructions (tcgen05.ld/st) never runs with part of the warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, err));
+}
+// After an abort: wait (bounded, ignoring the abort flag) for copies or MMAs this CTA itself issued, so that
+// none lands in shared memory or TMEM after they are released.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > 1000000000ull) return false;
+  return true;
 }
 // Events that request r really has in group g (variable-length sequences); kept in [0, L[g]] so that no
 // access ever leaves the padded layout (the sparse kernel reports a value outside that range).
@@ -385,6 +403,7 @@ inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, 
 cudaError_t prepare_gemm_kernels();  // shared-memory attributes; once per device before any launch
 cudaError_t prepare_mlp_kernels();
 cudaError_t prepare_attention_kernel();
+cudaError_t prepare_attention_tc_kernel();
 cudaError_t launch_sparse(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_seq_colsum(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_seq_mlp(const FwdArgs& a, const CUtensorMap& tmXs, const CUtensorMap& tmW13,
@@ -395,6 +414,8 @@ cudaError_t launch_tokenizer(const FwdArgs& a, const CUtensorMap& tmI, const CUt
                              const CUtensorMap& tmQo, cudaStream_t s);
 cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, const CUtensorMap& tmW, cudaStream_t s);
 cudaError_t launch_attention(const FwdArgs& a, __nv_bfloat16* zin, cudaStream_t s);
+cudaError_t launch_attention_tc(const FwdArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmH, __nv_bfloat16* zin,
+                                cudaStream_t s);
 cudaError_t launch_ple(const FwdArgs& a, const CUtensorMap& tmY, const CUtensorMap& tmW, const CUtensorMap& tmEx,
                        cudaStream_t s);
 cudaError_t launch_heads(const FwdArgs& a, const CUtensorMap& tmW1, cudaStream_t s);

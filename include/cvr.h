@@ -177,12 +177,16 @@ enum { CVR_STAGE_H = 0, CVR_STAGE_Z = 1, CVR_STAGE_Q = 2, CVR_STAGE_Y = 3, CVR_S
 cvr_status cvr_debug_stage(cvr_handle* h, int32_t stage, void* dst, int64_t bytes);
 
 /* Options (cvr_set_option):
+ *   CVR_OPT_ATTENTION_TC 1 = cross-attention on the tcgen05 kernel (S and O accumulated in tensor memory, one
+ *                            CTA per 128 candidates and group); 0 = on the register-tile kernel (default 0:
+ *                            with heads 32 wide its many small MMAs keep up better; both meet the same
+ *                            tolerance)
  *   CVR_OPT_PROFILE      1 = record a CUDA event after every kernel of a call (read with cvr_stage_times)
  *   CVR_OPT_CUDA_GRAPH   1 = replay the call's kernel sequence from a CUDA graph captured per (n_req, n_cand)
  *                            (default 1); 0 = launch eagerly
  *   CVR_OPT_PDL          1 = launch each kernel with programmatic dependent launch, so its prologue overlaps
  *                            the previous kernel (default 1); 0 = plain stream order */
-enum { CVR_OPT_PROFILE = 0, CVR_OPT_CUDA_GRAPH = 1, CVR_OPT_PDL = 2 };
+enum { CVR_OPT_PROFILE = 0, CVR_OPT_CUDA_GRAPH = 1, CVR_OPT_PDL = 2, CVR_OPT_ATTENTION_TC = 3 };
 cvr_status cvr_set_option(cvr_handle* h, int32_t option, int64_t value);
 
 /* With CVR_OPT_PROFILE set: per-kernel device times of the last call, in launch order. Writes up to
