@@ -8,7 +8,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from typing import Dict, Mapping, Optional, Sequence
+from typing import Dict, Mapping, Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -94,6 +94,10 @@ def lib() -> ctypes.CDLL:
         L.cvr_selftest_wait_timeout.restype = ctypes.c_int
         L.cvr_predict_noalloc.argtypes = [V, i32, V, V]
         L.cvr_predict_noalloc.restype = ctypes.c_int
+        L.cvr_cache_enable.argtypes = [V, i32, i64]
+        L.cvr_cache_enable.restype = ctypes.c_int
+        L.cvr_cache_stats.argtypes = [V, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        L.cvr_cache_stats.restype = ctypes.c_int
         L.cvr_destroy.argtypes = [V]
         L.cvr_destroy.restype = None
         _lib = L
@@ -230,6 +234,20 @@ class Scorer:
         if check:
             self._check(st)
         return st
+
+    def cache_enable(self, table: int, slots: int, check: bool = True) -> int:
+        """cvr_cache_enable: a hot-row cache of `slots` rows (power of two, 0 = none) in front of table
+        0..7 (user), 8..15 (item) or 16 (sequence)."""
+        st = self._lib.cvr_cache_enable(self._h, table, slots)
+        if check:
+            self._check(st)
+        return st
+
+    def cache_stats(self) -> Tuple[int, int]:
+        """cvr_cache_stats: (hits, misses) since the last read."""
+        hits, misses = ctypes.c_int64(0), ctypes.c_int64(0)
+        self._check(self._lib.cvr_cache_stats(self._h, ctypes.byref(hits), ctypes.byref(misses)))
+        return int(hits.value), int(misses.value)
 
     def debug_stage(self, stage: int, dst: int, nbytes: int) -> None:
         self._check(self._lib.cvr_debug_stage(self._h, stage, dst, nbytes))

@@ -60,7 +60,7 @@ struct GraphEntry {
 };
 
 const char* kStageNames[] = {"sparse", "seq_mlp", "seq_colsum", "tokenizer", "query", "attention", "token_mixer", "ple",
-                             "heads"};
+                             "heads", "cache_admit"};
 
 }  // namespace
 
@@ -103,6 +103,15 @@ struct cvr_handle {
   // graphs, profiling
   bool use_graph = true, profile = false, pdl = true;
   bool attn_tc = false;  // cross-attention on the tcgen05 kernel instead of the register-tile one
+  // hot-row caches in HBM, per table (slots == 0: none)
+  int64_t c_slots[kNTab] = {};
+  float* c_rows[kNTab] = {};
+  int64_t* c_tags[kNTab] = {};
+  unsigned* c_use[kNTab] = {};
+  unsigned* c_claim[kNTab] = {};
+  int64_t* miss_list = nullptr;
+  unsigned* cache_ctl = nullptr;             // misses logged, epoch, admission block counter
+  unsigned long long* cache_stat = nullptr;  // hits, misses
   std::map<std::pair<int, int>, GraphEntry> graphs;
   std::vector<cudaEvent_t> events;
   std::vector<const char*> event_names;
@@ -322,6 +331,30 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   return CVR_OK;
 }
 
+constexpr int kMissCap = 1 << 20;  // rows a call can log for admission (more misses are served, not admitted)
+
+int ilog2(int64_t v) {
+  int k = 0;
+  while ((int64_t(1) << k) < v) ++k;
+  return k;
+}
+
+void free_cache(cvr_handle* h, int t) {
+  for (void* p : {(void*)h->c_rows[t], (void*)h->c_tags[t], (void*)h->c_use[t], (void*)h->c_claim[t]})
+    if (p) cudaFree(p);
+  h->c_rows[t] = nullptr;
+  h->c_tags[t] = nullptr;
+  h->c_use[t] = nullptr;
+  h->c_claim[t] = nullptr;
+  h->c_slots[t] = 0;
+}
+
+void drop_graphs(cvr_handle* h) {
+  for (auto& kv : h->graphs)
+    if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+  h->graphs.clear();
+}
+
 FwdArgs make_args(cvr_handle* h, int R, int B, const int32_t* req_ids, const int64_t* bag_ids,
                   const int64_t* bag_offsets, const int64_t* seq_ids, float* out, float* dbg_pooled,
                   int64_t* dbg_rows) {
@@ -359,6 +392,18 @@ FwdArgs make_args(cvr_handle* h, int R, int B, const int32_t* req_ids, const int
   a.H = h->H;
   a.colsum = h->colsum;
   a.cs_count = h->cs_count;
+  for (int t = 0; t < kNTab; ++t) {
+    if (!h->c_slots[t]) continue;
+    a.cache_on = 1;
+    a.cache_rows[t] = h->c_rows[t];
+    a.cache_tags[t] = h->c_tags[t];
+    a.cache_use[t] = h->c_use[t];
+    a.cache_shift[t] = 64 - ilog2(h->c_slots[t]);
+  }
+  a.miss_list = h->miss_list;
+  a.miss_cap = kMissCap;
+  a.cache_ctl = h->cache_ctl;
+  a.cache_stat = h->cache_stat;
   a.attn_state = h->attn_state;
   a.attn_count = h->attn_count;
   a.attn_splits = h->attn_splits;
@@ -429,6 +474,10 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
   }
   run(launch_ple(a, zout == h->Z ? h->tm_full_Z : h->tm_full_Y, h->tm_pleW, h->tm_Ex, s), kStageNames[7]);
   run(launch_heads(a, h->tm_headW1, s), kStageNames[8]);
+  if (a.cache_on) {
+    run(launch_cache_admit(a, h->c_claim, s), kStageNames[9]);
+    ++n;  // (two kernels)
+  }
   h->last_zin = zin;
   h->last_zout = zout;
   if (launches) *launches = n;
@@ -891,9 +940,7 @@ cvr_status cvr_set_option(cvr_handle* h, int32_t option, int64_t value) {
   if (option == CVR_OPT_PDL || option == CVR_OPT_ATTENTION_TC) {
     if (option == CVR_OPT_PDL) h->pdl = value != 0;
     else h->attn_tc = value != 0;
-    for (auto& kv : h->graphs)
-      if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
-    h->graphs.clear();
+    drop_graphs(h);
     return CVR_OK;
   }
   return fail(h, CVR_E_ARG, "unknown option");
@@ -915,11 +962,72 @@ cvr_status cvr_stage_times(cvr_handle* h, float* ms, const char** names, int32_t
   return CVR_OK;
 }
 
+cvr_status cvr_cache_enable(cvr_handle* h, int32_t table, int64_t slots) {
+  if (!h) return CVR_E_ARG;
+  if (table < 0 || table >= kNTab) return fail(h, CVR_E_ARG, "table index outside [0, 17)");
+  if (slots != 0 && (slots < 1024 || slots > (int64_t(1) << 28) || (slots & (slots - 1))))
+    return fail(h, CVR_E_ARG, "cache slots must be 0 or a power of two in [1024, 2^28]");
+  cudaError_t ce = cudaSetDevice(h->device);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(h->stream);  // no call in flight still reads the old cache
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "cache setup");
+  free_cache(h, table);
+  drop_graphs(h);  // captured calls hold the old cache's pointers
+  if (slots == 0) return CVR_OK;
+  if (!h->miss_list) {
+    void* ctl = nullptr;
+    ce = cudaMalloc(&h->miss_list, (size_t)kMissCap * 8);
+    if (ce == cudaSuccess) ce = cudaMalloc(&ctl, 64);
+    if (ce == cudaSuccess) ce = cudaMemset(ctl, 0, 64);
+    const unsigned first_epoch = 1;  // slot epochs start at 0: no slot counts as read before its first hit
+    if (ce == cudaSuccess) ce = cudaMemcpy((unsigned*)ctl + 1, &first_epoch, 4, cudaMemcpyHostToDevice);
+    if (ce != cudaSuccess) {
+      if (h->miss_list) cudaFree(h->miss_list);
+      if (ctl) cudaFree(ctl);
+      h->miss_list = nullptr;
+      cudaGetLastError();
+      return fail(h, CVR_E_OOM, "cache miss log allocation failed");
+    }
+    h->cache_ctl = (unsigned*)ctl;
+    h->cache_stat = (unsigned long long*)((uint8_t*)ctl + 16);
+  }
+  ce = cudaMalloc(&h->c_rows[table], (size_t)slots * kE * 4);
+  if (ce == cudaSuccess) ce = cudaMalloc(&h->c_tags[table], (size_t)slots * 8);
+  if (ce == cudaSuccess) ce = cudaMalloc(&h->c_use[table], (size_t)slots * 4);
+  if (ce == cudaSuccess) ce = cudaMalloc(&h->c_claim[table], (size_t)slots * 4);
+  if (ce == cudaSuccess) ce = cudaMemset(h->c_tags[table], 0xFF, (size_t)slots * 8);  // -1: empty
+  if (ce == cudaSuccess) ce = cudaMemset(h->c_use[table], 0, (size_t)slots * 4);
+  if (ce == cudaSuccess) ce = cudaMemset(h->c_claim[table], 0, (size_t)slots * 4);
+  if (ce != cudaSuccess) {
+    free_cache(h, table);
+    cudaGetLastError();
+    return fail(h, CVR_E_OOM, "cache allocation failed");
+  }
+  h->c_slots[table] = slots;
+  return CVR_OK;
+}
+
+cvr_status cvr_cache_stats(cvr_handle* h, int64_t* hits, int64_t* misses) {
+  if (!h || !hits || !misses) return CVR_E_ARG;
+  *hits = *misses = 0;
+  if (!h->cache_stat) return CVR_OK;
+  unsigned long long v[2] = {0, 0};
+  cudaError_t ce = cudaStreamSynchronize(h->stream);
+  if (ce == cudaSuccess) ce = cudaMemcpy(v, h->cache_stat, 16, cudaMemcpyDeviceToHost);
+  if (ce == cudaSuccess) ce = cudaMemset(h->cache_stat, 0, 16);
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "cache statistics");
+  *hits = (int64_t)v[0];
+  *misses = (int64_t)v[1];
+  return CVR_OK;
+}
+
 void cvr_destroy(cvr_handle* h) {
   if (!h) return;
   cudaSetDevice(h->device);
   if (h->stream) cudaStreamSynchronize(h->stream);
   free_workspace(h);
+  for (int t = 0; t < kNTab; ++t) free_cache(h, t);
+  if (h->miss_list) cudaFree(h->miss_list);
+  if (h->cache_ctl) cudaFree(h->cache_ctl);
   if (h->stage) cudaFree(h->stage);
   if (h->wblob) cudaFree(h->wblob);
   if (h->err_host) cudaFreeHost(h->err_host);

@@ -14,6 +14,7 @@ namespace cvr {
 constexpr int kFu = 8;            // user/context fields (one bag per request)
 constexpr int kFi = 8;            // item fields (one bag per candidate)
 constexpr int kE = 32;            // embedding width
+constexpr int kNTab = 8 + 8 + 1;  // embedding tables: user fields, item fields, the shared sequence table
 constexpr int kUD = kFu * kE;     // 256: user half of the non-sequence embedding
 constexpr int kID = kFi * kE;     // 256: item half
 constexpr int kN = 13;            // non-sequence tokens
@@ -102,6 +103,16 @@ struct FwdArgs {
   int* err;               // device error word (bits below), reset by the last kernel of each call
   unsigned* done;         // CTA counter of the last kernel (finds the CTA that publishes the error word)
   int* err_host;          // device view of a pinned host word: the call's error bits are OR-ed into it
+  // hot-row cache in HBM in front of embedding tables (per table; null tags = no cache for that table)
+  int cache_on;                      // any table has a cache
+  const float* cache_rows[kNTab];      // [slots][32] fp32 copies of table rows
+  const int64_t* cache_tags[kNTab];    // [slots] the id held by each slot, -1 = empty
+  unsigned* cache_use[kNTab];          // [slots] epoch of the last call that read the slot
+  int cache_shift[kNTab];              // slot = (id * golden) >> shift, slots = 2^(64 - shift)
+  int64_t* miss_list;                // [miss_cap] (table << 48 | id) of rows that missed this call
+  int miss_cap;
+  unsigned* cache_ctl;               // [0] misses logged this call, [1] epoch of this call, [2] admit counter
+  unsigned long long* cache_stat;    // [0] hits, [1] misses, accumulated until read
   // packed weights (device)
   const __nv_bfloat16* tokU;   // [1664][256]
   const float* tok_b;          // [1664]
@@ -419,5 +430,8 @@ cudaError_t launch_attention_tc(const FwdArgs& a, const CUtensorMap& tmQ, const 
 cudaError_t launch_ple(const FwdArgs& a, const CUtensorMap& tmY, const CUtensorMap& tmW, const CUtensorMap& tmEx,
                        cudaStream_t s);
 cudaError_t launch_heads(const FwdArgs& a, const CUtensorMap& tmW1, cudaStream_t s);
+// hot-row cache admission after a call: rows that missed replace their slot's row unless that row was read
+// in the same call; claims [kNTab] are the per-table election arrays (zero between calls)
+cudaError_t launch_cache_admit(const FwdArgs& a, unsigned* const* claims, cudaStream_t s);
 
 }  // namespace cvr

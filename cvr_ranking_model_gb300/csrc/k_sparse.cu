@@ -5,6 +5,8 @@
 //                      clamp and bf16 cast after the lookup (GPU CTR inference article, section 三),
 //                      plus the sequence-event gather from the shared id table (iQIYI 3.2.1): one launch
 //                      for every lookup of the batch (iQIYI 3.4.2).
+//  cache admission     the hot-row cache in HBM in front of tables kept in host memory (GPU CTR inference
+//                      article, section 二: hot rows in HBM as the first tier, misses served from host DRAM)
 //  seq_colsum_kernel   partial column sums of the encoded sequences; the last block of each (request, group)
 //                      forms the mean-pooled sequence vector and the mean-pool half of that group's query
 //                      FFN, once per request (Query Decoding, iQIYI 3.2.3; the lazy user repeat of 3.4.5).
@@ -26,10 +28,54 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float4 v) {
   *reinterpret_cast<uint2*>(dst) = p;
 }
 
+// ---- hot-row cache: direct-mapped, slot = Fibonacci hash of the id. The cache is read-only during a call;
+// a hit stamps the slot with the call's epoch, a miss reads the table row itself (host memory over C2C, or
+// HBM) and logs (table, id) for admission after the call. Cached rows are exact copies, so a hit and a miss
+// give the same bits.
+constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ull;
+
+__device__ __forceinline__ int64_t cache_slot(int64_t id, int shift) {
+  return (int64_t)(((uint64_t)id * kGolden) >> shift);
+}
+
+// Where the row of `id` in table t is read from; `hit`/`miss` say whether the table has a cache and which.
+__device__ __forceinline__ const float* row_src(const FwdArgs& a, int t, int64_t id, unsigned epoch, bool mark,
+                                                bool& hit, bool& miss) {
+  const float* row = a.tables[t] + id * kE;
+  const int64_t* tags = a.cache_tags[t];
+  if (!tags) return row;
+  const int64_t slot = cache_slot(id, a.cache_shift[t]);
+  if (__ldcg(tags + slot) == id) {
+    hit = true;
+    if (mark) a.cache_use[t][slot] = epoch;
+    return a.cache_rows[t] + slot * kE;
+  }
+  miss = true;
+  return row;
+}
+
+// Logs the lanes' misses with one atomic per warp (entries past the log's capacity are not admitted).
+__device__ __forceinline__ void log_misses(const FwdArgs& a, bool miss, int t, int64_t id, int lane) {
+  const unsigned mb = __ballot_sync(0xffffffffu, miss);
+  if (!mb) return;
+  const int leader = __ffs(mb) - 1;
+  unsigned base = 0;
+  if (lane == leader) base = atomicAdd(a.cache_ctl, (unsigned)__popc(mb));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  const unsigned idx = base + __popc(mb & ((1u << lane) - 1u));
+  if (miss && idx < (unsigned)a.miss_cap) a.miss_list[idx] = ((int64_t)t << 48) | id;
+}
+
+__device__ __forceinline__ float4 ld_row(const float* p, int part, bool coherent) {
+  return coherent ? __ldcg(reinterpret_cast<const float4*>(p) + part) : __ldg(reinterpret_cast<const float4*>(p) + part);
+}
+
 // Persistent and software-pipelined: every warp walks units with a grid stride -- units of 4 bags (8 lanes
 // per bag, each lane 4 of the 32 columns), then single sequence events -- and while the table rows of unit k
 // are in flight it already loads the ids of unit k+1 and the offsets of unit k+2, so the three dependent
 // round trips of a lookup (offsets -> ids -> rows) overlap instead of adding up.
+// kCache: some table has a hot-row cache (a separate instantiation keeps the plain path's registers as they are)
+template <bool kCache>
 __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_kernel(const __grid_constant__ FwdArgs a) {
   const int tid = threadIdx.x, lane = tid & 31;
   const int64_t gw = (int64_t)blockIdx.x * (kSparseThreads / 32) + (tid >> 5);
@@ -45,6 +91,10 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
     if (bad) atomicOr(a.err, kErrReqIds);
   }
   int errbits = 0;
+  // with a cache, rows are read through L2 only (the admission after the previous call rewrote slots)
+  constexpr bool cached = kCache;
+  const unsigned epoch = cached ? a.cache_ctl[1] : 0u;
+  unsigned long long n_hit = 0, n_miss = 0;
 
   // ---------------------------------------------------------------- embedding bags
   {
@@ -90,7 +140,6 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
         field = kFu + f;
         dst = a.I + (ib / kFi) * kID + f * kE;
       }
-      const float* table = a.tables[field];
       const int64_t rows = a.table_rows[field];
       const int64_t s = s0;
       int64_t e = e0;
@@ -108,6 +157,8 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
       for (int64_t base = 0; base < nmax; base += 8) {
         const int64_t j = s + base + sub;
         int64_t mine = 0;
+        const float* src = a.tables[field];
+        bool hit = false, miss = false;
         if (j < e) {
           mine = base == 0 ? id0 : a.bag_ids[j];
           if (mine < 0 || mine >= rows) {
@@ -115,13 +166,21 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
             mine = 0;
           }
           if (a.dbg_rows && live) a.dbg_rows[j] = mine;
+          src = kCache ? row_src(a, field, mine, epoch, live, hit, miss) : src + mine * kE;
         }
+        if (cached) {
+          miss = miss && live;
+          n_hit += hit && live;
+          n_miss += miss;
+          log_misses(a, miss, field, mine, lane);
+        }
+        // the 8 lanes of a bag exchange row addresses (cache slot or table row) instead of ids
         float4 v[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const int64_t id = __shfl_sync(0xffffffffu, (long long)mine, u, 8);
+          const float* p = reinterpret_cast<const float*>(__shfl_sync(0xffffffffu, (long long)src, u, 8));
           v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (s + base + u < e) v[u] = __ldg(reinterpret_cast<const float4*>(table + id * kE) + sub);
+          if (s + base + u < e) v[u] = ld_row(p, sub, cached);
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -186,14 +245,25 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
         if (l == 0 && lane == 0 && (raw < 0 || raw > a.L[g])) errbits |= kErrSeqLens;
         pad = l >= seq_len_of(a, r, g);  // padding: its id is never looked up; encoded from zeros, never used
       }
-      if (pad) {
-        store_bf16x4(out, make_float4(0.f, 0.f, 0.f, 0.f));
-      } else {
+      bool hit = false, miss = false;
+      const float* src = nullptr;
+      if (!pad) {
         if (id < 0 || id >= a.table_rows[kFu + kFi]) {
           errbits |= kErrIdRange;
           id = 0;
         }
-        float4 v = __ldg(reinterpret_cast<const float4*>(a.tables[kFu + kFi] + id * kE) + part);
+        src = kCache ? row_src(a, kFu + kFi, id, epoch, part == 0, hit, miss) : a.tables[kFu + kFi] + id * kE;
+      }
+      if (cached) {  // one lane of each id's 8 counts and logs
+        miss = miss && part == 0;
+        n_hit += hit && part == 0;
+        n_miss += miss;
+        log_misses(a, miss, kFu + kFi, id, lane);
+      }
+      if (pad) {
+        store_bf16x4(out, make_float4(0.f, 0.f, 0.f, 0.f));
+      } else {
+        float4 v = ld_row(src, part, cached);
         v.x = clampf(v.x, a.clamp);
         v.y = clampf(v.y, a.clamp);
         v.z = clampf(v.z, a.clamp);
@@ -204,6 +274,69 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
     }
   }
   if (errbits) atomicOr(a.err, errbits);
+  if (cached) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      n_hit += __shfl_xor_sync(0xffffffffu, n_hit, o);
+      n_miss += __shfl_xor_sync(0xffffffffu, n_miss, o);
+    }
+    if (lane == 0 && (n_hit | n_miss)) {
+      atomicAdd(a.cache_stat, n_hit);
+      atomicAdd(a.cache_stat + 1, n_miss);
+    }
+  }
+}
+
+struct Claims {
+  unsigned* p[kNTab];
+};
+
+// Admission, step 1: every logged miss whose slot was not read this call bids for it; the highest log index
+// wins, so that exactly one row lands in each contested slot.
+__global__ void __launch_bounds__(256) cache_claim_kernel(const __grid_constant__ FwdArgs a, Claims c) {
+  pdl_trigger();
+  pdl_wait();
+  const unsigned n = min(a.cache_ctl[0], (unsigned)a.miss_cap), epoch = a.cache_ctl[1];
+  for (unsigned i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int64_t e = a.miss_list[i];
+    const int t = (int)(e >> 48);
+    const int64_t id = e & ((int64_t(1) << 48) - 1);
+    const int64_t slot = cache_slot(id, a.cache_shift[t]);
+    if (a.cache_use[t][slot] != epoch) atomicMax(c.p[t] + slot, i + 1);
+  }
+}
+
+// Admission, step 2: one warp per logged miss; the winner of a slot copies the row (32 floats) from the
+// table and then sets the tag. The last block resets the log and moves to the next epoch.
+__global__ void __launch_bounds__(256) cache_fill_kernel(const __grid_constant__ FwdArgs a, Claims c) {
+  pdl_trigger();
+  pdl_wait();
+  const unsigned n = min(a.cache_ctl[0], (unsigned)a.miss_cap);
+  const int lane = threadIdx.x & 31;
+  const unsigned warps = gridDim.x * (blockDim.x / 32);
+  for (unsigned i = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); i < n; i += warps) {
+    const int64_t e = a.miss_list[i];
+    const int t = (int)(e >> 48);
+    const int64_t id = e & ((int64_t(1) << 48) - 1);
+    const int64_t slot = cache_slot(id, a.cache_shift[t]);
+    if (__ldcg(c.p[t] + slot) != i + 1) continue;  // warp-uniform
+    const float v = a.tables[t][id * kE + lane];
+    const_cast<float*>(a.cache_rows[t])[slot * kE + lane] = v;
+    __syncwarp();
+    if (lane == 0) {
+      const_cast<int64_t*>(a.cache_tags[t])[slot] = id;
+      c.p[t][slot] = 0u;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.cache_ctl + 2, 1u) == gridDim.x - 1) {  // every block has read the log's length
+      a.cache_ctl[0] = 0u;
+      a.cache_ctl[1] += 1u;
+      a.cache_ctl[2] = 0u;
+    }
+  }
 }
 
 // Partial column sums of H over chunks of 64 positions; grid (max_chunks, G, R), 128 threads. The last
@@ -294,7 +427,17 @@ __global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__
 }  // namespace
 
 cudaError_t launch_sparse(const FwdArgs& a, cudaStream_t s) {
-  return launch_kernel(sparse_kernel, dim3(a.num_sms * kSparseBlocksPerSm), dim3(kSparseThreads), 0, s, false, a);
+  return launch_kernel(a.cache_on ? sparse_kernel<true> : sparse_kernel<false>, dim3(a.num_sms * kSparseBlocksPerSm),
+                       dim3(kSparseThreads), 0, s, false, a);
+}
+
+cudaError_t launch_cache_admit(const FwdArgs& a, unsigned* const* claims, cudaStream_t s) {
+  Claims c;
+  for (int t = 0; t < kNTab; ++t) c.p[t] = claims[t];
+  const dim3 grid(a.num_sms * 2), block(256);
+  cudaError_t e = launch_kernel(cache_claim_kernel, grid, block, 0, s, a.pdl != 0, a, c);
+  if (e == cudaSuccess) e = launch_kernel(cache_fill_kernel, grid, block, 0, s, a.pdl != 0, a, c);
+  return e;
 }
 
 cudaError_t launch_seq_colsum(const FwdArgs& a, cudaStream_t s) {

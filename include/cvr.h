@@ -223,6 +223,25 @@ cvr_status cvr_selftest_wait_timeout(cvr_handle* h);
 #define CVR_NOALLOC_MAX_CAND 1024
 cvr_status cvr_predict_noalloc(cvr_handle* h, int32_t n_cand, const void* y, float* out);
 
+/* Hot-row cache in HBM in front of one embedding table (GPU CTR inference article, section 二: the hot
+ * rows live in GPU memory, a lookup tries them first and falls back to host DRAM). Meant for tables kept
+ * in host memory that the GPU reads directly (pinned with cudaHostAlloc / cudaHostRegister; on a
+ * Grace-Blackwell node over NVLink-C2C): pass such a table's address in cvr_weights like any other.
+ *   table  0..7 user fields, 8..15 item fields, 16 the shared sequence table
+ *   slots  a power of two in [1024, 2^28] (rows held; 128 + 16 bytes of HBM each), or 0 to remove it
+ * Direct-mapped: slot = (id * 0x9E3779B97F4A7C15) >> (64 - log2(slots)). During a call the cache is only
+ * read; a row that misses is read from the table and logged (up to 2^20 per call), and after the call a
+ * logged row replaces its slot's row unless that row was read in the same call, so a hot row is never
+ * pushed out by the cold rows of the call that used it. Cached rows are exact fp32 copies: results do not
+ * depend on hits or misses. The tables must not change while a cache holds their rows. The handle's
+ * captured graphs are dropped (the next call of each shape captures again); the call waits for the stream.
+ * Errors: CVR_E_ARG (table or slots out of range), CVR_E_OOM. */
+cvr_status cvr_cache_enable(cvr_handle* h, int32_t table, int64_t slots);
+
+/* Cache lookups since the last read (all tables): rows served from a cache slot and rows read from their
+ * table. Waits for the stream, then resets both counts. Both are 0 while no cache is enabled. */
+cvr_status cvr_cache_stats(cvr_handle* h, int64_t* hits, int64_t* misses);
+
 /* Frees the handle's device memory, graphs and events. NULL is ignored. */
 void cvr_destroy(cvr_handle* h);
 
