@@ -6,7 +6,8 @@ A step is one cvr_score call over one full batch of the workload (all stages of 
 embedding bags, sequence encoders, tokeniser, Query Decoding, Token Mixer, PLE, heads), inputs
 resident in HBM, L2 flushed (256 MB write) before every step and each step timed alone with CUDA
 events on the scorer's stream. ``e2e`` repeats the measurement through cvr_score_host with pinned
-host buffers (input copies and the output read inside the timed region). ``roofline`` is the
+host buffers, which the kernels read (inputs) and write (output) in place over the C2C link inside the
+timed region. ``roofline`` is the
 dominant kernel's algorithmic FLOPs per launch over its event-timed duration. ``cpu_baseline`` times
 the CPU oracle on a bounded sample of the same workload. ``--impl reference`` times that oracle
 alone (the method has no other runnable reference implementation).
@@ -404,7 +405,7 @@ def main():
             "gflop_per_batch": total_flop / 1e9, "mbytes_per_batch": total_bytes / 1e6,
             "bound": "tensor" if total_flop / (peak_tf * 1e12) > total_bytes / (peak_bw * 1e9) else "hbm"}
 
-    # ---- end to end through the host-buffer entry point (pinned buffers, copies inside the timed region)
+    # ---- end to end through the host-buffer entry point (pinned buffers crossing the link inside the timed region)
     e2e = None
     if not args.no_e2e and not args.varlen:  # the host-buffer entry point has fixed lengths
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory().numpy()
@@ -429,7 +430,7 @@ def main():
         e_tot = max_over_ranks(e_tot, dev)
         e2e = {"value": job_throughput(world, B, args.steps, e_tot), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(h_out.nbytes), "p50_ms": statistics.median(e_ms),
-               "api": "cvr_score_host (pinned host buffers)"}
+               "api": "cvr_score_host (pinned host buffers, read and written in place by the kernels)"}
 
     if rank == 0:
         cpu = None

@@ -89,6 +89,7 @@ struct cvr_handle {
   int* err = nullptr;
   unsigned* done = nullptr;
   unsigned* cs_count = nullptr;
+  int32_t* req_copy = nullptr;  // the call's request ids in the workspace
   float* attn_state = nullptr;
   unsigned* attn_count = nullptr;
   int attn_splits = 1;
@@ -270,6 +271,7 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   const size_t oZ = take((size_t)B_cap * kYD * 2), oY = take((size_t)B_cap * kYD * 2);
   const size_t oQ = take((size_t)B_cap * kG * kD * 2), oEx = take((size_t)B_cap * kPleN * 2);
   const size_t oG = take((size_t)B_cap * 8 * 4), oErr = take(1024), oCnt = take((size_t)R_cap * kG * 4);
+  const size_t oReq = take((size_t)B_cap * 4);
   int splits = 1;
   for (int g = 0; g < kG; ++g) splits = std::max(splits, split_count(h->L[g]));
   // attention split state and merge counters, sized for either attention kernel: the register-tile one keeps
@@ -302,6 +304,7 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   h->err = (int*)(b + oErr);
   h->done = (unsigned*)(b + oErr + 256);
   h->cs_count = (unsigned*)(b + oCnt);
+  h->req_copy = (int32_t*)(b + oReq);
   h->attn_splits = splits;
   h->attn_state = splits > 1 ? (float*)(b + oAst) : nullptr;
   h->attn_count = (unsigned*)(b + oAcnt);
@@ -360,7 +363,9 @@ FwdArgs make_args(cvr_handle* h, int R, int B, const int32_t* req_ids, const int
                   int64_t* dbg_rows) {
   FwdArgs a;
   std::memset(&a, 0, sizeof(a));
-  a.req_ids = req_ids;
+  a.req_in = req_ids;
+  a.req_ids = h->req_copy;
+  a.req_copy = h->req_copy;
   a.bag_ids = bag_ids;
   a.bag_offsets = bag_offsets;
   a.seq_ids = seq_ids;
@@ -858,6 +863,23 @@ cvr_status cvr_score_host(cvr_handle* h, int32_t n_req, int32_t n_cand, const in
   const size_t b_off = ((size_t)n_req * kFu + (size_t)n_cand * kFi + 1) * 8;
   const size_t b_seq = (size_t)n_req * h->SL * kCols * 8, b_out = (size_t)n_cand * kNT * 4;
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+  // Arrays in pinned, device-mapped (or managed) host memory are read and written in place by the kernels
+  // -- over NVLink-C2C on a Grace-Blackwell node this beats a staging copy; the others are staged.
+  auto in_place = [](const void* ptr) -> void* {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    if (at.type == cudaMemoryTypeManaged) return const_cast<void*>(ptr);
+    if (at.type == cudaMemoryTypeHost && at.devicePointer) return at.devicePointer;
+    return nullptr;
+  };
+  const int32_t* z_req = (const int32_t*)in_place(req_ids);
+  const int64_t* z_ids = b_ids ? (const int64_t*)in_place(bag_ids) : nullptr;
+  const int64_t* z_off = (const int64_t*)in_place(bag_offsets);
+  const int64_t* z_seq = (const int64_t*)in_place(seq_ids);
+  float* z_out = (float*)in_place(out);
   const size_t need = al(b_req) + al(b_ids) + al(b_off) + al(b_seq) + al(b_out);
   if (need > h->stage_bytes) {
     // growing the staging area invalidates graphs that captured its addresses
@@ -883,16 +905,25 @@ cvr_status cvr_score_host(cvr_handle* h, int32_t n_req, int32_t n_cand, const in
   int64_t* d_seq = (int64_t*)(p + al(b_req) + al(b_ids) + al(b_off));
   float* d_out = (float*)(p + al(b_req) + al(b_ids) + al(b_off) + al(b_seq));
   cudaStream_t s = h->stream;
-  ce = cudaMemcpyAsync(d_req, req_ids, b_req, cudaMemcpyHostToDevice, s);
-  if (ce == cudaSuccess && b_ids) ce = cudaMemcpyAsync(d_ids, bag_ids, b_ids, cudaMemcpyHostToDevice, s);
-  if (ce == cudaSuccess) ce = cudaMemcpyAsync(d_off, bag_offsets, b_off, cudaMemcpyHostToDevice, s);
-  if (ce == cudaSuccess) ce = cudaMemcpyAsync(d_seq, seq_ids, b_seq, cudaMemcpyHostToDevice, s);
+  auto stage_in = [&](const void* src, void* dst, size_t bytes, const void* direct) -> const void* {
+    if (direct) return direct;
+    if (bytes && ce == cudaSuccess) ce = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s);
+    return dst;
+  };
+  const int32_t* q_req = (const int32_t*)stage_in(req_ids, d_req, b_req, z_req);
+  const int64_t* q_ids = (const int64_t*)stage_in(bag_ids, d_ids, b_ids, z_ids);
+  const int64_t* q_off = (const int64_t*)stage_in(bag_offsets, d_off, b_off, z_off);
+  const int64_t* q_seq = (const int64_t*)stage_in(seq_ids, d_seq, b_seq, z_seq);
   if (ce != cudaSuccess) return cuda_fail(h, ce, "host-to-device input copy");
-  cvr_status st = run_forward(h, n_req, n_cand, d_req, d_ids, d_off, d_seq, d_out, nullptr, nullptr);
-  ce = cudaMemcpyAsync(out, d_out, b_out, cudaMemcpyDeviceToHost, s);
-  if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
+  cvr_status st = run_forward(h, n_req, n_cand, q_req, q_ids, q_off, q_seq, z_out ? z_out : d_out, nullptr, nullptr,
+                              /*sync=*/false);
+  if (!z_out) ce = cudaMemcpyAsync(out, d_out, b_out, cudaMemcpyDeviceToHost, s);
   if (ce != cudaSuccess) return cuda_fail(h, ce, "device-to-host output copy");
-  return st;
+  if (st != CVR_OK) {
+    cudaStreamSynchronize(s);
+    return st;
+  }
+  return sync_status(h);
 }
 
 cvr_status cvr_debug_stage(cvr_handle* h, int32_t stage, void* dst, int64_t bytes) {

@@ -58,8 +58,10 @@ constexpr int kErrSeqLens = 64;     // a sequence length outside [0, L[g]]      
 
 // ---- arguments of the forward pass, one copy per call ----
 struct FwdArgs {
-  // caller inputs (device)
-  const int32_t* req_ids;
+  // caller inputs (device, or host memory the device reads in place)
+  const int32_t* req_in;     // the caller's request ids, read once by the sparse kernel
+  const int32_t* req_ids;    // their copy in the workspace, which every later kernel reads
+  int32_t* req_copy;         // (the same copy, written by the sparse kernel)
   const int64_t* bag_ids;
   const int64_t* bag_offsets;
   const int64_t* seq_ids;

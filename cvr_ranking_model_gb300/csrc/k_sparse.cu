@@ -82,13 +82,15 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
   const int64_t nw = (int64_t)gridDim.x * (kSparseThreads / 32);
   pdl_trigger();
   pdl_wait();
-  // request ids: in range and non-decreasing (checked once per candidate)
+  // request ids: in range and non-decreasing (checked once per candidate), and copied to the workspace for
+  // the later kernels (the caller's array may be host memory read over the C2C link)
   for (int64_t cand = (int64_t)blockIdx.x * kSparseThreads + tid; cand < a.B;
        cand += (int64_t)gridDim.x * kSparseThreads) {
-    const int r = a.req_ids[cand];
+    const int r = a.req_in[cand];
     bool bad = r < 0 || r >= a.R;
-    if (cand + 1 < a.B && a.req_ids[cand + 1] < r) bad = true;
+    if (cand + 1 < a.B && a.req_in[cand + 1] < r) bad = true;
     if (bad) atomicOr(a.err, kErrReqIds);
+    a.req_copy[cand] = r;
   }
   int errbits = 0;
   // with a cache, rows are read through L2 only (the admission after the previous call rewrote slots)

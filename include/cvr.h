@@ -159,9 +159,13 @@ cvr_status cvr_score_debug(cvr_handle* h, int32_t n_req, int32_t n_cand, const i
                            const int64_t* bag_ids, const int64_t* bag_offsets, const int64_t* seq_ids, float* out,
                            float* pooled_fp32, int64_t* rows);
 
-/* As cvr_score with HOST inputs and output: the inputs are copied to device staging buffers owned by
- * the handle (one asynchronous copy per array; pinned host memory makes them truly asynchronous) and
- * `out` is copied back before return. n_bag_ids = bag_offsets[last] (the length of bag_ids). */
+/* As cvr_score with HOST inputs and output (iQIYI ad-CVR article 3.4.1: input movement per batch).
+ * An array in pinned, device-mapped host memory (cudaHostAlloc / cudaHostRegister; PyTorch's
+ * pin_memory) or in managed memory is read -- `out` written -- in place by the kernels: on a
+ * Grace-Blackwell node over NVLink-C2C, with no staging copy. Any other host array is copied to a
+ * device staging buffer owned by the handle (one asynchronous copy per array), and `out` back. The call
+ * waits for the stream once and returns the call's status. n_bag_ids = bag_offsets[last] (the length
+ * of bag_ids). The caller must not modify the arrays until the call returns. */
 cvr_status cvr_score_host(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids, const int64_t* bag_ids,
                           int64_t n_bag_ids, const int64_t* bag_offsets, const int64_t* seq_ids, float* out);
 

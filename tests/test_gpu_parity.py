@@ -119,14 +119,21 @@ def test_eager_and_graph_agree_and_repeat():
 
 
 def test_host_entry_point_matches_device_entry_point():
+    # pageable arrays are staged by copies; pinned ones are read (and out written) in place over the C2C
+    # link; every mix gives the device entry point's bits
+    import torch
     wl = synth.make_workload("tiny", n_req=2, n_cand=33)
     w = synth.make_weights(wl.n_layers, wl.seed)
     g = GpuRun(wl, w)
     g.run()
     dev = g.out()
-    out = np.zeros((wl.n_cand, 2), np.float32)
-    g.sc.score_host(wl.n_req, wl.n_cand, wl.req_ids, wl.bag_ids, wl.bag_offsets, np.ascontiguousarray(wl.seq_ids), out)
-    assert np.array_equal(out.astype(np.float64), dev)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory().numpy()
+    arrays = [wl.req_ids, wl.bag_ids, wl.bag_offsets, np.ascontiguousarray(wl.seq_ids)]
+    for mask in (0b00000, 0b11111, 0b01010, 0b10101):
+        ins = [pin(a) if mask >> i & 1 else np.ascontiguousarray(a) for i, a in enumerate(arrays)]
+        out = pin(np.zeros((wl.n_cand, 2), np.float32)) if mask >> 4 & 1 else np.zeros((wl.n_cand, 2), np.float32)
+        g.sc.score_host(wl.n_req, wl.n_cand, *ins, out)
+        assert np.array_equal(out.astype(np.float64), dev), f"pinned mask {mask:05b}"
 
 
 # ------------------------------------------------------------------ error reporting (no fault)
