@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
 
 // ------------------------------------------------------------------------------------------
 // prediction heads: grid (ceil(B/128), tasks)
-constexpr int kHeadSmem = 1024 + 4 * kATile + 4 * kATile + 256;
+constexpr int kHeadSmem = 1024 + 4 * kATile + 4 * kATile + 256 + 2 * kHH * 4;
 
 __global__ void __launch_bounds__(kThreads, 1) heads_kernel(const __grid_constant__ FwdArgs a,
                                                             const __grid_constant__ CUtensorMap tmW1) {
@@ -309,8 +309,14 @@ __global__ void __launch_bounds__(kThreads, 1) heads_kernel(const __grid_constan
   uint64_t* barD = barW + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(barD + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  float* sB1 = reinterpret_cast<float*>(sW + 4 * kATile + 256);  // b1_t, then w2_t: constants, loaded up front
+  float* sW2 = sB1 + kHH;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * kBM, t = blockIdx.y;
+  if (threadIdx.x < kHH) {  // (weights: no dependency on the previous kernel)
+    sB1[threadIdx.x] = __ldg(a.head_b1 + t * kHH + threadIdx.x);
+    sW2[threadIdx.x] = __ldg(a.head_w2 + t * kHH + threadIdx.x);
+  }
   if (threadIdx.x == 0) {
     mbar_init(barA, kBuildWarps * 32);
     mbar_init(barW, 1);
@@ -389,13 +395,13 @@ __global__ void __launch_bounds__(kThreads, 1) heads_kernel(const __grid_constan
       tc_fence_after();
       float logit = 0.f;
 #pragma unroll 1
-      for (int c = 0; c < kHH / 32; ++c) {
-        float v[32], b1[32], w2[32];
-        ldg32(a.head_b1 + t * kHH + c * 32, b1);
-        ldg32(a.head_w2 + t * kHH + c * 32, w2);
-        tmem_ld32(tbase + ((uint32_t)(q * 32) << 16) + c * 32, v);
+      for (int c = 0; c < kHH / 32; c += 2) {  // two TMEM loads in flight, b1 and w2 from shared memory
+        uint32_t v[64];
+        tmem_ld32_nowait(tbase + ((uint32_t)(q * 32) << 16) + c * 32, v);
+        tmem_ld32_nowait(tbase + ((uint32_t)(q * 32) << 16) + c * 32 + 32, v + 32);
+        tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) logit += fmaxf(v[j] + b1[j], 0.f) * w2[j];
+        for (int j = 0; j < 64; ++j) logit += fmaxf(__uint_as_float(v[j]) + sB1[c * 32 + j], 0.f) * sW2[c * 32 + j];
       }
       if (live) a.out[(int64_t)row * kNT + t] = 1.f / (1.f + expf(-(logit + a.head_b2[t])));
     }
