@@ -349,16 +349,15 @@ __global__ void __launch_bounds__(256) cache_fill_kernel(const __grid_constant__
 __global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__ FwdArgs a) {
   const int chunk = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
   const int L = a.L[g];
-  const int t = threadIdx.x, cp = t & 63, half = t >> 6;
-  // constants of the query term, loaded before waiting for the encoder (only the last block uses them):
-  // row t of the first layer's mean-pool weights and its bias
-  uint4 w0[16];
-  {
-    const uint4* wrow = reinterpret_cast<const uint4*>(a.qm + ((int64_t)g * kD + t) * kD);
-#pragma unroll
-    for (int v = 0; v < 16; ++v) w0[v] = __ldg(wrow + v);
-  }
-  const float qb0 = __ldg(a.q_b + g * kD + t);
+  const int t = threadIdx.x;
+  // the mean-pool weight rows of this group (every layer) go to L2 while the encoder still runs; only the
+  // last block of a (request, group) reads them
+  if (chunk == 0 && r == 0)
+    for (int l = 0; l < a.n_layers; ++l) {
+      const uint8_t* wrow = reinterpret_cast<const uint8_t*>(a.qm + (((int64_t)l * kG + g) * kD + t) * kD);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(wrow));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(wrow + 128));
+    }
   pdl_trigger();
   pdl_wait();
   // positions that count: the request's real events (all L without variable lengths); an empty group still
@@ -368,21 +367,36 @@ __global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__
   if (chunk >= chunks) return;
   const __nv_bfloat16* base = a.H + (a.goff[g] + (int64_t)r * L) * kD;
   const int l_end = min(len, chunk * 64 + 64);
-  float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
-  for (int l = chunk * 64 + half; l < l_end; l += 2) {
-    const __nv_bfloat162 v = __ldg(reinterpret_cast<const __nv_bfloat162*>(base + (int64_t)l * kD) + cp);
-    s0 += __low2float(v);
-    s1 += __high2float(v);
+  // thread t sums columns [8 (t % 16), +8) over rows chunk*64 + t/16 + 8i, i = 0..7: eight 16-byte loads in
+  // flight, then the eight row groups are added in a fixed order (the result does not depend on timing)
+  const int cg = t & 15, rg = t >> 4;
+  uint4 v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int l = chunk * 64 + rg + 8 * i;
+    v[i] = l < l_end ? __ldg(reinterpret_cast<const uint4*>(base + (int64_t)l * kD) + cg) : make_uint4(0, 0, 0, 0);
   }
-  __shared__ float part[2][128];
-  __shared__ float m[128];
+  float sacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      sacc[2 * e] += __low2float(h[e]);
+      sacc[2 * e + 1] += __high2float(h[e]);
+    }
+  }
+  __shared__ float part[8][kD];
+  __shared__ float m[kD];
   __shared__ int last;
-  part[half][2 * cp] = s0;
-  part[half][2 * cp + 1] = s1;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) part[rg][cg * 8 + e] = sacc[e];
   __syncthreads();
-  float* rg = a.colsum + ((int64_t)r * kG + g) * a.max_chunks * kD;
-  rg[chunk * kD + t] = part[0][t] + part[1][t];
+  float colsum = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) colsum += part[j][t];
+  float* rgp = a.colsum + ((int64_t)r * kG + g) * a.max_chunks * kD;
+  rgp[chunk * kD + t] = colsum;
   __threadfence();
   __syncthreads();
   unsigned* cnt = a.cs_count + r * kG + g;
@@ -390,39 +404,34 @@ __global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__
   __syncthreads();
   if (!last) return;
   float sum = 0.f;
-  for (int c0 = 0; c0 < chunks; c0 += 4) {  // four loads in flight, summed in chunk order
-    float v[4];
+  for (int c0 = 0; c0 < chunks; c0 += 8) {  // eight loads in flight, summed in chunk order
+    float cv[8];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) v[c] = c0 + c < chunks ? __ldcg(rg + (c0 + c) * kD + t) : 0.f;
+    for (int c = 0; c < 8; ++c) cv[c] = c0 + c < chunks ? __ldcg(rgp + (c0 + c) * kD + t) : 0.f;
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (c0 + c < chunks) sum += v[c];
+    for (int c = 0; c < 8; ++c)
+      if (c0 + c < chunks) sum += cv[c];
   }
   m[t] = len > 0 ? sum / (float)len : 0.f;
   if (t == 0) *cnt = 0u;
   __syncthreads();
   for (int l = 0; l < a.n_layers; ++l) {
     uint4 wv[16];
-    if (l == 0) {
+    const uint4* wrow = reinterpret_cast<const uint4*>(a.qm + (((int64_t)l * kG + g) * kD + t) * kD);
 #pragma unroll
-      for (int v = 0; v < 16; ++v) wv[v] = w0[v];
-    } else {
-      const uint4* wrow = reinterpret_cast<const uint4*>(a.qm + (((int64_t)l * kG + g) * kD + t) * kD);
-#pragma unroll
-      for (int v = 0; v < 16; ++v) wv[v] = __ldg(wrow + v);
-    }
+    for (int x = 0; x < 16; ++x) wv[x] = __ldg(wrow + x);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int v = 0; v < 16; ++v) {
-      const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&wv[v]);
+    for (int x = 0; x < 16; ++x) {
+      const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&wv[x]);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        acc[q] += __low2float(e[q]) * m[v * 8 + 2 * q];
-        acc[q] += __high2float(e[q]) * m[v * 8 + 2 * q + 1];
+        acc[q] += __low2float(e[q]) * m[x * 8 + 2 * q];
+        acc[q] += __high2float(e[q]) * m[x * 8 + 2 * q + 1];
       }
     }
     a.qb[((int64_t)l * a.R + r) * (kG * kD) + g * kD + t] =
-        (l == 0 ? qb0 : a.q_b[l * kG * kD + g * kD + t]) + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+        __ldg(a.q_b + l * kG * kD + g * kD + t) + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
   }
 }
 
