@@ -221,58 +221,83 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
   }
 
   // ---------------------------------------------------------------- sequence events
-  // one warp per event: 4 id columns -> 4 rows of the shared table -> one 128-wide row; the ids of the next
-  // event load while this event's rows are in flight
+  // a warp takes four events per iteration (events ev + u * nw): per event 4 id columns -> 4 rows of the shared
+  // table -> one 128-wide row, 8 lanes per row; each lane has its four events' rows in flight at once, and the
+  // next iteration's ids load meanwhile
   {
+    constexpr int kEvU = 4;
     const int64_t n_events = (int64_t)a.R * a.SL;
     const int c = lane >> 3, part = lane & 7;
+    const int64_t stride = nw * kEvU;
     int64_t ev = gw;
-    int64_t id_next = ev < n_events ? a.seq_ids[ev * kCols + c] : 0;
+    int64_t id_next[kEvU];
+#pragma unroll
+    for (int u = 0; u < kEvU; ++u) {
+      const int64_t e = ev + u * nw;
+      id_next[u] = e < n_events ? a.seq_ids[e * kCols + c] : 0;
+    }
     while (ev < n_events) {  // warp-uniform
-      const int64_t ev1 = ev + nw;
-      int64_t id = id_next;
-      id_next = ev1 < n_events ? a.seq_ids[ev1 * kCols + c] : 0;
-      const int64_t r = ev / a.SL;
-      int l = (int)(ev - r * a.SL);
-      int g = 0;
-      while (g < kG - 1 && l >= a.L[g]) {
-        l -= a.L[g];
-        ++g;
+      int64_t id[kEvU];
+#pragma unroll
+      for (int u = 0; u < kEvU; ++u) {
+        id[u] = id_next[u];
+        const int64_t e1 = ev + stride + u * nw;
+        id_next[u] = e1 < n_events ? a.seq_ids[e1 * kCols + c] : 0;
       }
-      const int64_t row = a.goff[g] + r * a.L[g] + l;
-      __nv_bfloat16* out = a.Xs + row * kD + c * kE + part * 4;
-      bool pad = false;
-      if (a.seq_lens) {
-        const int raw = a.seq_lens[r * kG + g];
-        if (l == 0 && lane == 0 && (raw < 0 || raw > a.L[g])) errbits |= kErrSeqLens;
-        pad = l >= seq_len_of(a, r, g);  // padding: its id is never looked up; encoded from zeros, never used
-      }
-      bool hit = false, miss = false;
-      const float* src = nullptr;
-      if (!pad) {
-        if (id < 0 || id >= a.table_rows[kFu + kFi]) {
-          errbits |= kErrIdRange;
-          id = 0;
+      __nv_bfloat16* out[kEvU];
+      const float* src[kEvU];
+#pragma unroll
+      for (int u = 0; u < kEvU; ++u) {
+        const int64_t e = ev + u * nw;
+        out[u] = nullptr;
+        src[u] = nullptr;  // null: padding (stored as zeros) or past the last event
+        bool hit = false, miss = false;
+        if (e < n_events) {  // warp-uniform
+          const int64_t r = e / a.SL;
+          int l = (int)(e - r * a.SL);
+          int g = 0;
+          while (g < kG - 1 && l >= a.L[g]) {
+            l -= a.L[g];
+            ++g;
+          }
+          const int64_t row = a.goff[g] + r * a.L[g] + l;
+          out[u] = a.Xs + row * kD + c * kE + part * 4;
+          bool pad = false;
+          if (a.seq_lens) {
+            const int raw = a.seq_lens[r * kG + g];
+            if (l == 0 && lane == 0 && (raw < 0 || raw > a.L[g])) errbits |= kErrSeqLens;
+            pad = l >= seq_len_of(a, r, g);  // padding: its id is never looked up; encoded from zeros, never used
+          }
+          if (!pad) {
+            int64_t iv = id[u];
+            if (iv < 0 || iv >= a.table_rows[kFu + kFi]) {
+              errbits |= kErrIdRange;
+              iv = 0;
+            }
+            id[u] = iv;
+            src[u] = kCache ? row_src(a, kFu + kFi, iv, epoch, part == 0, hit, miss) : a.tables[kFu + kFi] + iv * kE;
+          }
         }
-        src = kCache ? row_src(a, kFu + kFi, id, epoch, part == 0, hit, miss) : a.tables[kFu + kFi] + id * kE;
+        if (cached) {  // one lane of each id's 8 counts and logs
+          miss = miss && part == 0;
+          n_hit += hit && part == 0;
+          n_miss += miss;
+          log_misses(a, miss, kFu + kFi, id[u], lane);
+        }
       }
-      if (cached) {  // one lane of each id's 8 counts and logs
-        miss = miss && part == 0;
-        n_hit += hit && part == 0;
-        n_miss += miss;
-        log_misses(a, miss, kFu + kFi, id, lane);
+      float4 v[kEvU];
+#pragma unroll
+      for (int u = 0; u < kEvU; ++u) v[u] = src[u] ? ld_row(src[u], part, cached) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < kEvU; ++u) {
+        if (!out[u]) continue;
+        v[u].x = clampf(v[u].x, a.clamp);
+        v[u].y = clampf(v[u].y, a.clamp);
+        v[u].z = clampf(v[u].z, a.clamp);
+        v[u].w = clampf(v[u].w, a.clamp);
+        store_bf16x4(out[u], v[u]);
       }
-      if (pad) {
-        store_bf16x4(out, make_float4(0.f, 0.f, 0.f, 0.f));
-      } else {
-        float4 v = ld_row(src, part, cached);
-        v.x = clampf(v.x, a.clamp);
-        v.y = clampf(v.y, a.clamp);
-        v.z = clampf(v.z, a.clamp);
-        v.w = clampf(v.w, a.clamp);
-        store_bf16x4(out, v);
-      }
-      ev = ev1;
+      ev += stride;
     }
   }
   if (errbits) atomicOr(a.err, errbits);
