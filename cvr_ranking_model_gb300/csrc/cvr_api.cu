@@ -75,6 +75,7 @@ struct cvr_handle {
   std::string last_error;
   // packed weights
   void* wblob = nullptr;
+  size_t wblob_bytes = 0;
   bf16 *tokI = nullptr, *tokU = nullptr, *seqW13 = nullptr, *seqW2 = nullptr, *qX = nullptr, *qm = nullptr;
   bf16 *tmW13 = nullptr, *tmW2 = nullptr, *pleW = nullptr, *headW1 = nullptr;
   float *tok_b = nullptr, *seq_b13 = nullptr, *seq_b2 = nullptr, *q_b = nullptr, *tm_b13 = nullptr, *tm_b2 = nullptr;
@@ -423,6 +424,8 @@ FwdArgs make_args(cvr_handle* h, int R, int B, const int32_t* req_ids, const int
   a.err = h->err;
   a.done = h->done;
   a.err_host = h->err_host_dev;
+  a.wblob = static_cast<const uint8_t*>(h->wblob);
+  a.wblob_bytes = (int64_t)h->wblob_bytes;
   a.tokU = h->tokU;
   a.tok_b = h->tok_b;
   a.seq_b13 = h->seq_b13;
@@ -764,6 +767,7 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
     cudaGetLastError();
     return CVR_E_OOM;
   }
+  h->wblob_bytes = bf_bytes + f_bytes;
   uint8_t* wb = static_cast<uint8_t*>(h->wblob);
   e = cudaMemcpy(wb, P.bf.data(), bf_bytes, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(wb + bf_bytes, P.f32.data(), f_bytes, cudaMemcpyHostToDevice);

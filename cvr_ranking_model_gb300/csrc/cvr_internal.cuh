@@ -115,7 +115,9 @@ struct FwdArgs {
   int miss_cap;
   unsigned* cache_ctl;               // [0] misses logged this call, [1] epoch of this call, [2] admit counter
   unsigned long long* cache_stat;    // [0] hits, [1] misses, accumulated until read
-  // packed weights (device)
+  // packed weights (device): one allocation, which the first kernel of a call prefetches into L2
+  const uint8_t* wblob;
+  int64_t wblob_bytes;
   const __nv_bfloat16* tokU;   // [1664][256]
   const float* tok_b;          // [1664]
   const float* seq_b13;        // [3][512] (interleaved like the weights)

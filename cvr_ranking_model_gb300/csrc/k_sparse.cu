@@ -80,6 +80,16 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
   const int tid = threadIdx.x, lane = tid & 31;
   const int64_t gw = (int64_t)blockIdx.x * (kSparseThreads / 32) + (tid >> 5);
   const int64_t nw = (int64_t)gridDim.x * (kSparseThreads / 32);
+  // The later kernels' weights (one packed allocation, a few MB) go to L2 while this kernel -- bound by the
+  // latency of its dependent loads, not by bandwidth -- does its lookups: each block prefetches one slice
+  // (256-byte aligned starts, sizes a multiple of 16 bytes, all inside the allocation).
+  if (tid == 0 && a.wblob) {
+    const int64_t slice = ((a.wblob_bytes + gridDim.x - 1) / gridDim.x + 255) / 256 * 256;
+    const int64_t b0 = (int64_t)blockIdx.x * slice;
+    const int64_t n = min(slice, a.wblob_bytes - b0) / 16 * 16;
+    if (n > 0)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.wblob + b0), "r"((unsigned)n) : "memory");
+  }
   pdl_trigger();
   pdl_wait();
   // request ids: in range and non-decreasing (checked once per candidate), and copied to the workspace for
