@@ -69,6 +69,10 @@ struct cvr_handle {
   int num_sms = 1;
   cudaStream_t stream = nullptr;
   cudaStream_t cap_stream = nullptr;
+  // the tokeniser's token columns run on a second stream, next to the sequence encoder (fork after the
+  // sparse kernel, join before the query columns)
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   cvr_config cfg{};
   int n_layers = 1, SL = 0;
   int L[kG] = {0, 0, 0};
@@ -105,6 +109,7 @@ struct cvr_handle {
   // graphs, profiling
   bool use_graph = true, profile = false, pdl = true;
   bool attn_tc = false;  // cross-attention on the tcgen05 kernel instead of the register-tile one
+  bool last_q_add = false;  // the last call left the first layer's queries without their mean-pooled term
   // hot-row caches in HBM, per table (slots == 0: none)
   int64_t c_slots[kNTab] = {};
   float* c_rows[kNTab] = {};
@@ -443,6 +448,27 @@ FwdArgs make_args(cvr_handle* h, int R, int B, const int32_t* req_ids, const int
 }
 
 // Enqueues the whole forward pass on `s`. With `events`, records one after each kernel.
+// Whether a call of R requests runs the tokeniser on the side stream, next to the sequence encoder: only when
+// the encoder leaves at least half the SMs free, without per-kernel events and with the register-tile attention
+// (which adds the first layer's mean-pooled query term the tokeniser then leaves out).
+bool fork_tokenizer(const cvr_handle* h, int R, bool events) {
+  int seq_tiles = 0;
+  for (int g = 0; g < kG; ++g) seq_tiles += (int)(((int64_t)R * h->L[g] + 127) / 128);
+  return !events && h->side && !h->attn_tc && std::min(seq_tiles, h->num_sms) <= h->num_sms / 2;
+}
+
+// CVR_STAGE_Q after such a call with one layer: the stored queries plus their mean-pooled term, rounded like
+// the attention kernel rounds them
+__global__ void q_with_mean_kernel(__nv_bfloat16* dst, const __nv_bfloat16* q, const float* qb, const int32_t* req,
+                                   int64_t n, int R) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t b = i / (kG * kD);
+    const int c = (int)(i - b * (kG * kD));
+    const int r = min(max(req[b], 0), R - 1);
+    dst[i] = __float2bfloat16_rn(__bfloat162float(q[i]) + qb[(int64_t)r * (kG * kD) + c]);
+  }
+}
+
 cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, bool events, bool external_events,
                             int* launches) {
   int n = 0, ev = 0;
@@ -467,9 +493,30 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
   run(launch_sparse(a, s), kStageNames[0]);
   int seq_tiles = 0;
   for (int g = 0; g < kG; ++g) seq_tiles += (int)(((int64_t)a.R * a.L[g] + 127) / 128);
-  run(launch_seq_mlp(a, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, s), kStageNames[1]);
-  run(launch_seq_colsum(a, s), kStageNames[2]);
-  run(launch_tokenizer(a, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, s), kStageNames[3]);
+  const int seq_grid = std::min(seq_tiles, a.num_sms);
+  // Two branches after the sparse kernel when the sequence encoder leaves at least half the SMs free. Side
+  // stream: the user half of the tokeniser, then the tokeniser itself (it needs the pooled embeddings only),
+  // on the SMs the encoder does not use. This stream: the sequence encoder and its column sums. The first
+  // layer's queries then lack their mean-pooled sequence term, which the attention kernel adds (the tcgen05
+  // attention reads Q by TMA and keeps the one-stream order).
+  const bool fork = fork_tokenizer(h, a.R, events);
+  FwdArgs af = a;
+  af.q_add = fork ? 1 : 0;
+  if (fork) {
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
+    run(launch_xu(af, false, h->side), "user_gemv");
+    run(launch_tokenizer(af, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, kTokAll, a.num_sms - seq_grid, h->side),
+        kStageNames[3]);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_join, h->side);
+    run(launch_seq_mlp(af, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, false, s), kStageNames[1]);
+    run(launch_seq_colsum(af, s), kStageNames[2]);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_join, 0);
+  } else {
+    run(launch_seq_mlp(a, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, true, s), kStageNames[1]);
+    run(launch_seq_colsum(a, s), kStageNames[2]);
+    run(launch_tokenizer(a, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, kTokAll, 0, s), kStageNames[3]);
+  }
   bf16* zin = h->Z;
   bf16* zout = h->Y;
   for (int l = 0; l < a.n_layers; ++l) {
@@ -477,7 +524,9 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
     const bool in_is_Z = zin == h->Z;
     // the first layer's queries come out of the tokeniser
     if (l > 0) run(launch_query(a, l, in_is_Z ? h->tm_x_Z : h->tm_x_Y, h->tm_qW[l], s), kStageNames[4]);
-    run(h->attn_tc ? launch_attention_tc(a, h->tm_Q, h->tm_H, zin, s) : launch_attention(a, zin, s), kStageNames[5]);
+    FwdArgs al = a;  // the first layer's queries may still lack their mean-pooled term (stacked layers' have it)
+    al.q_add = l == 0 ? af.q_add : 0;
+    run(h->attn_tc ? launch_attention_tc(al, h->tm_Q, h->tm_H, zin, s) : launch_attention(al, zin, s), kStageNames[5]);
     run(launch_tm_mlp(a, l, zin, zout, in_is_Z ? h->tm_5_Z : h->tm_5_Y, h->tm_tmW13, h->tm_tmW2, s), kStageNames[6]);
   }
   run(launch_ple(a, zout == h->Z ? h->tm_full_Z : h->tm_full_Y, h->tm_pleW, h->tm_Ex, s), kStageNames[7]);
@@ -563,6 +612,7 @@ cvr_status run_forward(cvr_handle* h, int32_t R, int32_t B, const int32_t* req_i
   }
   h->last_R = R;
   h->last_B = B;
+  h->last_q_add = fork_tokenizer(h, R, h->profile) && h->n_layers == 1;
   if (!sync) return CVR_OK;
   return sync_status(h);
 }
@@ -777,6 +827,9 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
     e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->err_host_dev), h->err_host, 0);
   }
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     cvr_destroy(h);
     cudaGetLastError();
@@ -946,7 +999,14 @@ cvr_status cvr_debug_stage(cvr_handle* h, int32_t stage, void* dst, int64_t byte
     default: return fail(h, CVR_E_ARG, "unknown stage");
   }
   if (bytes != need) return fail(h, CVR_E_SHAPE, "stage size mismatch: expected " + std::to_string(need) + " bytes");
-  cudaError_t ce = cudaMemcpyAsync(dst, src, (size_t)need, cudaMemcpyDeviceToDevice, h->stream);
+  cudaError_t ce = cudaSuccess;
+  if (stage == CVR_STAGE_Q && h->last_q_add) {
+    q_with_mean_kernel<<<h->num_sms * 4, 256, 0, h->stream>>>(static_cast<__nv_bfloat16*>(dst), h->Q, h->qb,
+                                                               h->req_copy, B * kG * kD, (int)R);
+    ce = cudaGetLastError();
+  } else {
+    ce = cudaMemcpyAsync(dst, src, (size_t)need, cudaMemcpyDeviceToDevice, h->stream);
+  }
   if (ce == cudaSuccess) ce = cudaStreamSynchronize(h->stream);
   if (ce != cudaSuccess) return cuda_fail(h, ce, "stage copy");
   return CVR_OK;
@@ -1068,6 +1128,9 @@ void cvr_destroy(cvr_handle* h) {
   if (h->err_host) cudaFreeHost(h->err_host);
   for (auto ev : h->events) cudaEventDestroy(ev);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  if (h->side) cudaStreamDestroy(h->side);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
   delete h;
 }
 

@@ -94,6 +94,8 @@ struct FwdArgs {
   float* attn_state;
   unsigned* attn_count;
   int attn_splits;         // splits of the longest group (grid z of the attention kernel)
+  int q_add;               // 1: Q holds the first layer's queries without their mean-pooled sequence term, which
+                           // the attention kernel adds (the tokeniser ran before the sequence side finished)
   int max_chunks;
   float* xu;              // [R][1664] user half of the tokeniser (+ bias)
   float* qb;              // [layers][R][384] per-request query term (+ bias)
@@ -422,11 +424,16 @@ cudaError_t prepare_attention_tc_kernel();
 cudaError_t launch_sparse(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_seq_colsum(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_seq_mlp(const FwdArgs& a, const CUtensorMap& tmXs, const CUtensorMap& tmW13,
-                           const CUtensorMap& tmW2, int n_tiles, cudaStream_t s);
+                           const CUtensorMap& tmW2, int n_tiles, bool with_xu, cudaStream_t s);
+// the user half of the tokeniser alone (otherwise extra CTAs of the sequence-encoder launch)
+cudaError_t launch_xu(const FwdArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_tm_mlp(const FwdArgs& a, int layer, const __nv_bfloat16* zin, __nv_bfloat16* yout,
                           const CUtensorMap& tmZ, const CUtensorMap& tmW13, const CUtensorMap& tmW2, cudaStream_t s);
+// the tokeniser GEMM over all 2048 packed columns, over the 13 token slots only (no dependency on the sequence
+// side), or over the first layer's 384 query columns only (which add the mean-pooled sequence term)
+enum { kTokAll = 0, kTokTokens = 1, kTokQueries = 2 };
 cudaError_t launch_tokenizer(const FwdArgs& a, const CUtensorMap& tmI, const CUtensorMap& tmW, const CUtensorMap& tmZo,
-                             const CUtensorMap& tmQo, cudaStream_t s);
+                             const CUtensorMap& tmQo, int part, int max_grid, cudaStream_t s);
 cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, const CUtensorMap& tmW, cudaStream_t s);
 cudaError_t launch_attention(const FwdArgs& a, __nv_bfloat16* zin, cudaStream_t s);
 cudaError_t launch_attention_tc(const FwdArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmH, __nv_bfloat16* zin,

@@ -91,6 +91,26 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
     qf[ks][2] = __ldg(qa + 4);
     qf[ks][3] = __ldg(qb + 4);
   }
+  if (a.q_add) {
+    // the first layer's queries still lack the mean-pooled sequence term of their request (the tokeniser ran
+    // next to the sequence encoder): q = q + qb[r], rounded to bf16 again
+    const int rA = min(max(a.req_ids[qrA], 0), R - 1), rB = min(max(a.req_ids[qrB], 0), R - 1);
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      const int col = g * kD + h * kHD + ks * 16 + 2 * tig;
+      const float2* pa = reinterpret_cast<const float2*>(a.qb + (int64_t)rA * (kG * kD) + col);
+      const float2* pb = reinterpret_cast<const float2*>(a.qb + (int64_t)rB * (kG * kD) + col);
+      const float2 ta0 = __ldg(pa), tb0 = __ldg(pb), ta1 = __ldg(pa + 4), tb1 = __ldg(pb + 4);
+      auto add2 = [](uint32_t q, float2 t) {
+        const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&q);
+        return pack_bf16(__low2float(v) + t.x, __high2float(v) + t.y);
+      };
+      qf[ks][0] = add2(qf[ks][0], ta0);
+      qf[ks][1] = add2(qf[ks][1], tb0);
+      qf[ks][2] = add2(qf[ks][2], ta1);
+      qf[ks][3] = add2(qf[ks][3], tb1);
+    }
+  }
   // logits * log2(e) / (tau * sqrt(head_dim)) so that the softmax runs on exp2
   const float sl2 = 1.4426950408889634f / (a.tau * sqrtf((float)kHD));
 

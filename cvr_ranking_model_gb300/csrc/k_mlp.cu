@@ -477,6 +477,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The user half of the tokeniser as a kernel of its own (when it runs on the side stream next to the encoder)
+__global__ void __launch_bounds__(kXuThreads) xu_kernel(const __grid_constant__ FwdArgs a) {
+  extern __shared__ uint8_t xu_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(xu_smem_raw) + 15) & ~uintptr_t(15));
+  pdl_trigger();
+  xu_block(a, (int)blockIdx.x, smem);
+}
+
 }  // namespace
 
 cudaError_t prepare_mlp_kernels() {
@@ -487,11 +495,16 @@ cudaError_t prepare_mlp_kernels() {
 }
 
 cudaError_t launch_seq_mlp(const FwdArgs& a, const CUtensorMap& tmXs, const CUtensorMap& tmW13, const CUtensorMap& tmW2,
-                           int n_tiles, cudaStream_t s) {
+                           int n_tiles, bool with_xu, cudaStream_t s) {
   const int grid = n_tiles < a.num_sms ? n_tiles : a.num_sms;
   static_assert(kXuSmemBytes <= kSmemBytes && kXuThreads <= kThreads, "the user-side GEMV fits the CTA");
-  return launch_kernel(swiglu_mlp_kernel<MODE_SEQ>, dim3(grid + kXuBlocks), dim3(kThreads), kSmemBytes, s, a.pdl != 0,
-                       a, tmXs, tmW13, tmW2, 0, n_tiles, grid, (const __nv_bfloat16*)nullptr, (__nv_bfloat16*)nullptr);
+  return launch_kernel(swiglu_mlp_kernel<MODE_SEQ>, dim3(grid + (with_xu ? kXuBlocks : 0)), dim3(kThreads), kSmemBytes,
+                       s, a.pdl != 0, a, tmXs, tmW13, tmW2, 0, n_tiles, grid, (const __nv_bfloat16*)nullptr,
+                       (__nv_bfloat16*)nullptr);
+}
+
+cudaError_t launch_xu(const FwdArgs& a, bool pdl, cudaStream_t s) {
+  return launch_kernel(xu_kernel, dim3(kXuBlocks), dim3(kXuThreads), kXuSmemBytes + 16, s, pdl, a);
 }
 
 cudaError_t launch_tm_mlp(const FwdArgs& a, int layer, const __nv_bfloat16* zin, __nv_bfloat16* yout,
