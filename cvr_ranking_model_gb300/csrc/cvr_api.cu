@@ -1064,6 +1064,7 @@ cvr_status cvr_cache_enable(cvr_handle* h, int32_t table, int64_t slots) {
     return fail(h, CVR_E_ARG, "cache slots must be 0 or a power of two in [1024, 2^28]");
   cudaError_t ce = cudaSetDevice(h->device);
   if (ce == cudaSuccess) ce = cudaStreamSynchronize(h->stream);  // no call in flight still reads the old cache
+  if (ce == cudaSuccess && h->side) ce = cudaStreamSynchronize(h->side);
   if (ce != cudaSuccess) return cuda_fail(h, ce, "cache setup");
   free_cache(h, table);
   drop_graphs(h);  // captured calls hold the old cache's pointers
@@ -1119,6 +1120,7 @@ void cvr_destroy(cvr_handle* h) {
   if (!h) return;
   cudaSetDevice(h->device);
   if (h->stream) cudaStreamSynchronize(h->stream);
+  if (h->side) cudaStreamSynchronize(h->side);  // (joins the handle's stream, unless a launch failed in between)
   free_workspace(h);
   for (int t = 0; t < kNTab; ++t) free_cache(h, t);
   if (h->miss_list) cudaFree(h->miss_list);
