@@ -506,7 +506,7 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
     if (e == cudaSuccess) e = cudaEventRecord(h->ev_fork, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
     run(launch_xu(af, false, h->side), "user_gemv");
-    run(launch_tokenizer(af, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, kTokAll, a.num_sms - seq_grid, h->side),
+    run(launch_tokenizer(af, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, a.num_sms - seq_grid, h->side),
         kStageNames[3]);
     if (e == cudaSuccess) e = cudaEventRecord(h->ev_join, h->side);
     run(launch_seq_mlp(af, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, false, s), kStageNames[1]);
@@ -515,7 +515,7 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
   } else {
     run(launch_seq_mlp(a, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, true, s), kStageNames[1]);
     run(launch_seq_colsum(a, s), kStageNames[2]);
-    run(launch_tokenizer(a, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, kTokAll, 0, s), kStageNames[3]);
+    run(launch_tokenizer(a, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, 0, s), kStageNames[3]);
   }
   bf16* zin = h->Z;
   bf16* zout = h->Y;

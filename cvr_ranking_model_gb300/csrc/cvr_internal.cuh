@@ -429,11 +429,10 @@ cudaError_t launch_seq_mlp(const FwdArgs& a, const CUtensorMap& tmXs, const CUte
 cudaError_t launch_xu(const FwdArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_tm_mlp(const FwdArgs& a, int layer, const __nv_bfloat16* zin, __nv_bfloat16* yout,
                           const CUtensorMap& tmZ, const CUtensorMap& tmW13, const CUtensorMap& tmW2, cudaStream_t s);
-// the tokeniser GEMM over all 2048 packed columns, over the 13 token slots only (no dependency on the sequence
-// side), or over the first layer's 384 query columns only (which add the mean-pooled sequence term)
-enum { kTokAll = 0, kTokTokens = 1, kTokQueries = 2 };
+// the tokeniser GEMM (13 tokens + the first layer's queries, 2048 packed columns) on at most max_grid CTAs
+// (0: one per SM)
 cudaError_t launch_tokenizer(const FwdArgs& a, const CUtensorMap& tmI, const CUtensorMap& tmW, const CUtensorMap& tmZo,
-                             const CUtensorMap& tmQo, int part, int max_grid, cudaStream_t s);
+                             const CUtensorMap& tmQo, int max_grid, cudaStream_t s);
 cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, const CUtensorMap& tmW, cudaStream_t s);
 cudaError_t launch_attention(const FwdArgs& a, __nv_bfloat16* zin, cudaStream_t s);
 cudaError_t launch_attention_tc(const FwdArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmH, __nv_bfloat16* zin,

@@ -53,7 +53,7 @@ template <int BN, int STAGES, int EPI, int NEPI>
 __global__ void __launch_bounds__(64 + NEPI * 32, 1)
     gemm_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap tmA,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmZo,
-                const __grid_constant__ CUtensorMap tmQo, int M, int N, int K, int layer, int n_base) {
+                const __grid_constant__ CUtensorMap tmQo, int M, int N, int K, int layer) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int B_TILE = BN * kBK * 2;
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
       int kc = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const int m0 = (tile / tiles_n) * kBM, n0 = n_base + (tile % tiles_n) * BN;
+        const int m0 = (tile / tiles_n) * kBM, n0 = (tile % tiles_n) * BN;
         for (int kb = 0; kb < nk; ++kb, ++kc) {
           const int s = kc % STAGES;
           if (kc >= STAGES && !mbar_wait(&empty[s], ((kc / STAGES) & 1) ^ 1, abort_flag, a.err)) {
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     int i = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++i) {
-      const int m0 = (tile / tiles_n) * kBM, n0 = n_base + (tile % tiles_n) * BN;
+      const int m0 = (tile / tiles_n) * kBM, n0 = (tile % tiles_n) * BN;
       const int buf = i & 1;
       const int row = m0 + q * 32 + lane;
       const bool live = row < M;
@@ -434,16 +434,15 @@ cudaError_t prepare_gemm() {
                               gemm_smem_bytes<BN, STAGES, EPI>());
 }
 
-// columns [n_base, n_base + N) of the output; a persistent grid of at most max_grid CTAs
+// a persistent grid of at most max_grid CTAs (0: one per SM)
 template <int BN, int STAGES, int EPI, int NEPI>
 cudaError_t launch_gemm(const FwdArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmZo,
-                        const CUtensorMap& tmQo, int M, int N, int K, int layer, cudaStream_t s, int n_base = 0,
-                        int max_grid = 0) {
+                        const CUtensorMap& tmQo, int M, int N, int K, int layer, cudaStream_t s, int max_grid = 0) {
   const int tiles = ((M + kBM - 1) / kBM) * (N / BN);
   const int cap = max_grid > 0 && max_grid < a.num_sms ? max_grid : a.num_sms;
   const int grid = tiles < cap ? tiles : cap;
   return launch_kernel(gemm_kernel<BN, STAGES, EPI, NEPI>, dim3(grid), dim3(64 + NEPI * 32), gemm_smem_bytes<BN, STAGES, EPI>(),
-                       s, a.pdl != 0, a, tmA, tmB, tmZo, tmQo, M, N, K, layer, n_base);
+                       s, a.pdl != 0, a, tmA, tmB, tmZo, tmQo, M, N, K, layer);
 }
 
 constexpr int kTokBN = 128, kTokStages = 4, kTokEpi = 8;
@@ -462,13 +461,10 @@ cudaError_t prepare_gemm_kernels() {
 }
 
 cudaError_t launch_tokenizer(const FwdArgs& a, const CUtensorMap& tmI, const CUtensorMap& tmW, const CUtensorMap& tmZo,
-                             const CUtensorMap& tmQo, int part, int max_grid, cudaStream_t s) {
+                             const CUtensorMap& tmQo, int max_grid, cudaStream_t s) {
   static_assert(kXD % kTokBN == 0 && kTokN % kTokBN == 0, "token and query columns fall in separate tiles");
   static_assert(kTokBN % 64 == 0 && gemm_smem_bytes<kTokBN, kTokStages, EPI_TOKENIZE>() <= 232448, "staging fits");
-  const int n_base = part == kTokQueries ? kXD : 0;
-  const int N = part == kTokAll ? kTokN : part == kTokTokens ? kXD : kTokN - kXD;
-  return launch_gemm<kTokBN, kTokStages, EPI_TOKENIZE, kTokEpi>(a, tmI, tmW, tmZo, tmQo, a.B, N, kID, 0, s, n_base,
-                                                                max_grid);
+  return launch_gemm<kTokBN, kTokStages, EPI_TOKENIZE, kTokEpi>(a, tmI, tmW, tmZo, tmQo, a.B, kTokN, kID, 0, s, max_grid);
 }
 
 cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, const CUtensorMap& tmW, cudaStream_t s) {
