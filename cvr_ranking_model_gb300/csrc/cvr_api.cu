@@ -418,6 +418,8 @@ FwdArgs make_args(cvr_handle* h, int R, int B, const int32_t* req_ids, const int
   a.attn_state = h->attn_state;
   a.attn_count = h->attn_count;
   a.attn_splits = h->attn_splits;
+  for (int g = 0; g < kG; ++g) a.g_order[g] = g;  // groups by padded length, longest first (stable)
+  std::stable_sort(a.g_order, a.g_order + kG, [&](int x, int y) { return h->L[x] > h->L[y]; });
   a.max_chunks = h->max_chunks;
   a.xu = h->xu;
   a.qb = h->qb;

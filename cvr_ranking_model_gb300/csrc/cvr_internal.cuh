@@ -94,6 +94,8 @@ struct FwdArgs {
   float* attn_state;
   unsigned* attn_count;
   int attn_splits;         // splits of the longest group (grid z of the attention kernel)
+  int g_order[kG];         // attention grid row y runs group g_order[y]: longest sequences first, so that the
+                           // CTAs that set the kernel's length are dispatched before the short ones
   int q_add;               // 1: Q holds the first layer's queries without their mean-pooled sequence term, which
                            // the attention kernel adds (the tokeniser ran before the sequence side finished)
   int max_chunks;

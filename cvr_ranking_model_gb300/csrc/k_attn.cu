@@ -53,7 +53,7 @@ __device__ __forceinline__ float ex2(float x) {
 __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_constant__ FwdArgs a,
                                                                 __nv_bfloat16* __restrict__ zin) {
   extern __shared__ __align__(16) uint8_t smem[];
-  const int g = blockIdx.y, sp = blockIdx.z;
+  const int g = a.g_order[blockIdx.y], sp = blockIdx.z;
   const int b0 = blockIdx.x * kCandPerCta;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;

@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_tc_kernel(const __grid_
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + kNBar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
-  const int g = blockIdx.y, sp = blockIdx.z;
+  const int g = a.g_order[blockIdx.y], sp = blockIdx.z;
   const int b0 = blockIdx.x * kRows;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = a.L[g];
