@@ -121,7 +121,10 @@ cvr_status cvr_create(const cvr_weights* weights, const cvr_config* cfg, void* c
  *   out         [n_cand][2] fp32 pCVR per task, written by the call (caller-owned).
  * Sizes: 1 <= n_req <= n_cand <= 2^20. Workspace grows on demand (first call at a size allocates).
  * Returns CVR_E_SHAPE on sizes out of range, CVR_E_ID_RANGE / CVR_E_INPUT on bad ids, offsets or
- * request ids (detected on the device, never read out of bounds), CVR_E_CUDA on CUDA errors. */
+ * request ids (detected on the device, never read out of bounds), CVR_E_CUDA on CUDA errors.
+ * When the sequence encoder leaves SMs free, part of a call runs on a second stream owned by the handle; it
+ * forks from the handle's stream after the call's first kernel and joins it again before the attention, so
+ * a call stays ordered on the handle's stream like one sequence of kernels. */
 cvr_status cvr_score(cvr_handle* h, int32_t n_req, int32_t n_cand, const int32_t* req_ids, const int64_t* bag_ids,
                      const int64_t* bag_offsets, const int64_t* seq_ids, float* out);
 
@@ -185,7 +188,8 @@ cvr_status cvr_debug_stage(cvr_handle* h, int32_t stage, void* dst, int64_t byte
  *                            CTA per 128 candidates and group); 0 = on the register-tile kernel (default 0:
  *                            with heads 32 wide its many small MMAs keep up better; both meet the same
  *                            tolerance)
- *   CVR_OPT_PROFILE      1 = record a CUDA event after every kernel of a call (read with cvr_stage_times)
+ *   CVR_OPT_PROFILE      1 = record a CUDA event after every kernel of a call (read with cvr_stage_times);
+ *                            such calls keep every kernel on the handle's stream, so each time is one kernel's
  *   CVR_OPT_CUDA_GRAPH   1 = replay the call's kernel sequence from a CUDA graph captured per (n_req, n_cand)
  *                            (default 1); 0 = launch eagerly
  *   CVR_OPT_PDL          1 = launch each kernel with programmatic dependent launch, so its prologue overlaps
