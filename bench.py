@@ -62,7 +62,7 @@ def algorithmic_work(wl, nnz: int, seq_events=None):
         "attention": NL * B * 4 * D * SL,                        # q.k and p.v: 2 * 2 * 128 per position
         "token_mixer": NL * B * 16 * swiglu_row,
         "ple": B * 2 * 2048 * (768 + 6),
-        "heads": B * 2 * (2 * 256 * 128 + 128),
+        "heads": B * 2 * 2 * (256 * 128 + 128),                  # 2 tasks x (256->128 and 128->1) MACs x 2
     }
     bf16_weights = (1664 * 512 + 3 * (512 * 128 + 128 * 256) + NL * (3 * 128 * 1792 + 512 * 128 + 128 * 256)
                     + 774 * 2048 + 2 * 128 * 256) * 2
