@@ -125,7 +125,11 @@ def measured_traffic(config: str, kernel: str):
 
 # ---------------------------------------------------------------------------------------------
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clocks and throttle reasons (every 20 ms) around the timed region.
+
+    A timed region of a few ms holds one sample at best, so the same steps go on (``soak``) for about a
+    second right after it, under the same sampler: the clock record covers the timed region and that window
+    of identical work, and says how many samples fell inside each."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -135,13 +139,14 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t_timed_end = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu=timestamp,{self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -149,8 +154,14 @@ class ClockSampler:
         self.t0 = time.time()
         return self
 
+    def mark_timed_end(self):
+        """End of the timed region (what follows until exit is the soak window)."""
+        self.t_timed_end = time.time()
+
     def __exit__(self, *exc):
         self.t1 = time.time()
+        if self.t_timed_end is None:
+            self.t_timed_end = self.t1
         time.sleep(0.1)
         if self.proc:
             self.proc.terminate()
@@ -160,12 +171,12 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        """Median SM clock and the throttle reasons seen among the samples taken inside the timed region
-        (all samples if none falls inside it)."""
+        """Median SM clock and the throttle reasons seen among the samples taken inside the timed region and
+        the soak window after it (all samples if none falls inside them)."""
         from datetime import datetime
         if not self.proc or not self.path or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows, inside = [], []
+        rows, inside, timed = [], [], 0
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 10:
@@ -178,6 +189,7 @@ class ClockSampler:
             rows.append(row)
             if self.t0 <= ts <= self.t1:
                 inside.append(row)
+                timed += ts <= self.t_timed_end
         os.unlink(self.path)
         use = inside or rows
         if not use:
@@ -185,8 +197,11 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for _, _, r in use for i, v in enumerate(r) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[0] for r in use), "sm_max_mhz": max(r[1] for r in use),
-                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside),
-                "timed_region_s": round(self.t1 - self.t0, 3)}
+                "sm_mhz_min": min(r[0] for r in use), "reasons": reasons, "samples": len(use),
+                "samples_in_timed_region": timed, "samples_in_soak": len(inside) - timed,
+                "timed_region_s": round(self.t_timed_end - self.t0, 4),
+                "soak_s": round(self.t1 - self.t_timed_end, 3),
+                "window": "timed region, then the same steps repeated for the soak window"}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -248,6 +263,43 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------------------------
+def gather_roofline(dev: str, stream, flush, peak_bw: float, n_steps: int = 50):
+    """The embedding gathers on a workload where they move enough bytes to be bandwidth-bound: deep, 32
+    requests x 2048 candidates (a1-a3: 1.2 M bag ids and 115 k sequence events, ~340 MB of algorithmic bytes).
+    The sparse kernel's time comes from the events the scorer records after each kernel (profiling on), L2
+    flushed before every step."""
+    import torch
+
+    import cvr_ranking_model_gb300 as cvr
+    import synth
+    from synth.harness import DeviceWorkload, make_scorer
+    wl = synth.make_workload("deep", n_cand=2048)
+    w = synth.make_weights(wl.n_layers, synth.default_seed("deep"))
+    with torch.cuda.stream(stream):
+        dw = DeviceWorkload(wl, device=dev)
+    torch.cuda.synchronize(dev)
+    sc = make_scorer(dw, w, stream=stream.cuda_stream)
+    sc.set_option(cvr.OPT_PROFILE, 1)
+    r, b, o, s, out = dw.ptrs()
+    ms = []
+    with torch.cuda.stream(stream):
+        for i in range(3 + n_steps):
+            flush.zero_()
+            sc.score(wl.n_req, wl.n_cand, r, b, o, s, out)
+            if i >= 3:
+                ms.append(sum(t for name, t in sc.stage_list() if name == "sparse"))
+    sc.close()
+    nnz = int(wl.bag_offsets[-1])
+    _, _, sparse_bytes = algorithmic_work(wl, nnz)
+    t = statistics.median(ms)
+    gbs = sparse_bytes / (t / 1e3) / 1e9
+    return {"kernel": "sparse", "workload": f"deep: R={wl.n_req} x C=2048, L={'/'.join(map(str, wl.seq_len))}, "
+                                           f"{nnz} bag ids, tables 100000/1000000 rows",
+            "bound": "hbm", "achieved": gbs, "peak": peak_bw, "unit": "GB/s", "frac": gbs / peak_bw,
+            "bytes_per_launch": sparse_bytes, "launch_ms": t, "traffic": measured_traffic("deep2048", "sparse"),
+            "timing": f"median of {n_steps} launches, events after each kernel, L2 flushed before each step"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -258,6 +310,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-gather", action="store_true", help="skip the embedding-gather roofline on deep C=2048")
     ap.add_argument("--varlen", action="store_true",
                     help="variable-length sequences: every request's length per group uniform in [1, L_g]")
     args = ap.parse_args()
@@ -348,23 +401,54 @@ def main():
             dist.barrier()
         return [starts[i].elapsed_time(ends[i]) for i in range(n_steps)], stages, n_launch
 
-    # timed region: the scoring calls alone (no per-kernel events inside the graph)
+    # timed region: the scoring calls alone (no per-kernel events inside the graph); then the same steps for
+    # about a second more under the clock sampler (the soak window), which is not timed
     with ClockSampler(local) as clocks:
         step_ms, _, launches = timed_region(profile=False, n_steps=args.steps)
+        clocks.mark_timed_end()
+        t_soak = time.time()
+        with torch.cuda.stream(stream):
+            while time.time() - t_soak < 1.0:
+                for _ in range(50):
+                    flush.zero_()
+                    if args.varlen:
+                        sc.score_varlen_async(wl.n_req, B, r, b, o, s, d_lens.data_ptr(), out)
+                    else:
+                        sc.score_async(wl.n_req, B, r, b, o, s, out)
+                sc.sync()
     total_ms = sum(step_ms)
     total_ms = max_over_ranks(total_ms, dev)
     # second timed region, same steps, with an event recorded after every kernel: per-kernel durations
     n_prof = min(args.steps, 1000)
     prof_ms, stage_sum, _ = timed_region(profile=True, n_steps=n_prof)
-    # latency of the synchronous call as a caller sees it (host wall clock, L2 flushed before each call)
-    call_ms = []
-    with torch.cuda.stream(stream):
-        for i in range(min(args.steps, 100)):
-            flush.zero_()
-            torch.cuda.synchronize(dev)
-            t0 = time.perf_counter()
-            step()
-            call_ms.append((time.perf_counter() - t0) * 1e3)
+    # request latency as the caller sees it: host wall clock around the synchronous call (argument checks, graph
+    # launch, the wait and the error-word read), the GPU idle and L2 flushed before each call; 500 calls after
+    # 50 warm-up calls, for the batch and for a single request of the same shape (R = 1, same C)
+    def call_latency(n_req, n_cand, ptrs, n_calls=500, n_warm=50):
+        rr, bb, oo, ss, oo_out = ptrs
+        sc.set_option(cvr.OPT_PROFILE, 0)
+        ms = []
+        with torch.cuda.stream(stream):
+            for i in range(n_warm + n_calls):
+                flush.zero_()
+                torch.cuda.synchronize(dev)
+                t0 = time.perf_counter()
+                sc.score(n_req, n_cand, rr, bb, oo, ss, oo_out)
+                if i >= n_warm:
+                    ms.append((time.perf_counter() - t0) * 1e3)
+        return ms
+
+    call_ms = call_latency(wl.n_req, B, (r, b, o, s, out)) if not args.varlen else []
+    r1 = None
+    if not args.varlen:
+        wl1 = synth.make_workload(args.config, n_req=1, n_cand=args.n_cand)
+        with torch.cuda.stream(stream):
+            dw1 = DeviceWorkload(wl1, device=dev, tables=dw.tables)
+        torch.cuda.synchronize(dev)
+        r1_ms = call_latency(1, wl1.n_cand, dw1.ptrs())
+        r1 = {"n_req": 1, "n_cand": wl1.n_cand, "p50_ms": statistics.median(r1_ms),
+              "p99_ms": float(np.percentile(r1_ms, 99)),
+              "what": "synchronous cvr_score call, host wall clock, 500 calls after 50 warm-up, L2 flushed"}
     value = job_throughput(world, B, args.steps, total_ms)
 
     # per-kernel times (events recorded between the kernels, on the scorer's stream, every timed step)
@@ -432,6 +516,10 @@ def main():
                "d2h_bytes_per_step": int(h_out.nbytes), "p50_ms": statistics.median(e_ms),
                "api": "cvr_score_host (pinned host buffers, read and written in place by the kernels)"}
 
+    gather = None
+    if rank == 0 and not args.no_gather and not args.varlen:
+        gather = gather_roofline(dev, stream, flush, peak_bw)
+
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
@@ -449,9 +537,15 @@ def main():
                        **({"seq_lens": f"variable: uniform in [1, L_g] per request and group, "
                                        f"{float(lens.sum()) / wl.n_req:.1f} of {wl.sum_len} events per request"}
                           if args.varlen else {})},
-            "p50_ms": p50, "p99_ms": p99, "call_p50_ms": statistics.median(call_ms),
-            "call_p99_ms": float(np.percentile(call_ms, 99)), "profiled_p50_ms": statistics.median(prof_ms),
-            "roofline": roofline, "sparse_roofline": sparse, "path_roofline": path,
+            "latency": ({"p50_ms": statistics.median(call_ms), "p99_ms": float(np.percentile(call_ms, 99)),
+                         "what": "request latency: synchronous cvr_score call on the batch, host wall clock "
+                                 "(checks, graph launch, wait, error-word read), 500 calls after 50 warm-up, "
+                                 "L2 flushed and the GPU idle before each"} if call_ms else None),
+            "r1_latency_ms": r1["p50_ms"] if r1 else None, "single_request": r1,
+            "p50_ms": p50, "p99_ms": p99, "device_time": "p50_ms / p99_ms: GPU time of one batch (CUDA events "
+                                                          "around back-to-back calls)",
+            "profiled_p50_ms": statistics.median(prof_ms),
+            "roofline": roofline, "sparse_roofline": sparse, "gather_roofline": gather, "path_roofline": path,
             "stage_ms": {k: round(v, 5) for k, v in per_kernel.items()},
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks.summary(),
             "gpu_launches": launches,

@@ -115,27 +115,25 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
     const int64_t n_units = (n_bags + 3) / 4;
     const int grp = lane >> 3, sub = lane & 7;  // bag of this lane within the unit, its 4 columns
     auto bag_of = [&](int64_t u) { return min(u * 4 + grp, n_bags - 1); };
+    // A bag's [s, e) from the offsets, checked where it is loaded: a negative start or an end before the start
+    // is reported and the bag is read as empty, so no id is ever read outside bag_ids.
+    auto load_bag = [&](int64_t b, int64_t& s, int64_t& e) {
+      s = a.bag_offsets[b];
+      e = a.bag_offsets[b + 1];
+      if (s < 0 || e < s) {
+        errbits |= kErrOffsets;
+        s = e = 0;
+      }
+    };
     int64_t u0 = gw, s0 = 0, e0 = 0, id0 = 0, s1 = 0, e1 = 0;
-    if (u0 < n_units) {
-      const int64_t b = bag_of(u0);
-      s0 = a.bag_offsets[b];
-      e0 = a.bag_offsets[b + 1];
-    }
-    if (u0 + nw < n_units) {
-      const int64_t b = bag_of(u0 + nw);
-      s1 = a.bag_offsets[b];
-      e1 = a.bag_offsets[b + 1];
-    }
+    if (u0 < n_units) load_bag(bag_of(u0), s0, e0);
+    if (u0 + nw < n_units) load_bag(bag_of(u0 + nw), s1, e1);
     if (u0 < n_units && s0 + sub < e0) id0 = a.bag_ids[s0 + sub];
     while (u0 < n_units) {  // warp-uniform
       const int64_t u1 = u0 + nw, u2 = u1 + nw;
       // stage A: offsets of unit k+2; stage B: first ids of unit k+1 (raw; checked when used)
       int64_t s2 = 0, e2 = 0, id1 = 0;
-      if (u2 < n_units) {
-        const int64_t b = bag_of(u2);
-        s2 = a.bag_offsets[b];
-        e2 = a.bag_offsets[b + 1];
-      }
+      if (u2 < n_units) load_bag(bag_of(u2), s2, e2);
       if (u1 < n_units && s1 + sub < e1) id1 = a.bag_ids[s1 + sub];
       // stage C: the rows of unit k
       const int64_t bag_raw = u0 * 4 + grp;
@@ -153,12 +151,7 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
         dst = a.I + (ib / kFi) * kID + f * kE;
       }
       const int64_t rows = a.table_rows[field];
-      const int64_t s = s0;
-      int64_t e = e0;
-      if (e < s) {
-        if (live) errbits |= kErrOffsets;
-        e = s;
-      }
+      const int64_t s = s0, e = e0;  // (checked when loaded)
       // The 8 lanes of a bag hold 8 ids at once (one each), share them by shuffle, then have all 8 rows in
       // flight; the fp32 sum still runs in bag order from 0 (bit-exact with the definition). The loop count
       // is the warp's largest bag, so every lane reaches every shuffle.

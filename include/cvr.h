@@ -114,7 +114,9 @@ cvr_status cvr_create(const cvr_weights* weights, const cvr_config* cfg, void* c
 /* Scores one batch of n_req requests and n_cand candidates (all DEVICE pointers):
  *   req_ids     [n_cand] int32: request index of each candidate, in [0, n_req), non-decreasing.
  *   bag_offsets [n_req*8 + n_cand*8 + 1] int64 CSR offsets into bag_ids: first the user bags in
- *               (request, field) order, then the item bags in (candidate, field) order; non-decreasing.
+ *               (request, field) order, then the item bags in (candidate, field) order; non-negative and
+ *               non-decreasing (normally bag_offsets[0] = 0). A negative or decreasing offset returns
+ *               CVR_E_INPUT and its bag is read as empty.
  *   bag_ids     [bag_offsets[last]] int64 row ids, local to each field's table. An empty bag pools to 0.
  *   seq_ids     [n_req][sum(seq_len)][4] int64 rows of the shared sequence table; per request the
  *               events of group 0, then group 1, then group 2.

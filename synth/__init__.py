@@ -170,7 +170,7 @@ def make_workload(name: str, n_req: Optional[int] = None, n_cand: Optional[int] 
     field[: R * Fu] = np.tile(np.arange(Fu, dtype=np.int32), R)
     field[R * Fu:] = np.tile(np.arange(Fu, Fu + Fi, dtype=np.int32), B)
     rows = np.array([c["user_rows"]] * Fu + [c["item_rows"]] * Fi, dtype=np.int64)
-    assert 1 <= c["bag_min"] <= c["bag_max"] <= 64
+    assert 0 <= c["bag_min"] <= c["bag_max"] <= 64  # bag_min = 0 draws empty bags
     offsets = np.empty(n_bags + 1, dtype=np.int64)
     lib().synth_bags(sd, n_bags, _ptr(field), _ptr(rows), c["bag_min"], c["bag_max"], c["zipf_s"], _ptr(offsets), None)
     ids = np.empty(int(offsets[-1]), dtype=np.int64)

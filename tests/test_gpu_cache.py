@@ -9,8 +9,9 @@ cache warming up.
 import numpy as np
 import pytest
 
+import oracle
 import synth
-from gpu_util import GpuRun
+from gpu_util import GpuRun, assert_pcvr_close
 
 pytestmark = pytest.mark.gpu
 
@@ -40,6 +41,24 @@ def _assert_same(a, b, what):
         assert np.array_equal(x, y, equal_nan=True), f"{what}: {name} differs from the all-HBM path"
 
 
+def _assert_oracle(got, wl, w, what, requests=None):
+    """The cached call against the CPU oracle itself: pooled fp32 bits and resolved rows of the scored
+    requests' bags, and pCVR within the acceptance tolerance."""
+    pooled, rows, out = got
+    ref = oracle.score(wl, w, dumps=True, requests=requests)
+    assert ref.status == 0
+    sel = np.ones(wl.n_cand, bool) if requests is None else np.isin(wl.req_ids, requests)
+    reqs = range(wl.n_req) if requests is None else requests
+    bags = np.concatenate([np.arange(r * 8, r * 8 + 8) for r in reqs] +
+                          [wl.n_req * 8 + np.arange(c * 8, c * 8 + 8) for c in np.nonzero(sel)[0]])
+    assert np.array_equal(pooled[bags].view(np.uint32), ref.dumps["pooled"][bags].view(np.uint32)), \
+        f"{what}: pooled fp32 not bit-exact with the oracle"
+    for bag in bags:
+        lo, hi = wl.bag_offsets[bag], wl.bag_offsets[bag + 1]
+        assert np.array_equal(rows[lo:hi], ref.dumps["rows"][lo:hi]), f"{what}: rows of bag {bag} differ"
+    assert_pcvr_close(out.astype(np.float64)[sel], ref.out[sel], what)
+
+
 def _workload(seed=None, n_req=2):
     return synth.make_workload("prod", n_req=n_req, seed=seed)
 
@@ -56,7 +75,10 @@ def test_cached_host_tables_give_identical_bits_and_warm_up():
         g.sc.cache_enable(t, 1 << 14)
     hit_rates = []
     for call in range(3):
-        _assert_same(_run(g), ref, f"call {call}")
+        got = _run(g)
+        _assert_same(got, ref, f"call {call}")
+        if call == 1:  # a warm call, served mostly from the caches
+            _assert_oracle(got, wl, w, "warm cached call")
         hits, misses = g.sc.cache_stats()
         assert hits + misses > 0
         hit_rates.append(hits / (hits + misses))
@@ -85,7 +107,10 @@ def test_varying_batches_evict_and_stay_exact():
                                   device="cuda:0")
             g.rows = torch.full((max(len(wl.bag_ids), 1),), -7, dtype=torch.int64, device="cuda:0")
         ref = _run(GpuRun(wl, w, tables=dev))
-        _assert_same(_run(g), ref, f"batch {i} (seed {seed})")
+        got = _run(g)
+        _assert_same(got, ref, f"batch {i} (seed {seed})")
+        if i == 3:  # a batch seen before, after three others evicted part of its rows
+            _assert_oracle(got, wl, w, f"batch {i} (seed {seed})", requests=[0])
     hits, misses = g.sc.cache_stats()
     assert hits > 0 and misses > 0
 

@@ -97,6 +97,23 @@ def test_two_layers_small():
     _check_full(wl, w, stages=True)
 
 
+@pytest.mark.parametrize("bag_min,bag_max", [(0, 3), (9, 17), (0, 64)])
+def test_empty_and_long_bags(bag_min, bag_max):
+    # empty bags (pool to 0) on the user and the item side, and bags longer than the 8 ids a bag's lanes hold
+    # at once (the second and later passes of the gather's id loop: 9, 16, 17 and 64 ids), bit for bit
+    wl = synth.make_workload("tiny", n_req=3, n_cand=37, bag_min=bag_min, bag_max=bag_max, user_rows=5000,
+                             item_rows=5000)
+    sizes = np.diff(wl.bag_offsets)
+    nu = wl.n_req * 8
+    if bag_min == 0:
+        assert (sizes[:nu] == 0).any() and (sizes[nu:] == 0).any(), "the workload has empty user and item bags"
+    for n in (9, 16, 17, 64):
+        if bag_min <= n <= bag_max:
+            assert (sizes == n).any(), f"the workload has a bag of {n} ids"
+    w = synth.make_weights(wl.n_layers, wl.seed, bias_scale=0.02)
+    _check_full(wl, w, stages=True)
+
+
 def test_single_request_single_candidate():
     wl = synth.make_workload("tiny", n_req=1, n_cand=1, seq_len=(1, 1, 1))
     w = synth.make_weights(wl.n_layers, wl.seed)
@@ -129,11 +146,27 @@ def test_host_entry_point_matches_device_entry_point():
     dev = g.out()
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory().numpy()
     arrays = [wl.req_ids, wl.bag_ids, wl.bag_offsets, np.ascontiguousarray(wl.seq_ids)]
+    ref = oracle.score(wl, w).out
     for mask in (0b00000, 0b11111, 0b01010, 0b10101):
         ins = [pin(a) if mask >> i & 1 else np.ascontiguousarray(a) for i, a in enumerate(arrays)]
         out = pin(np.zeros((wl.n_cand, 2), np.float32)) if mask >> 4 & 1 else np.zeros((wl.n_cand, 2), np.float32)
         g.sc.score_host(wl.n_req, wl.n_cand, *ins, out)
         assert np.array_equal(out.astype(np.float64), dev), f"pinned mask {mask:05b}"
+        assert_pcvr_close(out.astype(np.float64), ref, f"host entry point, pinned mask {mask:05b}")
+
+
+def test_host_entry_point_prod_matches_oracle():
+    # the host-buffer entry point on the production shape (pinned inputs read in place, as the benchmark's
+    # end-to-end leg calls it), every candidate against the oracle
+    import torch
+    wl = synth.make_workload("prod")
+    w = synth.make_weights(wl.n_layers, wl.seed)
+    g = GpuRun(wl, w, debug=False)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory().numpy()
+    ins = [pin(a) for a in (wl.req_ids, wl.bag_ids, wl.bag_offsets, np.ascontiguousarray(wl.seq_ids))]
+    out = pin(np.zeros((wl.n_cand, 2), np.float32))
+    g.sc.score_host(wl.n_req, wl.n_cand, *ins, out)
+    assert_pcvr_close(out.astype(np.float64), oracle.score(wl, w).out, "prod through the host entry point")
 
 
 # ------------------------------------------------------------------ error reporting (no fault)
@@ -169,6 +202,22 @@ def test_bad_offsets_and_request_ids_are_reported():
     wl4.req_ids[-1] = 99                           # out of range
     g = GpuRun(wl4, w)
     assert g.run(check=False) == 6
+
+
+def test_negative_offsets_are_reported_not_read():
+    # a negative first offset (and a negative offset in the middle) would point before bag_ids: the bag is read
+    # as empty and the call reports CVR_E_INPUT; the handle keeps working
+    wl = synth.make_workload("tiny")
+    w = synth.make_weights(wl.n_layers, wl.seed)
+    for pos, val in ((0, -3), (5, -1)):
+        bad = synth.make_workload("tiny")
+        bad.bag_offsets = bad.bag_offsets.copy()
+        bad.bag_offsets[pos] = val
+        g = GpuRun(bad, w)
+        assert g.run(check=False) == 6
+        assert np.all(g.pooled.cpu().numpy()[pos] == 0.0), "the malformed bag pools to zero"
+    g = GpuRun(wl, w)
+    assert g.run(check=False) == 0
 
 
 def test_shape_errors_on_the_host():

@@ -54,3 +54,15 @@ def test_weights_are_bf16_valued_glorot():
     assert np.all(w["tok_b"] == 0) and np.all(w["l0_tm_gain"] == 1)
     wb = synth.make_weights(1, 123, bias_scale=0.05, gain_jitter=0.1)
     assert np.abs(wb["tok_b"]).max() > 0 and np.abs(wb["l0_tm_gain"] - 1).max() > 0
+
+
+def test_bag_sizes_span_empty_and_long_bags():
+    # bag_min = 0 draws empty bags, bag_max up to 64 long ones; sizes are uniform over [bag_min, bag_max]
+    wl = synth.make_workload("tiny", n_req=4, n_cand=60, bag_min=0, bag_max=64)
+    sizes = np.diff(wl.bag_offsets)
+    assert sizes.min() == 0 and sizes.max() == 64
+    assert abs(sizes.mean() - 32) < 2.5
+    assert len(wl.bag_ids) == wl.bag_offsets[-1]
+    # and repeatable
+    a = synth.make_workload("tiny", n_req=4, n_cand=60, bag_min=0, bag_max=64)
+    assert np.array_equal(a.bag_ids, wl.bag_ids)
