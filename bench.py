@@ -3,7 +3,7 @@
 python bench.py [--gpus N] [--steps K] [--warmup W] [--config prod] [--impl reference]
 
 A step is one cvr_score call over one full batch of the workload (all stages of the forward pass:
-embedding bags, sequence encoders, tokeniser, Query Decoding, Token Mixer, PLE, heads), inputs
+embedding bags, sequence encoders, tokeniser, Query Decoding, Token Mixer, PLE with the heads), inputs
 resident in HBM, L2 flushed (256 MB write) before every step and each step timed alone with CUDA
 events on the scorer's stream. ``e2e`` repeats the measurement through cvr_score_host with pinned
 host buffers, which the kernels read (inputs) and write (output) in place over the C2C link inside the
@@ -61,8 +61,8 @@ def algorithmic_work(wl, nnz: int, seq_events=None):
         "query": NL * B * 2 * 1664 * 384,
         "attention": NL * B * 4 * D * SL,                        # q.k and p.v: 2 * 2 * 128 per position
         "token_mixer": NL * B * 16 * swiglu_row,
-        "ple": B * 2 * 2048 * (768 + 6),
-        "heads": B * 2 * 2 * (256 * 128 + 128),                  # 2 tasks x (256->128 and 128->1) MACs x 2
+        # PLE experts and gates, then per task the heads 256->128 and 128->1 (one kernel)
+        "ple_heads": B * 2 * 2048 * (768 + 6) + B * 2 * 2 * (256 * 128 + 128),
     }
     bf16_weights = (1664 * 512 + 3 * (512 * 128 + 128 * 256) + NL * (3 * 128 * 1792 + 512 * 128 + 128 * 256)
                     + 774 * 2048 + 2 * 128 * 256) * 2
@@ -311,10 +311,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-gather", action="store_true", help="skip the embedding-gather roofline on deep C=2048")
+    ap.add_argument("--minimal", action="store_true",
+                    help="warm-up and timed steps only (for profiler captures): no clock soak, latency loops, "
+                         "per-kernel region, end-to-end leg, gather roofline or CPU baseline")
     ap.add_argument("--varlen", action="store_true",
                     help="variable-length sequences: every request's length per group uniform in [1, L_g]")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.minimal:
+        args.no_cpu_baseline = args.no_e2e = args.no_gather = True
     if args.impl == "reference":
         run_reference(args)
         return
@@ -408,7 +413,7 @@ def main():
         clocks.mark_timed_end()
         t_soak = time.time()
         with torch.cuda.stream(stream):
-            while time.time() - t_soak < 1.0:
+            while not args.minimal and time.time() - t_soak < 1.0:
                 for _ in range(50):
                     flush.zero_()
                     if args.varlen:
@@ -420,7 +425,9 @@ def main():
     total_ms = max_over_ranks(total_ms, dev)
     # second timed region, same steps, with an event recorded after every kernel: per-kernel durations
     n_prof = min(args.steps, 1000)
-    prof_ms, stage_sum, _ = timed_region(profile=True, n_steps=n_prof)
+    prof_ms, stage_sum = [float("nan")], {}
+    if not args.minimal:
+        prof_ms, stage_sum, _ = timed_region(profile=True, n_steps=n_prof)
     # request latency as the caller sees it: host wall clock around the synchronous call (argument checks, graph
     # launch, the wait and the error-word read), the GPU idle and L2 flushed before each call; 500 calls after
     # 50 warm-up calls, for the batch and for a single request of the same shape (R = 1, same C)
@@ -438,9 +445,9 @@ def main():
                     ms.append((time.perf_counter() - t0) * 1e3)
         return ms
 
-    call_ms = call_latency(wl.n_req, B, (r, b, o, s, out)) if not args.varlen else []
+    call_ms = call_latency(wl.n_req, B, (r, b, o, s, out)) if not (args.varlen or args.minimal) else []
     r1 = None
-    if not args.varlen:
+    if not (args.varlen or args.minimal):
         wl1 = synth.make_workload(args.config, n_req=1, n_cand=args.n_cand)
         with torch.cuda.stream(stream):
             dw1 = DeviceWorkload(wl1, device=dev, tables=dw.tables)

@@ -9,7 +9,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcvr.so")
-SOURCES = ["cvr_api.cu", "k_sparse.cu", "k_mlp.cu", "k_gemm.cu", "k_attn.cu", "k_attn_tc.cu"]
+SOURCES = ["cvr_api.cu", "k_sparse.cu", "k_mlp.cu", "k_gemm.cu", "k_ple.cu", "k_attn.cu", "k_attn_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

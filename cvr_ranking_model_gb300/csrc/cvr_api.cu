@@ -59,8 +59,8 @@ struct GraphEntry {
   int launches = 0;
 };
 
-const char* kStageNames[] = {"sparse", "seq_mlp", "seq_colsum", "tokenizer", "query", "attention", "token_mixer", "ple",
-                             "heads", "cache_admit"};
+const char* kStageNames[] = {"sparse", "seq_mlp", "seq_colsum", "tokenizer", "query", "attention", "token_mixer",
+                             "ple_heads", "cache_admit"};
 
 }  // namespace
 
@@ -94,6 +94,9 @@ struct cvr_handle {
   int* err = nullptr;
   unsigned* done = nullptr;
   unsigned* cs_count = nullptr;
+  unsigned* ple_ready = nullptr;  // per 128-row block: Token Mixer tiles written
+  bf16* Rt = nullptr;             // [2][B_cap][256] gate-weighted expert sums
+  unsigned* xu_ready = nullptr;   // [R_cap/128][16] user row-tiles of the tokeniser written
   int32_t* req_copy = nullptr;  // the call's request ids in the workspace
   float* attn_state = nullptr;
   unsigned* attn_count = nullptr;
@@ -104,8 +107,8 @@ struct cvr_handle {
   void* stage = nullptr;
   size_t stage_bytes = 0;
   // tensor maps
-  CUtensorMap tm_seqW13, tm_seqW2, tm_tokI, tm_qW[kMaxLayers], tm_tmW13, tm_tmW2, tm_pleW, tm_headW1;
-  CUtensorMap tm_Xs, tm_I, tm_x_Z, tm_x_Y, tm_5_Z, tm_5_Y, tm_full_Z, tm_full_Y, tm_Q, tm_H, tm_Ex;
+  CUtensorMap tm_seqW13, tm_seqW2, tm_tokI, tm_tokU, tm_qW[kMaxLayers], tm_tmW13, tm_tmW2, tm_pleW, tm_headW1;
+  CUtensorMap tm_Xs, tm_I, tm_U, tm_x_Z, tm_x_Y, tm_5_Z, tm_5_Y, tm_full_Z, tm_full_Y, tm_Q, tm_H, tm_R, tm_Ex;
   // graphs, profiling
   bool use_graph = true, profile = false, pdl = true;
   bool attn_tc = false;  // cross-attention on the tcgen05 kernel instead of the register-tile one
@@ -148,20 +151,6 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Expert outputs Ex[rows][768] (bf16), plain layout, boxes of [128 rows][208 columns]: the PLE epilogue's
-// TMA stores (columns past 768 are clipped)
-bool encode_ex(CUtensorMap* m, const void* base, uint64_t rows) {
-  EncodeTiledFn enc = get_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)kPleN, rows};
-  cuuint64_t strides[1] = {(cuuint64_t)kPleN * 2};
-  cuuint32_t box[2] = {208, 128};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -262,7 +251,7 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   const int R_cap = std::max(R, h->R_cap);
   const int B_cap = (int)(((int64_t)std::max(B, h->B_cap) + 127) / 128 * 128);
   int max_chunks = 0;
-  for (int g = 0; g < kG; ++g) max_chunks = std::max(max_chunks, (h->L[g] + 63) / 64);
+  for (int g = 0; g < kG; ++g) max_chunks = std::max(max_chunks, (h->L[g] + 511) / 512);  // column-sum blocks
   const int64_t seq_rows = (int64_t)R_cap * h->SL;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -270,7 +259,8 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
     off += (bytes + 1023) / 1024 * 1024;
     return o;
   };
-  const size_t oU = take((size_t)R_cap * kUD * 2), oI = take((size_t)B_cap * kID * 2);
+  const int R_pad = (R_cap + 127) / 128 * 128;  // U is read by the tokeniser in 128-row tiles
+  const size_t oU = take((size_t)R_pad * kUD * 2), oI = take((size_t)B_cap * kID * 2);
   const size_t oXs = take((size_t)seq_rows * kD * 2), oH = take((size_t)seq_rows * kD * 2);
   const size_t oCs = take((size_t)R_cap * kG * max_chunks * kD * 4), oXu = take((size_t)R_cap * kTokN * 4);
   const size_t oQb = take((size_t)h->n_layers * R_cap * kG * kD * 4);
@@ -278,6 +268,10 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   const size_t oQ = take((size_t)B_cap * kG * kD * 2), oEx = take((size_t)B_cap * kPleN * 2);
   const size_t oG = take((size_t)B_cap * 8 * 4), oErr = take(1024), oCnt = take((size_t)R_cap * kG * 4);
   const size_t oReq = take((size_t)B_cap * 4);
+  const size_t ready_bytes = (size_t)(B_cap + 127) / 128 * 4;  // Token Mixer tiles written per 128-row block
+  const size_t oRdy = take(ready_bytes);
+  const size_t oR = take((size_t)2 * B_cap * kDE * 2);
+  const size_t oXr = take((size_t)R_pad / 128 * (kTokN / 128) * 4);
   int splits = 1;
   for (int g = 0; g < kG; ++g) splits = std::max(splits, split_count(h->L[g]));
   // attention split state and merge counters, sized for either attention kernel: the register-tile one keeps
@@ -311,12 +305,16 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   h->done = (unsigned*)(b + oErr + 256);
   h->cs_count = (unsigned*)(b + oCnt);
   h->req_copy = (int32_t*)(b + oReq);
+  h->ple_ready = (unsigned*)(b + oRdy);
+  h->Rt = (bf16*)(b + oR);
+  h->xu_ready = (unsigned*)(b + oXr);
   h->attn_splits = splits;
   h->attn_state = splits > 1 ? (float*)(b + oAst) : nullptr;
   h->attn_count = (unsigned*)(b + oAcnt);
   e = cudaMemset(h->err, 0, 1024);  // error word and CTA counter start at zero; the last kernel resets them
   if (e == cudaSuccess) e = cudaMemset(h->cs_count, 0, (size_t)R_cap * kG * 4);  // reset by their last block
   if (e == cudaSuccess) e = cudaMemset(h->attn_count, 0, cnt_bytes);  // reset by the merging CTA or warp
+  if (e == cudaSuccess) e = cudaMemset(h->ple_ready, 0, ready_bytes);  // (also cleared by every call's first kernel)
   if (e != cudaSuccess) {
     free_workspace(h);
     return fail(h, CVR_E_CUDA, "workspace initialisation failed");
@@ -326,13 +324,15 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   h->max_chunks = max_chunks;
   bool ok = encode_2d(&h->tm_Xs, h->Xs, kD, (uint64_t)seq_rows, kD, 64, 128) &&
             encode_2d(&h->tm_I, h->I, kID, B_cap, kID, 64, 128) &&
+            encode_2d(&h->tm_U, h->U, kUD, R_pad, kUD, 64, 128) &&
             encode_2d(&h->tm_x_Z, h->Z, kXD, B_cap, kYD, 64, 128) &&
             encode_2d(&h->tm_x_Y, h->Y, kXD, B_cap, kYD, 64, 128) && encode_mix5d(&h->tm_5_Z, h->Z, B_cap) &&
             encode_mix5d(&h->tm_5_Y, h->Y, B_cap) && encode_2d(&h->tm_full_Z, h->Z, kYD, B_cap, kYD, 64, 128) &&
             encode_2d(&h->tm_full_Y, h->Y, kYD, B_cap, kYD, 64, 128) &&
             encode_2d(&h->tm_Q, h->Q, kG * kD, B_cap, kG * kD, 64, 128) &&
             encode_2d(&h->tm_H, h->H, kD, (uint64_t)seq_rows, kD, 64, 64) &&
-            encode_ex(&h->tm_Ex, h->Ex, B_cap);
+            encode_2d(&h->tm_R, h->Rt, kDE, (uint64_t)2 * B_cap, kDE, 64, 128) &&
+            encode_2d(&h->tm_Ex, h->Ex, kPleN, B_cap, kPleN, 64, 128);
   if (!ok) {
     free_workspace(h);
     return fail(h, CVR_E_CUDA, "cuTensorMapEncodeTiled failed for a workspace tensor");
@@ -422,12 +422,15 @@ FwdArgs make_args(cvr_handle* h, int R, int B, const int32_t* req_ids, const int
   std::stable_sort(a.g_order, a.g_order + kG, [&](int x, int y) { return h->L[x] > h->L[y]; });
   a.max_chunks = h->max_chunks;
   a.xu = h->xu;
+  a.xu_ready = h->xu_ready;
   a.qb = h->qb;
   a.Z = h->Z;
   a.Y = h->Y;
   a.Q = h->Q;
   a.Ex = h->Ex;
   a.gates = h->gates;
+  a.ple_ready = h->ple_ready;
+  a.Rt = h->Rt;
   a.err = h->err;
   a.done = h->done;
   a.err_host = h->err_host_dev;
@@ -507,17 +510,22 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
   if (fork) {
     if (e == cudaSuccess) e = cudaEventRecord(h->ev_fork, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
-    run(launch_xu(af, false, h->side), "user_gemv");
-    run(launch_tokenizer(af, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, a.num_sms - seq_grid, h->side),
+    // (without a programmatic edge: its CTAs must not queue ahead of the encoder's for the SMs the gather frees)
+    run(launch_tokenizer(af, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, h->tm_U, h->tm_tokU, a.num_sms - seq_grid,
+                         false, h->side),
         kStageNames[3]);
     if (e == cudaSuccess) e = cudaEventRecord(h->ev_join, h->side);
-    run(launch_seq_mlp(af, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, false, s), kStageNames[1]);
-    run(launch_seq_colsum(af, s), kStageNames[2]);
+    run(launch_seq_mlp(af, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, s), kStageNames[1]);
+    // the column sums and the attention wait for their inputs where they are launched, not on an SM: CTAs launched
+    // early would sit on the SMs the tokeniser's CTAs need (a tokeniser CTA needs an SM's whole shared memory)
+    FwdArgs an = af;
+    an.pdl = 0;
+    run(launch_seq_colsum(an, s), kStageNames[2]);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_join, 0);
   } else {
-    run(launch_seq_mlp(a, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, true, s), kStageNames[1]);
+    run(launch_seq_mlp(a, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, s), kStageNames[1]);
     run(launch_seq_colsum(a, s), kStageNames[2]);
-    run(launch_tokenizer(a, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, 0, s), kStageNames[3]);
+    run(launch_tokenizer(a, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, h->tm_U, h->tm_tokU, 0, true, s), kStageNames[3]);
   }
   bf16* zin = h->Z;
   bf16* zout = h->Y;
@@ -528,13 +536,15 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
     if (l > 0) run(launch_query(a, l, in_is_Z ? h->tm_x_Z : h->tm_x_Y, h->tm_qW[l], s), kStageNames[4]);
     FwdArgs al = a;  // the first layer's queries may still lack their mean-pooled term (stacked layers' have it)
     al.q_add = l == 0 ? af.q_add : 0;
+    if (l == 0 && fork) al.pdl = 0;  // (after the join: see the column sums above)
     run(h->attn_tc ? launch_attention_tc(al, h->tm_Q, h->tm_H, zin, s) : launch_attention(al, zin, s), kStageNames[5]);
     run(launch_tm_mlp(a, l, zin, zout, in_is_Z ? h->tm_5_Z : h->tm_5_Y, h->tm_tmW13, h->tm_tmW2, s), kStageNames[6]);
   }
-  run(launch_ple(a, zout == h->Z ? h->tm_full_Z : h->tm_full_Y, h->tm_pleW, h->tm_Ex, s), kStageNames[7]);
-  run(launch_heads(a, h->tm_headW1, s), kStageNames[8]);
+  run(launch_ple_heads(a, zout == h->Z ? h->tm_full_Z : h->tm_full_Y, h->tm_pleW, h->tm_R, h->tm_Ex, h->tm_headW1,
+                       h->B_cap, s),
+      kStageNames[7]);
   if (a.cache_on) {
-    run(launch_cache_admit(a, h->c_claim, s), kStageNames[9]);
+    run(launch_cache_admit(a, h->c_claim, s), kStageNames[8]);
     ++n;  // (two kernels)
   }
   h->last_zin = zin;
@@ -630,6 +640,7 @@ cvr_status sync_status(cvr_handle* h) {
     // a CTA that gave up may have left a group or split counter part-way; the next call starts from zero
     if (h->cs_count) cudaMemset(h->cs_count, 0, (size_t)h->R_cap * kG * 4);
     if (h->attn_count) cudaMemset(h->attn_count, 0, attn_count_bytes(h->B_cap));
+    if (h->ple_ready) cudaMemset(h->ple_ready, 0, (size_t)(h->B_cap + 127) / 128 * 4);
     return fail(h, CVR_E_TIMEOUT, "a bounded device-side wait gave up");
   }
   if (ew & kErrLayout) return fail(h, CVR_E_CUDA, "a kernel's shared-memory window was not 1024-byte aligned");
@@ -699,6 +710,7 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
     if (pe == cudaSuccess) pe = prepare_mlp_kernels();
     if (pe == cudaSuccess) pe = prepare_attention_kernel();
     if (pe == cudaSuccess) pe = prepare_attention_tc_kernel();
+    if (pe == cudaSuccess) pe = prepare_ple_kernel();
     if (pe != cudaSuccess) {
       fprintf(stderr, "cvr_create: kernel attribute setup failed: %s\n", cudaGetErrorString(pe));
       cudaGetLastError();
@@ -796,16 +808,26 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
     std::memcpy(F + f_tm_b2 + l * kD, w->tm_b2[l], sizeof(float) * kD);
     std::memcpy(F + f_gain + l * kD, w->tm_gain[l], sizeof(float) * kD);
   }
-  for (int k = 0; k < kNE; ++k) {
-    for (size_t i = 0; i < (size_t)kDE * kYD; ++i) B[o_pleW + (size_t)k * kDE * kYD + i] = f32_to_bf16_bits(w->ple_w[k][i]);
-    std::memcpy(F + f_ple_b + k * kDE, w->ple_b[k], sizeof(float) * kDE);
-  }
-  for (int t = 0; t < kNT; ++t)
-    for (int k = 0; k < kNE; ++k) {
-      for (int c = 0; c < kYD; ++c)
-        B[o_pleW + (size_t)(kPleN + t * kNE + k) * kYD + c] = f32_to_bf16_bits(w->gate_w[t][(size_t)k * kYD + c]);
-      F[f_ple_b + kPleN + t * kNE + k] = w->gate_b[t][k];
+  // PLE rows in 4 slices of 208, one per CTA of a row block's cluster: slice n = units [64n, 64n + 64) of
+  // experts 0, 1, 2, then the 6 gate rows (task-major), then 10 zero rows; biases in the same order
+  for (int n = 0; n < 4; ++n) {
+    for (int j = 0; j < 208; ++j) {
+      const size_t row = (size_t)n * 208 + j;
+      const float* src = nullptr;
+      float bias = 0.f;
+      if (j < kNE * 64) {
+        const int k = j / 64, u = n * 64 + j % 64;
+        src = w->ple_w[k] + (size_t)u * kYD;
+        bias = w->ple_b[k][u];
+      } else if (j < kNE * 64 + kNT * kNE) {
+        const int t = (j - kNE * 64) / kNE, k = (j - kNE * 64) % kNE;
+        src = w->gate_w[t] + (size_t)k * kYD;
+        bias = w->gate_b[t][k];
+      }
+      for (int c = 0; c < kYD; ++c) B[o_pleW + row * kYD + c] = src ? f32_to_bf16_bits(src[c]) : 0;
+      F[f_ple_b + row] = bias;
     }
+  }
   for (int t = 0; t < kNT; ++t) {
     for (size_t i = 0; i < (size_t)kHH * kDE; ++i) B[o_headW1 + (size_t)t * kHH * kDE + i] = f32_to_bf16_bits(w->head_w1[t][i]);
     std::memcpy(F + f_hb1 + t * kHH, w->head_b1[t], sizeof(float) * kHH);
@@ -863,10 +885,11 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
   ok = encode_2d(&h->tm_seqW13, h->seqW13, kD, kG * 512, kD, 64, 256) &&
        encode_2d(&h->tm_seqW2, h->seqW2, kHid, kG * kD, kHid, 64, 128) &&
        encode_2d(&h->tm_tokI, h->tokI, kID, kTokN, kID, 64, 128) &&
+       encode_2d(&h->tm_tokU, h->tokU, kUD, kTokN, kUD, 64, 128) &&
        encode_2d(&h->tm_tmW13, h->tmW13, kD, (uint64_t)NL * 512, kD, 64, 256) &&
        encode_2d(&h->tm_tmW2, h->tmW2, kHid, (uint64_t)NL * kD, kHid, 64, 128) &&
        encode_2d(&h->tm_pleW, h->pleW, kYD, kPleCols, kYD, 64, 208) &&
-       encode_2d(&h->tm_headW1, h->headW1, kDE, kNT * kHH, kDE, 64, 128);
+       encode_2d(&h->tm_headW1, h->headW1, kDE, kNT * kHH, kDE, 64, 64);
   for (int l = 0; l < NL && ok; ++l)
     ok = encode_2d(&h->tm_qW[l], h->qX + (size_t)l * kG * kD * kXD, kXD, kG * kD, kXD, 64, 96);
   if (!ok) {
@@ -1161,7 +1184,6 @@ __global__ void selftest_wait_kernel(int* err, int* err_host) {
     const int e = atomicExch(err, 0);
     volatile int* hw = err_host;
     *hw = *hw | e;
-    __threadfence_system();
   }
 }
 }  // namespace
@@ -1181,14 +1203,15 @@ extern "C" cvr_status cvr_selftest_wait_timeout(cvr_handle* h) {
 }
 
 // ------------------------------------------------------------------------------------------
-// Prediction step without allocation: the PLE expert GEMM and the heads kernel on a caller's Token
-// Mixer output, their intermediates (expert outputs, gates) and the error word in one fixed
-// file-scope device array instead of the handle's growable workspace.
+// Prediction step without allocation: the PLE and prediction-head kernel on a caller's Token Mixer
+// output, its intermediates (expert outputs, gates) and the error word in one fixed file-scope device
+// array instead of the handle's growable workspace.
 namespace {
 
 constexpr int kNoAllocMaxCand = CVR_NOALLOC_MAX_CAND;
 constexpr size_t kNaGatesOff = (size_t)kNoAllocMaxCand * kPleN * 2;       // expert outputs, bf16 [n][768]
-constexpr size_t kNaErrOff = kNaGatesOff + (size_t)kNoAllocMaxCand * 8 * 4;  // gates, fp32 [n][8]
+constexpr size_t kNaROff = kNaGatesOff + (size_t)kNoAllocMaxCand * 8 * 4;    // gates, fp32 [n][8]
+constexpr size_t kNaErrOff = kNaROff + (size_t)2 * kNoAllocMaxCand * kDE * 2;  // r_t, bf16 [2][n][256]
 constexpr size_t kNaBytes = kNaErrOff + 512;                                 // error word (+0), CTA counter (+256)
 constexpr int kNaMaxDevices = 64;
 
@@ -1246,14 +1269,18 @@ cvr_status cvr_predict_noalloc(cvr_handle* h, int32_t n_cand, const void* y, flo
   a.attn_count = nullptr;
   a.Ex = reinterpret_cast<bf16*>(sc);
   a.gates = reinterpret_cast<float*>(sc + kNaGatesOff);
+  a.Rt = reinterpret_cast<bf16*>(sc + kNaROff);
+  a.ple_ready = nullptr;  // a caller's Y: the kernel waits for the preceding work in the stream instead
+
   a.err = reinterpret_cast<int*>(sc + kNaErrOff);
   a.done = reinterpret_cast<unsigned*>(sc + kNaErrOff + 256);
   cudaStream_t s = h->stream;
   ce = cudaMemsetAsync(sc + kNaErrOff, 0, 512, s);  // the error word and the CTA counter start at zero
-  CUtensorMap tmEx;
-  if (!encode_ex(&tmEx, a.Ex, (uint64_t)kNoAllocMaxCand)) return fail(h, CVR_E_CUDA, "cuTensorMapEncodeTiled failed for Ex");
-  if (ce == cudaSuccess) ce = launch_ple(a, tmY, h->tm_pleW, tmEx, s);
-  if (ce == cudaSuccess) ce = launch_heads(a, h->tm_headW1, s);
+  CUtensorMap tmR, tmEx;
+  if (!encode_2d(&tmR, a.Rt, kDE, (uint64_t)2 * kNoAllocMaxCand, kDE, 64, 128) ||
+      !encode_2d(&tmEx, a.Ex, kPleN, (uint64_t)kNoAllocMaxCand, kPleN, 64, 128))
+    return fail(h, CVR_E_CUDA, "cuTensorMapEncodeTiled failed for the prediction scratch");
+  if (ce == cudaSuccess) ce = launch_ple_heads(a, tmY, h->tm_pleW, tmR, tmEx, h->tm_headW1, kNoAllocMaxCand, s);
   if (ce != cudaSuccess) return cuda_fail(h, ce, "prediction kernels");
   return sync_status(h);
 }

@@ -33,7 +33,7 @@ constexpr int kDE = 256;          // expert width
 constexpr int kNT = 2;            // tasks
 constexpr int kHH = 128;          // head hidden width
 constexpr int kPleN = kNE * kDE;  // 768 expert columns
-constexpr int kPleCols = 832;     // + 2x3 gate logits, zero-padded to 4 tiles of 208
+constexpr int kPleCols = 832;     // packed PLE rows: 4 slices of [3 x 64 expert units, 6 gate logits, 10 zero rows]
 constexpr int kMaxLayers = 4;
 // cross-attention over long sequences: a CTA takes at most kChunksPerSplit chunks of 64 positions; a
 // group longer than that is split over up to kMaxSplits CTAs whose softmax states are merged
@@ -85,7 +85,7 @@ struct FwdArgs {
   __nv_bfloat16* I;       // [B][256]
   __nv_bfloat16* Xs;      // [sum_g R*L_g][128] sequence rows, group-major
   __nv_bfloat16* H;       // same layout: encoded sequence states
-  float* colsum;          // [R][G][max_chunks][128] partial column sums of H
+  float* colsum;          // [R][G][max_chunks][128] partial column sums of H (chunks of 512 positions)
   unsigned* cs_count;     // [R][G] blocks of the column-sum kernel done (zero between calls)
   const int32_t* seq_lens;  // [R][G] events each request really has per group, or null (all L[g])
   // partial softmax states of split sequences and the merge counters (zero between calls), laid out by the
@@ -99,13 +99,17 @@ struct FwdArgs {
   int q_add;               // 1: Q holds the first layer's queries without their mean-pooled sequence term, which
                            // the attention kernel adds (the tokeniser ran before the sequence side finished)
   int max_chunks;
-  float* xu;              // [R][1664] user half of the tokeniser (+ bias)
+  float* xu;              // [R][2048] user half of the tokeniser and of the folded first-layer queries (+ bias)
+  unsigned* xu_ready;     // [R/128][16] user row-tiles of xu written by the tokeniser launch (zeroed every call)
   float* qb;              // [layers][R][384] per-request query term (+ bias)
   __nv_bfloat16* Z;       // [B][2048] interaction-layer buffers (ping-pong with Y)
   __nv_bfloat16* Y;       // [B][2048]
   __nv_bfloat16* Q;       // [B][384]
   __nv_bfloat16* Ex;      // [B][768] expert outputs (after ReLU)
   float* gates;           // [B][8] task gate probabilities (2 x 3, padded)
+  __nv_bfloat16* Rt;      // [2][rows][256] gate-weighted expert sums r_t (task-major), the heads' A operand
+  unsigned* ple_ready;    // [B/128] per 128-row block: 8-candidate tiles the last Token Mixer has written, or null
+                          // (zeroed by the first kernel of each call; null: wait for the previous grid instead)
   int* err;               // device error word (bits below), reset by the last kernel of each call
   unsigned* done;         // CTA counter of the last kernel (finds the CTA that publishes the error word)
   int* err_host;          // device view of a pinned host word: the call's error bits are OR-ed into it
@@ -131,7 +135,7 @@ struct FwdArgs {
   const float* tm_b13;         // [layers][512]
   const float* tm_b2;          // [layers][128]
   const float* tm_gain;        // [layers][128]
-  const float* ple_b;          // [832 + 32]
+  const float* ple_b;          // [4][208]: biases of the PLE slices (3 x 64 expert units, 6 gates, zeros)
   const float* head_b1;        // [2][128]
   const float* head_w2;        // [2][128]
   const float* head_b2;        // [2]
@@ -359,6 +363,24 @@ __device__ __forceinline__ void ldg32(const float* p, float* v) {
   }
 }
 
+// 32 consecutive fp32 values through L2 (data written earlier in the same launch by another CTA)
+__device__ __forceinline__ void ldcg32(const float* p, float* v) {
+  const float4* q = reinterpret_cast<const float4*>(p);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 x = __ldcg(q + i);
+    v[4 * i] = x.x;
+    v[4 * i + 1] = x.y;
+    v[4 * i + 2] = x.z;
+    v[4 * i + 3] = x.w;
+  }
+}
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -426,22 +448,26 @@ cudaError_t prepare_attention_tc_kernel();
 cudaError_t launch_sparse(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_seq_colsum(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_seq_mlp(const FwdArgs& a, const CUtensorMap& tmXs, const CUtensorMap& tmW13,
-                           const CUtensorMap& tmW2, int n_tiles, bool with_xu, cudaStream_t s);
-// the user half of the tokeniser alone (otherwise extra CTAs of the sequence-encoder launch)
-cudaError_t launch_xu(const FwdArgs& a, bool pdl, cudaStream_t s);
+                           const CUtensorMap& tmW2, int n_tiles, cudaStream_t s);
 cudaError_t launch_tm_mlp(const FwdArgs& a, int layer, const __nv_bfloat16* zin, __nv_bfloat16* yout,
                           const CUtensorMap& tmZ, const CUtensorMap& tmW13, const CUtensorMap& tmW2, cudaStream_t s);
-// the tokeniser GEMM (13 tokens + the first layer's queries, 2048 packed columns) on at most max_grid CTAs
-// (0: one per SM)
+// the tokeniser GEMM (13 tokens + the first layer's queries, 2048 packed columns; its first M-tiles compute the
+// user half xu from U = tmU with the user weights tmWu) on at most max_grid CTAs (0: one per SM); pdl = false
+// launches it after the previous work in the stream has completed (the first kernel of the side stream)
 cudaError_t launch_tokenizer(const FwdArgs& a, const CUtensorMap& tmI, const CUtensorMap& tmW, const CUtensorMap& tmZo,
-                             const CUtensorMap& tmQo, int max_grid, cudaStream_t s);
+                             const CUtensorMap& tmQo, const CUtensorMap& tmU, const CUtensorMap& tmWu, int max_grid,
+                             bool pdl, cudaStream_t s);
 cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, const CUtensorMap& tmW, cudaStream_t s);
 cudaError_t launch_attention(const FwdArgs& a, __nv_bfloat16* zin, cudaStream_t s);
 cudaError_t launch_attention_tc(const FwdArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmH, __nv_bfloat16* zin,
                                 cudaStream_t s);
-cudaError_t launch_ple(const FwdArgs& a, const CUtensorMap& tmY, const CUtensorMap& tmW, const CUtensorMap& tmEx,
-                       cudaStream_t s);
-cudaError_t launch_heads(const FwdArgs& a, const CUtensorMap& tmW1, cudaStream_t s);
+cudaError_t prepare_ple_kernel();
+// PLE experts, gates and r_t (four CTAs per 128-row block), then the heads of each block in its last CTA;
+// tmW = packed PLE slices [832][2048], tmR = R viewed as [2 * r_rows][256], tmEx = expert outputs [rows][768],
+// tmW1 = head first layers [2 * 128][256] (boxes of 64 x 64; the others 64 x 128; all 128-byte swizzle); launched as
+// clusters of four CTAs
+cudaError_t launch_ple_heads(const FwdArgs& a, const CUtensorMap& tmY, const CUtensorMap& tmW, const CUtensorMap& tmR,
+                             const CUtensorMap& tmEx, const CUtensorMap& tmW1, int r_rows, cudaStream_t s);
 // hot-row cache admission after a call: rows that missed replace their slot's row unless that row was read
 // in the same call; claims [kNTab] are the per-table election arrays (zero between calls)
 cudaError_t launch_cache_admit(const FwdArgs& a, unsigned* const* claims, cudaStream_t s);

@@ -19,7 +19,6 @@
 // chunk keep the single issuing thread ahead of the tensor pipe.
 // TMEM: up 256, down 128, hidden 64, mixed activations 64 columns.
 #include "cvr_internal.cuh"
-#include "request_gemv.cuh"
 
 namespace cvr {
 
@@ -84,11 +83,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmW13, const __grid_constant__ CUtensorMap tmW2, int layer,
                       int n_tiles, int n_cta, const __nv_bfloat16* __restrict__ zin, __nv_bfloat16* __restrict__ yout) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  if (MODE == MODE_SEQ && (int)blockIdx.x >= n_cta) {  // CTAs past the encoder tiles: the user-side GEMV
-    pdl_trigger();
-    xu_block(a, (int)blockIdx.x - n_cta, smem);
-    return;
-  }
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) atomicOr(a.err, kErrLayout);
     return;
@@ -111,6 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dn_empty = bar + 9;        // epilogue has read it
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + kNBar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  unsigned* ydone = tslot + 2;  // TM: epilogue-warp parts of tiles written (16 per tile)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -125,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dn_full, 1);
     mbar_init(dn_empty, kEpiWarps);
     *abort_flag = 0;
+    *ydone = 0u;
     fence_mbar_init();
     if (MODE == MODE_SEQ) tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmW13);
@@ -172,6 +168,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (!waited) pdl_wait();
+    if (MODE == MODE_TM && lane == 0 && a.ple_ready && layer == a.n_layers - 1) {
+      // publish each tile once its 16 epilogue warps have written it: count it for its 128-row block, which the
+      // PLE starts when all of the block's tiles are in (bounded wait, as every wait here)
+      for (int i = 0; i < n_my; ++i) {
+        const unsigned need = (unsigned)(kEpiWarps * (i + 1));
+        const uint64_t t0 = global_timer_ns();
+        bool ok = true;
+        while (*reinterpret_cast<volatile unsigned*>(ydone) < need) {
+          if (*abort_flag || global_timer_ns() - t0 > 1000000000ull) {
+            ok = false;
+            break;
+          }
+          __nanosleep(32);
+        }
+        if (!ok) break;
+        __threadfence();
+        atomicAdd(a.ple_ready + (blockIdx.x + i * n_cta) / 16, 1u);  // tile = 8 candidates, block = 16 tiles
+      }
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the schedule and waits (it stays converged); lane 0 issues the MMAs and commits.
@@ -436,6 +451,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (live) *reinterpret_cast<uint4*>(yout + bcand * kYD + (grp * 4 + tt) * kD + j * 8) = p;
       }
+      if (MODE == MODE_TM) {
+        // this warp's part of the tile is written: count it in shared memory (the producer warp publishes whole
+        // tiles to the PLE, so no epilogue warp waits on a device-scope fence)
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          atomicAdd(ydone, 1u);
+        }
+      }
       return true;
     };
     if (MODE == MODE_TM && n_my > 0) {
@@ -477,14 +501,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// The user half of the tokeniser as a kernel of its own (when it runs on the side stream next to the encoder)
-__global__ void __launch_bounds__(kXuThreads) xu_kernel(const __grid_constant__ FwdArgs a) {
-  extern __shared__ uint8_t xu_smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(xu_smem_raw) + 15) & ~uintptr_t(15));
-  pdl_trigger();
-  xu_block(a, (int)blockIdx.x, smem);
-}
-
 }  // namespace
 
 cudaError_t prepare_mlp_kernels() {
@@ -495,16 +511,11 @@ cudaError_t prepare_mlp_kernels() {
 }
 
 cudaError_t launch_seq_mlp(const FwdArgs& a, const CUtensorMap& tmXs, const CUtensorMap& tmW13, const CUtensorMap& tmW2,
-                           int n_tiles, bool with_xu, cudaStream_t s) {
+                           int n_tiles, cudaStream_t s) {
   const int grid = n_tiles < a.num_sms ? n_tiles : a.num_sms;
-  static_assert(kXuSmemBytes <= kSmemBytes && kXuThreads <= kThreads, "the user-side GEMV fits the CTA");
-  return launch_kernel(swiglu_mlp_kernel<MODE_SEQ>, dim3(grid + (with_xu ? kXuBlocks : 0)), dim3(kThreads), kSmemBytes,
+  return launch_kernel(swiglu_mlp_kernel<MODE_SEQ>, dim3(grid), dim3(kThreads), kSmemBytes,
                        s, a.pdl != 0, a, tmXs, tmW13, tmW2, 0, n_tiles, grid, (const __nv_bfloat16*)nullptr,
                        (__nv_bfloat16*)nullptr);
-}
-
-cudaError_t launch_xu(const FwdArgs& a, bool pdl, cudaStream_t s) {
-  return launch_kernel(xu_kernel, dim3(kXuBlocks), dim3(kXuThreads), kXuSmemBytes + 16, s, pdl, a);
 }
 
 cudaError_t launch_tm_mlp(const FwdArgs& a, int layer, const __nv_bfloat16* zin, __nv_bfloat16* yout,

@@ -92,6 +92,16 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
   }
   pdl_trigger();
   pdl_wait();
+  // the per-row-block counters that start the PLE block by block begin every call at zero
+  if (a.ple_ready) {
+    const int nrb = (a.B + 127) / 128;
+    for (int i = blockIdx.x * kSparseThreads + tid; i < nrb; i += gridDim.x * kSparseThreads) {
+      a.ple_ready[i] = 0u;
+    }
+  }
+  if (a.xu_ready)  // and so do the tokeniser's user row-tile flags
+    for (int i = blockIdx.x * kSparseThreads + tid; i < (a.R + 127) / 128 * (kTokN / 128); i += gridDim.x * kSparseThreads)
+      a.xu_ready[i] = 0u;
   // request ids: in range and non-decreasing (checked once per candidate), and copied to the workspace for
   // the later kernels (the caller's array may be host memory read over the C2C link)
   for (int64_t cand = (int64_t)blockIdx.x * kSparseThreads + tid; cand < a.B;
@@ -369,18 +379,21 @@ __global__ void __launch_bounds__(256) cache_fill_kernel(const __grid_constant__
   }
 }
 
-// Partial column sums of H over chunks of 64 positions; grid (max_chunks, G, R), 128 threads. The last
-// block of each (request, group) to finish -- found with a counter, nobody waits -- adds the partials up into
-// the mean-pooled sequence vector m_g (iQIYI 3.2.3, Query Decoding item 1: mean over positions of the encoded
-// states) and computes that group's per-request query term for every layer,
-// qb[l][r][g*128 + n] = q_b[l][g*128 + n] + sum_k Wq[l][g][n][1664 + k] * m_g[k], then resets the counter.
-__global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__ FwdArgs a) {
+// Column sums of H over chunks of kCsRows positions; grid (chunks, G, R), 256 threads. A (request, group) that
+// fits one chunk (every one at the usual lengths) is summed by one block, which goes on directly; longer
+// sequences write one partial sum per chunk and the last of their blocks -- found with a counter, nobody waits --
+// adds the partials up in chunk order. That block then forms the mean-pooled sequence vector m_g (iQIYI 3.2.3,
+// Query Decoding item 1: mean over positions of the encoded states) and that group's per-request query term
+// for every layer, qb[l][r][g*128 + n] = q_b[l][g*128 + n] + sum_k Wq[l][g][n][1664 + k] * m_g[k].
+constexpr int kCsRows = 512;
+constexpr int kCsThreads = 256;
+
+__global__ void __launch_bounds__(kCsThreads) seq_colsum_kernel(const __grid_constant__ FwdArgs a) {
   const int chunk = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
   const int L = a.L[g];
   const int t = threadIdx.x;
-  // the mean-pool weight rows of this group (every layer) go to L2 while the encoder still runs; only the
-  // last block of a (request, group) reads them
-  if (chunk == 0 && r == 0)
+  // the mean-pool weight rows of this group (every layer) go to L2 while the encoder still runs
+  if (chunk == 0 && r == 0 && t < kD)
     for (int l = 0; l < a.n_layers; ++l) {
       const uint8_t* wrow = reinterpret_cast<const uint8_t*>(a.qm + (((int64_t)l * kG + g) * kD + t) * kD);
       asm volatile("prefetch.global.L2 [%0];" ::"l"(wrow));
@@ -391,75 +404,83 @@ __global__ void __launch_bounds__(128) seq_colsum_kernel(const __grid_constant__
   // positions that count: the request's real events (all L without variable lengths); an empty group still
   // has one block, which writes a zero mean
   const int len = seq_len_of(a, r, g);
-  const int chunks = len > 0 ? (len + 63) / 64 : 1;
+  const int chunks = len > 0 ? (len + kCsRows - 1) / kCsRows : 1;
   if (chunk >= chunks) return;
   const __nv_bfloat16* base = a.H + (a.goff[g] + (int64_t)r * L) * kD;
-  const int l_end = min(len, chunk * 64 + 64);
-  // thread t sums columns [8 (t % 16), +8) over rows chunk*64 + t/16 + 8i, i = 0..7: eight 16-byte loads in
-  // flight, then the eight row groups are added in a fixed order (the result does not depend on timing)
+  const int l0 = chunk * kCsRows, l_end = min(len, l0 + kCsRows);
+  // thread t sums columns [8 (t % 16), +8) over rows l0 + t/16 + 16 i, eight 16-byte loads in flight, in a fixed
+  // order (the result does not depend on timing)
   const int cg = t & 15, rg = t >> 4;
-  uint4 v[8];
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int lb = l0 + rg; lb < l_end; lb += 16 * 8) {
+    uint4 v[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int l = chunk * 64 + rg + 8 * i;
-    v[i] = l < l_end ? __ldg(reinterpret_cast<const uint4*>(base + (int64_t)l * kD) + cg) : make_uint4(0, 0, 0, 0);
-  }
-  float sacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int i = 0; i < 8; ++i) {
+      const int l = lb + 16 * i;
+      v[i] = l < l_end ? __ldg(reinterpret_cast<const uint4*>(base + (int64_t)l * kD) + cg) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+    for (int i = 0; i < 8; ++i) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      sacc[2 * e] += __low2float(h[e]);
-      sacc[2 * e + 1] += __high2float(h[e]);
+      for (int e = 0; e < 4; ++e) {
+        acc[2 * e] += __low2float(h[e]);
+        acc[2 * e + 1] += __high2float(h[e]);
+      }
     }
   }
-  __shared__ float part[8][kD];
+  __shared__ float part[16][kD];
   __shared__ float m[kD];
+  __shared__ float gpart[2][kD];
   __shared__ int last;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) part[rg][cg * 8 + e] = sacc[e];
+  for (int e = 0; e < 8; ++e) part[rg][cg * 8 + e] = acc[e];
   __syncthreads();
   float colsum = 0.f;
+  if (t < kD) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) colsum += part[j][t];
-  float* rgp = a.colsum + ((int64_t)r * kG + g) * a.max_chunks * kD;
-  rgp[chunk * kD + t] = colsum;
-  __threadfence();
-  __syncthreads();
-  unsigned* cnt = a.cs_count + r * kG + g;
-  if (t == 0) last = atomicAdd(cnt, 1u) == (unsigned)(chunks - 1);
-  __syncthreads();
-  if (!last) return;
-  float sum = 0.f;
-  for (int c0 = 0; c0 < chunks; c0 += 8) {  // eight loads in flight, summed in chunk order
-    float cv[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) cv[c] = c0 + c < chunks ? __ldcg(rgp + (c0 + c) * kD + t) : 0.f;
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-      if (c0 + c < chunks) sum += cv[c];
+    for (int j = 0; j < 16; ++j) colsum += part[j][t];
   }
-  m[t] = len > 0 ? sum / (float)len : 0.f;
-  if (t == 0) *cnt = 0u;
+  unsigned* cnt = a.cs_count + r * kG + g;
+  if (chunks > 1) {
+    float* rgp = a.colsum + ((int64_t)r * kG + g) * a.max_chunks * kD;
+    if (t < kD) rgp[chunk * kD + t] = colsum;
+    __threadfence();
+    __syncthreads();
+    if (t == 0) last = atomicAdd(cnt, 1u) == (unsigned)(chunks - 1);
+    __syncthreads();
+    if (!last) return;
+    if (t < kD) {
+      colsum = 0.f;
+      for (int c = 0; c < chunks; ++c) colsum += __ldcg(rgp + c * kD + t);  // in chunk order
+    }
+    if (t == 0) *cnt = 0u;
+  }
+  if (t < kD) m[t] = len > 0 ? colsum / (float)len : 0.f;
   __syncthreads();
+  // thread t: output row n = t % 128, half of K = t / 128; the two halves are added in a fixed order
+  const int nrow = t & (kD - 1), half = t >> 7;
   for (int l = 0; l < a.n_layers; ++l) {
-    uint4 wv[16];
-    const uint4* wrow = reinterpret_cast<const uint4*>(a.qm + (((int64_t)l * kG + g) * kD + t) * kD);
+    uint4 wv[8];
+    const uint4* wrow = reinterpret_cast<const uint4*>(a.qm + (((int64_t)l * kG + g) * kD + nrow) * kD + half * 64);
 #pragma unroll
-    for (int x = 0; x < 16; ++x) wv[x] = __ldg(wrow + x);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int x = 0; x < 8; ++x) wv[x] = __ldg(wrow + x);
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int x = 0; x < 16; ++x) {
+    for (int x = 0; x < 8; ++x) {
       const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&wv[x]);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        acc[q] += __low2float(e[q]) * m[x * 8 + 2 * q];
-        acc[q] += __high2float(e[q]) * m[x * 8 + 2 * q + 1];
+        s4[q] += __low2float(e[q]) * m[half * 64 + x * 8 + 2 * q];
+        s4[q] += __high2float(e[q]) * m[half * 64 + x * 8 + 2 * q + 1];
       }
     }
-    a.qb[((int64_t)l * a.R + r) * (kG * kD) + g * kD + t] =
-        __ldg(a.q_b + l * kG * kD + g * kD + t) + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+    gpart[half][nrow] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    __syncthreads();
+    if (t < kD)
+      a.qb[((int64_t)l * a.R + r) * (kG * kD) + g * kD + t] =
+          __ldg(a.q_b + l * kG * kD + g * kD + t) + (gpart[0][t] + gpart[1][t]);
+    __syncthreads();
   }
 }
 
@@ -480,7 +501,7 @@ cudaError_t launch_cache_admit(const FwdArgs& a, unsigned* const* claims, cudaSt
 }
 
 cudaError_t launch_seq_colsum(const FwdArgs& a, cudaStream_t s) {
-  return launch_kernel(seq_colsum_kernel, dim3(a.max_chunks, kG, a.R), dim3(128), 0, s, a.pdl != 0, a);
+  return launch_kernel(seq_colsum_kernel, dim3(a.max_chunks, kG, a.R), dim3(kCsThreads), 0, s, a.pdl != 0, a);
 }
 
 
