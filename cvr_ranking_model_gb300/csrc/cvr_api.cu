@@ -108,7 +108,7 @@ struct cvr_handle {
   size_t stage_bytes = 0;
   // tensor maps
   CUtensorMap tm_seqW13, tm_seqW2, tm_tokI, tm_tokU, tm_qW[kMaxLayers], tm_tmW13, tm_tmW2, tm_pleW, tm_headW1;
-  CUtensorMap tm_Xs, tm_I, tm_U, tm_x_Z, tm_x_Y, tm_5_Z, tm_5_Y, tm_full_Z, tm_full_Y, tm_Q, tm_H, tm_R, tm_Ex;
+  CUtensorMap tm_Xs, tm_I, tm_U, tm_x_Z, tm_x_Y, tm_full_Z, tm_full_Y, tm_Q, tm_H, tm_R, tm_Ex;
   // graphs, profiling
   bool use_graph = true, profile = false, pdl = true;
   bool attn_tc = false;  // cross-attention on the tcgen05 kernel instead of the register-tile one
@@ -154,22 +154,6 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Token-mix view of Z[nb][16][128] (bf16): dims (inner -> outer) e(8), j%8(8), t(16), j/8(2), b(nb).
-// One box {8,8,16,2,8} lands in shared memory as [b][j/8][t][j%8][e]: for mixed row (b, j) and K index
-// 8t+e, 8x16-byte core matrices of 8 consecutive mixed rows, 128 B apart along K and 2048 B apart
-// between 8-row groups -- the no-swizzle K-major operand layout of tcgen05.
-bool encode_mix5d(CUtensorMap* m, const void* base, uint64_t nb) {
-  EncodeTiledFn enc = get_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[5] = {8, 8, (cuuint64_t)kT, 2, nb};
-  cuuint64_t strides[4] = {16, (cuuint64_t)kD * 2, 128, (cuuint64_t)kYD * 2};
-  cuuint32_t box[5] = {8, 8, (cuuint32_t)kT, 2, 8};
-  cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 cvr_status check_config(const cvr_config* c, std::string* why) {
   auto bad = [&](const char* m) {
     *why = m;
@@ -212,19 +196,20 @@ struct Packer {
 };
 
 // Hidden chunk c (c = 0..3) of a SwiGLU occupies rows [128c, 128c+64) = W1 rows [64c, 64c+64) and rows
-// [128c+64, 128c+128) = W3 rows [64c, 64c+64): one N=128 MMA yields matching pre-activation columns.
+// [128c+64, 128c+128) = W3 rows [64c, 64c+64): one N=128 MMA yields matching pre-activation columns. W1 and b1
+// are stored halved (exact: a power of two), so the kernels get a / 2 for silu(a) = a/2 (1 + tanh(a/2)).
 void pack_w13(uint16_t* dst, const float* w1, const float* w3, int din) {
   for (int c = 0; c < 4; ++c)
     for (int i = 0; i < 64; ++i)
       for (int k = 0; k < din; ++k) {
-        dst[(size_t)(c * 128 + i) * din + k] = f32_to_bf16_bits(w1[(size_t)(c * 64 + i) * din + k]);
+        dst[(size_t)(c * 128 + i) * din + k] = f32_to_bf16_bits(0.5f * bf16_round(w1[(size_t)(c * 64 + i) * din + k]));
         dst[(size_t)(c * 128 + 64 + i) * din + k] = f32_to_bf16_bits(w3[(size_t)(c * 64 + i) * din + k]);
       }
 }
 void pack_b13(float* dst, const float* b1, const float* b3) {
   for (int c = 0; c < 4; ++c)
     for (int i = 0; i < 64; ++i) {
-      dst[c * 128 + i] = b1[c * 64 + i];
+      dst[c * 128 + i] = 0.5f * b1[c * 64 + i];
       dst[c * 128 + 64 + i] = b3[c * 64 + i];
     }
 }
@@ -326,8 +311,8 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
             encode_2d(&h->tm_I, h->I, kID, B_cap, kID, 64, 128) &&
             encode_2d(&h->tm_U, h->U, kUD, R_pad, kUD, 64, 128) &&
             encode_2d(&h->tm_x_Z, h->Z, kXD, B_cap, kYD, 64, 128) &&
-            encode_2d(&h->tm_x_Y, h->Y, kXD, B_cap, kYD, 64, 128) && encode_mix5d(&h->tm_5_Z, h->Z, B_cap) &&
-            encode_mix5d(&h->tm_5_Y, h->Y, B_cap) && encode_2d(&h->tm_full_Z, h->Z, kYD, B_cap, kYD, 64, 128) &&
+            encode_2d(&h->tm_x_Y, h->Y, kXD, B_cap, kYD, 64, 128) &&
+            encode_2d(&h->tm_full_Z, h->Z, kYD, B_cap, kYD, 64, 128) &&
             encode_2d(&h->tm_full_Y, h->Y, kYD, B_cap, kYD, 64, 128) &&
             encode_2d(&h->tm_Q, h->Q, kG * kD, B_cap, kG * kD, 64, 128) &&
             encode_2d(&h->tm_H, h->H, kD, (uint64_t)seq_rows, kD, 64, 64) &&
@@ -538,7 +523,7 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
     al.q_add = l == 0 ? af.q_add : 0;
     if (l == 0 && fork) al.pdl = 0;  // (after the join: see the column sums above)
     run(h->attn_tc ? launch_attention_tc(al, h->tm_Q, h->tm_H, zin, s) : launch_attention(al, zin, s), kStageNames[5]);
-    run(launch_tm_mlp(a, l, zin, zout, in_is_Z ? h->tm_5_Z : h->tm_5_Y, h->tm_tmW13, h->tm_tmW2, s), kStageNames[6]);
+    run(launch_tm_mlp(a, l, zin, zout, h->tm_tmW13, h->tm_tmW2, s), kStageNames[6]);
   }
   run(launch_ple_heads(a, zout == h->Z ? h->tm_full_Z : h->tm_full_Y, h->tm_pleW, h->tm_R, h->tm_Ex, h->tm_headW1,
                        h->B_cap, s),

@@ -404,16 +404,18 @@ __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
-// silu(a) * g for two pairs at once: silu(a) = a * (0.5 + 0.5 tanh(a / 2)), one tanh.approx per value;
-// returns the two products packed as bf16x2 (round to nearest even)
-__device__ __forceinline__ uint32_t silu_mul_bf16x2(uint64_t a, uint64_t g) {
-  const uint64_t half = f2pack(0.5f, 0.5f);
-  const uint64_t h = mul_f32x2(a, half);
+// silu(a) * g for two pairs at once, given h = a / 2 (the first SwiGLU weights and bias are stored halved):
+// silu(a) g = a sigmoid(a) g = h g (1 + tanh(h)). Both tanh values come from one tanh.approx.f16x2 (the multi-
+// function unit, the epilogues' narrowest pipe, then does one op per pair); its half-precision error is below the
+// bf16 rounding of the result. Returns bf16x2 (round to nearest even).
+__device__ __forceinline__ uint32_t silu_half_mul_bf16x2(uint64_t h, uint64_t g) {
+  uint32_t hh, th;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hh) : "f"(__uint_as_float((uint32_t)(h >> 32))), "f"(__uint_as_float((uint32_t)h)));
+  asm("tanh.approx.f16x2 %0, %1;" : "=r"(th) : "r"(hh));
   float t0, t1;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t0) : "f"(__uint_as_float((uint32_t)h)));
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t1) : "f"(__uint_as_float((uint32_t)(h >> 32))));
-  const uint64_t sg = fma_f32x2(f2pack(t0, t1), half, half);
-  const uint64_t r = mul_f32x2(mul_f32x2(a, sg), g);
+  asm("{\n .reg .f16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.f32.f16 %0, lo;\n cvt.f32.f16 %1, hi;\n}" : "=f"(t0), "=f"(t1) : "r"(th));
+  const uint64_t hg = mul_f32x2(h, g);
+  const uint64_t r = fma_f32x2(hg, f2pack(t0, t1), hg);
   return pack_bf16(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
 }
 // byte offset of 16-byte chunk `c` of row `r` inside a 128B-swizzled K-major tile (rows of 128 B)
@@ -449,8 +451,9 @@ cudaError_t launch_sparse(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_seq_colsum(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_seq_mlp(const FwdArgs& a, const CUtensorMap& tmXs, const CUtensorMap& tmW13,
                            const CUtensorMap& tmW2, int n_tiles, cudaStream_t s);
+// the Token Mixer of layer `layer`: zin [B][16][128] -> yout
 cudaError_t launch_tm_mlp(const FwdArgs& a, int layer, const __nv_bfloat16* zin, __nv_bfloat16* yout,
-                          const CUtensorMap& tmZ, const CUtensorMap& tmW13, const CUtensorMap& tmW2, cudaStream_t s);
+                          const CUtensorMap& tmW13, const CUtensorMap& tmW2, cudaStream_t s);
 // the tokeniser GEMM (13 tokens + the first layer's queries, 2048 packed columns; its first M-tiles compute the
 // user half xu from U = tmU with the user weights tmWu) on at most max_grid CTAs (0: one per SM); pdl = false
 // launches it after the previous work in the stream has completed (the first kernel of the side stream)

@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         f2pack(bav.x, bav.y));
           const uint64_t gv = add_f32x2(f2pack(__uint_as_float(rg[2 * e]), __uint_as_float(rg[2 * e + 1])),
                                         f2pack(bgv.x, bgv.y));
-          hp[8 * hh + e] = silu_mul_bf16x2(av, gv);
+          hp[8 * hh + e] = silu_half_mul_bf16x2(av, gv);
         }
       }
       if (cc >= 1 && !mbar_wait(hm_empty, (cc - 1) & 1, abort_flag, a.err)) return false;
@@ -519,11 +519,13 @@ cudaError_t launch_seq_mlp(const FwdArgs& a, const CUtensorMap& tmXs, const CUte
 }
 
 cudaError_t launch_tm_mlp(const FwdArgs& a, int layer, const __nv_bfloat16* zin, __nv_bfloat16* yout,
-                          const CUtensorMap& tmZ, const CUtensorMap& tmW13, const CUtensorMap& tmW2, cudaStream_t s) {
+                          const CUtensorMap& tmW13, const CUtensorMap& tmW2, cudaStream_t s) {
   const int n_tiles = (a.B + 7) / 8;  // 8 candidates x 16 mixed rows per tile
   const int grid = n_tiles < a.num_sms ? n_tiles : a.num_sms;
-  return launch_kernel(swiglu_mlp_kernel<MODE_TM>, dim3(grid), dim3(kThreads), kSmemBytes, s, a.pdl != 0, a, tmZ, tmW13,
-                       tmW2, layer, n_tiles, grid, zin, yout);
+  // (the activation operand of the Token Mixer is written into TMEM by its epilogue warps: the first tensor map is
+  // not used)
+  return launch_kernel(swiglu_mlp_kernel<MODE_TM>, dim3(grid), dim3(kThreads), kSmemBytes, s, a.pdl != 0, a, tmW13,
+                       tmW13, tmW2, layer, n_tiles, grid, zin, yout);
 }
 
 }  // namespace cvr
