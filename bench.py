@@ -300,6 +300,59 @@ def gather_roofline(dev: str, stream, flush, peak_bw: float, n_steps: int = 50):
             "timing": f"median of {n_steps} launches, events after each kernel, L2 flushed before each step"}
 
 
+def run_timeline(args):
+    """Per-CTA timeline of one synchronous call (L2 flushed, the GPU idle before it) from the diagnostic build with
+    per-CTA timestamps (cvr_timeline): for every kernel, when its CTAs started, when their wait for the previous
+    kernel's data returned and when they finished, in microseconds from the first CTA of the call. Median of 5 calls
+    per figure. Prints a table, not a benchmark line."""
+    os.environ["CVR_TIMELINE"] = "1"
+    import torch
+
+    import cvr_ranking_model_gb300._build as cvr_build
+    cvr_build.LIB = cvr_build.LIB_TIMELINE
+    cvr_build.build(timeline=True)
+    import cvr_ranking_model_gb300 as cvr
+    import synth
+    from synth.harness import DeviceWorkload, make_scorer
+    wl = synth.make_workload(args.config, n_cand=args.n_cand)
+    w = synth.make_weights(wl.n_layers, synth.default_seed(args.config))
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        dw = DeviceWorkload(wl)
+    torch.cuda.synchronize()
+    sc = make_scorer(dw, w, stream=stream.cuda_stream)
+    r, b, o, s, out = dw.ptrs()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    reps = []
+    with torch.cuda.stream(stream):
+        for rep in range(5 + args.warmup):
+            flush.zero_()
+            torch.cuda.synchronize()
+            sc.timeline(clear=True)
+            sc.score(wl.n_req, wl.n_cand, r, b, o, s, out)
+            if rep >= args.warmup:
+                reps.append(sc.timeline(clear=False).astype(np.int64))
+    rows = {}
+    for t in reps:
+        t0 = t[:, :, 0][t[:, :, 0] > 0].min()
+        for k, name in enumerate(cvr.binding.TIMELINE_KERNELS):
+            e = t[k]
+            m = e[:, 0] > 0
+            if not m.any():
+                continue
+            st, en = (e[m, 0] - t0) / 1e3, (e[m, 2] - t0) / 1e3
+            wd = (e[m, 1][e[m, 1] > 0] - t0) / 1e3
+            rows.setdefault(name, []).append((int(m.sum()), st.min(), np.median(st), st.max(),
+                                               np.median(wd) if len(wd) else float("nan"), np.median(en), en.max()))
+    print(f"timeline of one {args.config} call (us from the first CTA; median of {len(reps)} calls)")
+    print(f"{'kernel':13s} {'CTAs':>5s} {'start min':>9s} {'start med':>9s} {'start max':>9s} {'wait med':>9s} "
+          f"{'end med':>9s} {'end max':>9s}")
+    for name, lst in sorted(rows.items(), key=lambda kv: np.median([x[1] for x in kv[1]])):
+        v = np.median(np.array(lst), axis=0)
+        print(f"{name:13s} {int(v[0]):5d} " + " ".join(f"{x:9.2f}" for x in v[1:]))
+    sc.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -311,6 +364,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-gather", action="store_true", help="skip the embedding-gather roofline on deep C=2048")
+    ap.add_argument("--timeline", action="store_true",
+                    help="print the per-CTA timeline of one call (diagnostic build with per-CTA timestamps), no bench line")
     ap.add_argument("--minimal", action="store_true",
                     help="warm-up and timed steps only (for profiler captures): no clock soak, latency loops, "
                          "per-kernel region, end-to-end leg, gather roofline or CPU baseline")
@@ -322,6 +377,9 @@ def main():
         args.no_cpu_baseline = args.no_e2e = args.no_gather = True
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.timeline:
+        run_timeline(args)
         return
 
     import torch

@@ -18,6 +18,9 @@ MAX_LAYERS, N_USER_FIELDS, N_ITEM_FIELDS, N_GROUPS, N_EXPERTS, N_TASKS = 4, 8, 8
 STAGE_H, STAGE_Z, STAGE_Q, STAGE_Y, STAGE_EXPERTS, STAGE_GATES = range(6)
 OPT_PROFILE, OPT_CUDA_GRAPH, OPT_PDL, OPT_ATTENTION_TC = 0, 1, 2, 3
 NOALLOC_MAX_CAND = 1024  # CVR_NOALLOC_MAX_CAND
+TIMELINE_RECORDS = 10 * 8192 * 3  # CVR_TIMELINE_RECORDS
+TIMELINE_KERNELS = ["sparse", "seq_mlp", "seq_colsum", "tokenizer", "query", "attention", "token_mixer", "ple_heads",
+                    "attention_tc"]
 
 STATUS = {0: "CVR_OK", 1: "CVR_E_ARG", 2: "CVR_E_SHAPE", 3: "CVR_E_ID_RANGE", 4: "CVR_E_OOM", 5: "CVR_E_CUDA",
           6: "CVR_E_INPUT", 7: "CVR_E_TIMEOUT"}
@@ -58,7 +61,7 @@ def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
         if not os.path.exists(_build.LIB):
-            _build.build()
+            _build.build(timeline=_build.LIB == _build.LIB_TIMELINE)
         L = ctypes.CDLL(_build.LIB)
         V, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
         L.cvr_create.argtypes = [V, V, V, ctypes.POINTER(V)]
@@ -92,6 +95,8 @@ def lib() -> ctypes.CDLL:
         L.cvr_score_varlen_async.restype = ctypes.c_int
         L.cvr_selftest_wait_timeout.argtypes = [V]
         L.cvr_selftest_wait_timeout.restype = ctypes.c_int
+        L.cvr_timeline.argtypes = [V, V, i64, i32]
+        L.cvr_timeline.restype = ctypes.c_int
         L.cvr_predict_noalloc.argtypes = [V, i32, V, V]
         L.cvr_predict_noalloc.restype = ctypes.c_int
         L.cvr_cache_enable.argtypes = [V, i32, i64]
@@ -226,6 +231,13 @@ class Scorer:
     def selftest_wait_timeout(self) -> int:
         """cvr_selftest_wait_timeout: a wait that nothing ends; returns the status (7 = CVR_E_TIMEOUT)."""
         return int(self._lib.cvr_selftest_wait_timeout(self._h))
+
+    def timeline(self, clear: bool = True) -> np.ndarray:
+        """cvr_timeline: uint64 [10 kernels][8192 CTAs][3] (entry, dependency wait returned, exit; ns, 0 = none)
+        of a library built with -DCVR_TIMELINE."""
+        rec = np.zeros(TIMELINE_RECORDS, dtype=np.uint64)
+        self._check(self._lib.cvr_timeline(self._h, rec.ctypes.data, rec.size, int(clear)))
+        return rec.reshape(10, 8192, 3)
 
     def predict_noalloc(self, n_cand: int, y: int, out: int, check: bool = True) -> int:
         """cvr_predict_noalloc: PLE + heads on a device bf16 [n_cand][16][128] Token Mixer output, with

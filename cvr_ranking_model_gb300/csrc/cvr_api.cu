@@ -1149,6 +1149,38 @@ void cvr_destroy(cvr_handle* h) {
 }  // extern "C"
 
 // ------------------------------------------------------------------------------------------
+// Per-CTA timeline of the forward-pass kernels (a diagnostic of builds with -DCVR_TIMELINE).
+#ifdef CVR_TIMELINE
+namespace cvr {
+__device__ unsigned long long g_timeline[kTlKernels * kTlCtas * 3];
+}
+#endif
+
+extern "C" cvr_status cvr_timeline(cvr_handle* h, uint64_t* records, int64_t n_records, int32_t clear) {
+  if (!h) return CVR_E_ARG;
+#ifdef CVR_TIMELINE
+  const int64_t total = (int64_t)kTlKernels * kTlCtas * 3;
+  if (records && n_records != total)
+    return fail(h, CVR_E_SHAPE, "cvr_timeline: records must hold " + std::to_string(total) + " values");
+  cudaError_t ce = cudaStreamSynchronize(h->stream);
+  if (ce == cudaSuccess && records) ce = cudaMemcpyFromSymbol(records, cvr::g_timeline, total * 8);
+  if (ce == cudaSuccess && clear) {
+    void* addr = nullptr;
+    ce = cudaGetSymbolAddress(&addr, cvr::g_timeline);
+    if (ce == cudaSuccess) ce = cudaMemset(addr, 0, total * 8);
+    if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
+  }
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "cvr_timeline");
+  return CVR_OK;
+#else
+  (void)records;
+  (void)n_records;
+  (void)clear;
+  return fail(h, CVR_E_ARG, "cvr_timeline: this library was built without -DCVR_TIMELINE");
+#endif
+}
+
+// ------------------------------------------------------------------------------------------
 // Self-test of the bounded waits: one CTA waits on an mbarrier that nothing arrives at, with the same wait
 // the tensor-core kernels use; after its ~1 s limit the wait gives up, raises the timeout bit and the kernel
 // publishes it like the last kernel of a call does. Nothing faults, traps or hangs.

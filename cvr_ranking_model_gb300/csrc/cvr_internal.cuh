@@ -142,6 +142,41 @@ struct FwdArgs {
 };
 
 // ------------------------------------------------------------------------------------------
+// Per-CTA timeline (builds with -DCVR_TIMELINE only; a diagnostic, off in the normal build): the first thread of every
+// CTA of the forward-pass kernels records %globaltimer at entry, when its dependency wait returned and at exit, in
+// g_timeline[kernel id][CTA][3]; cvr_timeline copies the last call's records out.
+constexpr int kTlKernels = 10, kTlCtas = 8192;
+enum { TL_SPARSE = 0, TL_SEQ_MLP = 1, TL_COLSUM = 2, TL_TOKENIZER = 3, TL_QUERY = 4, TL_ATTENTION = 5,
+       TL_TOKEN_MIXER = 6, TL_PLE_HEADS = 7, TL_ATTENTION_TC = 8 };
+#ifdef CVR_TIMELINE
+extern __device__ unsigned long long g_timeline[kTlKernels * kTlCtas * 3];
+struct TimelineCta {
+  unsigned slot;
+  __device__ explicit TimelineCta(int kernel) {
+    const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    slot = cta < (unsigned)kTlCtas ? ((unsigned)kernel * kTlCtas + cta) * 3 : 0xffffffffu;
+    if (threadIdx.x == 0 && slot != 0xffffffffu) g_timeline[slot] = stamp();
+  }
+  __device__ void waited() const {
+    if (slot != 0xffffffffu) g_timeline[slot + 1] = stamp();
+  }
+  __device__ ~TimelineCta() {
+    if (threadIdx.x == 0 && slot != 0xffffffffu) g_timeline[slot + 2] = stamp();
+  }
+  __device__ static unsigned long long stamp() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+  }
+};
+#define CVR_TL_BEGIN(kernel) const TimelineCta cvr_tl_(kernel)
+#define CVR_TL_WAITED() cvr_tl_.waited()
+#else
+#define CVR_TL_BEGIN(kernel) ((void)0)
+#define CVR_TL_WAITED() ((void)0)
+#endif
+
+// ------------------------------------------------------------------------------------------
 // inline PTX
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -53,6 +53,7 @@ __device__ __forceinline__ float ex2(float x) {
 __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_constant__ FwdArgs a,
                                                                 __nv_bfloat16* __restrict__ zin) {
   extern __shared__ __align__(16) uint8_t smem[];
+  CVR_TL_BEGIN(TL_ATTENTION);
   const int g = a.g_order[blockIdx.y], sp = blockIdx.z;
   const int b0 = blockIdx.x * kCandPerCta;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
   pdl_trigger();
   if (sp >= n_split) return;
   pdl_wait();
+  if (threadIdx.x == 0) CVR_TL_WAITED();
   const int b_last = min(b0 + kCandPerCta, B) - 1;
   // request ids are validated by the sparse kernel; here they are only kept in range
   const int r_first = min(max(a.req_ids[b0], 0), R - 1);

@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_tc_kernel(const __grid_
                                                                    const __grid_constant__ CUtensorMap tmH,
                                                                    __nv_bfloat16* __restrict__ zin) {
   extern __shared__ uint8_t smem_raw[];
+  CVR_TL_BEGIN(TL_ATTENTION_TC);
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + kOffQ;
   uint8_t* sKV = smem + kOffKV;
@@ -175,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_tc_kernel(const __grid_
   tc_fence_after();
   const uint32_t tbase = *tslot;
   pdl_wait();
+  if (threadIdx.x == 0) CVR_TL_WAITED();
 
   const int B = a.B, R = a.R;
   const int b_last = min(b0 + kRows, B) - 1;

@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
                 const __grid_constant__ CUtensorMap tmQo, const __grid_constant__ CUtensorMap tmU,
                 const __grid_constant__ CUtensorMap tmWu, int M, int N, int K, int layer, int mu) {
   extern __shared__ uint8_t smem_raw[];
+  CVR_TL_BEGIN(EPI == EPI_TOKENIZE ? TL_TOKENIZER : TL_QUERY);
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int B_TILE = BN * kBK * 2;
   constexpr uint32_t TC = tmem_cols<BN>();
@@ -93,6 +94,7 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
   const uint32_t tbase = *tslot;
   pdl_trigger();
   pdl_wait();
+  if (threadIdx.x == 0) CVR_TL_WAITED();
 
   if (warp == 0) {
     if (lane == 0) {

@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmW13, const __grid_constant__ CUtensorMap tmW2, int layer,
                       int n_tiles, int n_cta, const __nv_bfloat16* __restrict__ zin, __nv_bfloat16* __restrict__ yout) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  CVR_TL_BEGIN(MODE == MODE_SEQ ? TL_SEQ_MLP : TL_TOKEN_MIXER);
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) atomicOr(a.err, kErrLayout);
     return;
@@ -291,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     pdl_wait();
+    if (threadIdx.x == 64) CVR_TL_WAITED();
     // TM: this thread's 4 pieces Z[b][t][8j..8j+8) (tokens t = 4 grp.. of its column quarter), written into
     // TMEM lane (b, j) at columns 4t.., form the mixed activation row (b, j) (K slot t holds head j of token t)
     // that the up projection reads as its A operand; the same TMEM columns later give the residual back.

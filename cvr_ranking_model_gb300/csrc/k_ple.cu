@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmR,
                const __grid_constant__ CUtensorMap tmEx, const __grid_constant__ CUtensorMap tmW1, int r_rows) {
   extern __shared__ uint8_t smem_raw[];
+  CVR_TL_BEGIN(TL_PLE_HEADS);
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* sbias = reinterpret_cast<float*>(smem + kOffBias);  // [208]
   float* sb1 = sbias + kBN;                                  // [64]
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (a.ple_ready) {
         wait_count(a.ple_ready + rb, (unsigned)((min(kBM, a.B - m0) + 7) / 8), a.err);
         asm volatile("fence.proxy.async.global;" ::: "memory");  // the rows are read by TMA (async proxy)
+        CVR_TL_WAITED();
       } else {
         pdl_wait();
       }

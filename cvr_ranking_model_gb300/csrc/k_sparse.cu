@@ -77,6 +77,7 @@ __device__ __forceinline__ float4 ld_row(const float* p, int part, bool coherent
 // kCache: some table has a hot-row cache (a separate instantiation keeps the plain path's registers as they are)
 template <bool kCache>
 __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_kernel(const __grid_constant__ FwdArgs a) {
+  CVR_TL_BEGIN(TL_SPARSE);
   const int tid = threadIdx.x, lane = tid & 31;
   const int64_t gw = (int64_t)blockIdx.x * (kSparseThreads / 32) + (tid >> 5);
   const int64_t nw = (int64_t)gridDim.x * (kSparseThreads / 32);
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
   }
   pdl_trigger();
   pdl_wait();
+  if (tid == 0) CVR_TL_WAITED();
   // the per-row-block counters that start the PLE block by block begin every call at zero
   if (a.ple_ready) {
     const int nrb = (a.B + 127) / 128;
@@ -389,6 +391,7 @@ constexpr int kCsRows = 512;
 constexpr int kCsThreads = 256;
 
 __global__ void __launch_bounds__(kCsThreads) seq_colsum_kernel(const __grid_constant__ FwdArgs a) {
+  CVR_TL_BEGIN(TL_COLSUM);
   const int chunk = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
   const int L = a.L[g];
   const int t = threadIdx.x;
@@ -401,6 +404,7 @@ __global__ void __launch_bounds__(kCsThreads) seq_colsum_kernel(const __grid_con
     }
   pdl_trigger();
   pdl_wait();
+  if (t == 0) CVR_TL_WAITED();
   // positions that count: the request's real events (all L without variable lengths); an empty group still
   // has one block, which writes a zero mean
   const int len = seq_len_of(a, r, g);

@@ -210,6 +210,16 @@ int32_t cvr_last_launch_count(const cvr_handle* h);
 const char* cvr_last_error(const cvr_handle* h);
 const char* cvr_status_string(cvr_status s);
 
+/* Diagnostic (the pages have no counterpart): the per-CTA timeline of the forward-pass kernels, in builds compiled with
+ * -DCVR_TIMELINE (otherwise CVR_E_ARG). The first thread of every CTA records the device clock (%globaltimer, ns) at
+ * entry, when its wait for the previous kernel's data returned, and at exit: records [10 kernels][8192 CTAs][3]
+ * (HOST uint64; 0 = not recorded; kernels in the order sparse, seq_mlp, seq_colsum, tokenizer, query, attention,
+ * token_mixer, ple_heads, attention_tc; CTA = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z), CTAs
+ * past 8192 not recorded; a stacked layer's launch overwrites the previous layer's). Waits for the handle's stream,
+ * copies out when records is not NULL (n_records must be 245760), then clears every record when clear != 0. */
+#define CVR_TIMELINE_RECORDS (10 * 8192 * 3)
+cvr_status cvr_timeline(cvr_handle* h, uint64_t* records, int64_t n_records, int32_t clear);
+
 /* Diagnostic (the pages have no counterpart): launches one CTA that waits on a barrier nothing arrives at,
  * through the same bounded wait as the scoring kernels, and returns what a call would report when a wait
  * gives up: CVR_E_TIMEOUT after about 1 s, the handle staying usable. Shows that a stuck wait ends as a
