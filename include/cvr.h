@@ -121,7 +121,7 @@ cvr_status cvr_create(const cvr_weights* weights, const cvr_config* cfg, void* c
  *   seq_ids     [n_req][sum(seq_len)][4] int64 rows of the shared sequence table; per request the
  *               events of group 0, then group 1, then group 2.
  *   out         [n_cand][2] fp32 pCVR per task, written by the call (caller-owned).
- * Sizes: 1 <= n_req <= n_cand <= 2^20. Workspace grows on demand (first call at a size allocates).
+ * Sizes: 1 <= n_req <= 65535, 1 <= n_cand <= 2^20. Workspace grows on demand (first call at a size allocates).
  * Returns CVR_E_SHAPE on sizes out of range, CVR_E_ID_RANGE / CVR_E_INPUT on bad ids, offsets or
  * request ids (detected on the device, never read out of bounds), CVR_E_CUDA on CUDA errors.
  * When the sequence encoder leaves SMs free, part of a call runs on a second stream owned by the handle; it
@@ -226,12 +226,13 @@ cvr_status cvr_timeline(cvr_handle* h, uint64_t* records, int64_t n_records, int
  * status instead of a hung GPU. */
 cvr_status cvr_selftest_wait_timeout(cvr_handle* h);
 
-/* The prediction step alone -- PLE experts and gates, task towers and sigmoid -- on a caller's Token Mixer
+/* The prediction step alone -- PLE experts and gates, task towers and sigmoid (one kernel) -- on a caller's Token Mixer
  * output, without allocating device memory. The papers have no counterpart: it serves callers that
  * cannot allocate mid-flight (a serving loop whose device memory is all pre-reserved by its own pool, or
  * one that cannot afford the device-wide synchronisation of cudaMalloc / cudaFree that a growing
  * cvr_score workspace would cost). Its intermediates (expert outputs, gates, error word) live in one
- * fixed device array of CVR_NOALLOC_MAX_CAND x 1,568 + 512 bytes (1.6 MB) inside this library.
+ * fixed device array of CVR_NOALLOC_MAX_CAND x 2,592 + 512 bytes (2.5 MB) inside this library (expert outputs,
+ * gates and the gate-weighted expert sums of every candidate).
  *   y    DEVICE bf16 [n_cand][16][128]: the last Token Mixer's output (the layout of CVR_STAGE_Y), 16-byte
  *        aligned; read only.
  *   out  DEVICE fp32 [n_cand][2]: pCVR per task, written by the call (caller-owned).
