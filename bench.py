@@ -369,6 +369,8 @@ def main():
     ap.add_argument("--minimal", action="store_true",
                     help="warm-up and timed steps only (for profiler captures): no clock soak, latency loops, "
                          "per-kernel region, end-to-end leg, gather roofline or CPU baseline")
+    ap.add_argument("--ple-int8", action="store_true",
+                    help="time the PLE on 8-bit weights (CVR_OPT_PLE_INT8) in the headline region as well")
     ap.add_argument("--varlen", action="store_true",
                     help="variable-length sequences: every request's length per group uniform in [1, L_g]")
     args = ap.parse_args()
@@ -405,6 +407,7 @@ def main():
     torch.cuda.synchronize(dev)
     sc = make_scorer(dw, w, stream=stream.cuda_stream)
     sc.set_option(cvr.OPT_CUDA_GRAPH, 1)
+    sc.set_option(cvr.OPT_PLE_INT8, int(args.ple_int8))
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     r, b, o, s, out = dw.ptrs()
     B = wl.n_cand
@@ -581,6 +584,20 @@ def main():
                "d2h_bytes_per_step": int(h_out.nbytes), "p50_ms": statistics.median(e_ms),
                "api": "cvr_score_host (pinned host buffers, read and written in place by the kernels)"}
 
+    # the same steps with the PLE on 8-bit weights (the option the accuracy gate admits): batch time and the
+    # PLE + heads kernel's own time
+    int8 = None
+    if not (args.minimal or args.varlen or args.ple_int8):
+        sc.set_option(cvr.OPT_PLE_INT8, 1)
+        i8_ms, _, _ = timed_region(profile=False, n_steps=min(args.steps, 1000))
+        _, i8_stages, _ = timed_region(profile=True, n_steps=200)
+        sc.set_option(cvr.OPT_PLE_INT8, 0)
+        i8_tot = max_over_ranks(sum(i8_ms), dev)
+        int8 = {"value": job_throughput(world, B, len(i8_ms), i8_tot), "unit": UNIT,
+                "p50_ms": statistics.median(i8_ms),
+                "ple_heads_ms": sum(i8_stages.get("ple_heads", [float("nan")])) / 200,
+                "what": "CVR_OPT_PLE_INT8: PLE expert and gate weights int8 with a scale per row, bf16 activations"}
+
     gather = None
     if rank == 0 and not args.no_gather and not args.varlen:
         gather = gather_roofline(dev, stream, flush, peak_bw)
@@ -593,7 +610,7 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "bf16 (PLE weights int8)" if args.ple_int8 else "bf16", "data": "synthetic",
             "config": {"workload": f"{args.config}: R={wl.n_req} requests x C={B // wl.n_req} candidates, "
                                    f"L={Lstr}, {wl.n_layers} interaction layer(s), tables {wl.user_rows}/"
                                    f"{wl.item_rows}/{wl.seq_rows} rows x 32 fp32, bags 1-8, Zipf({wl.zipf_s})",
@@ -612,7 +629,7 @@ def main():
             "profiled_p50_ms": statistics.median(prof_ms),
             "roofline": roofline, "sparse_roofline": sparse, "gather_roofline": gather, "path_roofline": path,
             "stage_ms": {k: round(v, 5) for k, v in per_kernel.items()},
-            "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks.summary(),
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks.summary(), "ple_int8": int8,
             "gpu_launches": launches,
         }
         print(json.dumps(line))

@@ -80,6 +80,9 @@ struct cvr_handle {
   // packed weights
   void* wblob = nullptr;
   size_t wblob_bytes = 0;
+  void* w8blob = nullptr;    // PLE expert and gate rows as int8 [4 x 208][2048], then their fp32 scales [4 x 208]
+  float* ple_s8 = nullptr;
+  bool ple_int8 = false;     // the PLE runs on the 8-bit rows
   bf16 *tokI = nullptr, *tokU = nullptr, *seqW13 = nullptr, *seqW2 = nullptr, *qX = nullptr, *qm = nullptr;
   bf16 *tmW13 = nullptr, *tmW2 = nullptr, *pleW = nullptr, *headW1 = nullptr;
   float *tok_b = nullptr, *seq_b13 = nullptr, *seq_b2 = nullptr, *q_b = nullptr, *tm_b13 = nullptr, *tm_b2 = nullptr;
@@ -107,7 +110,7 @@ struct cvr_handle {
   void* stage = nullptr;
   size_t stage_bytes = 0;
   // tensor maps
-  CUtensorMap tm_seqW13, tm_seqW2, tm_tokI, tm_tokU, tm_qW[kMaxLayers], tm_tmW13, tm_tmW2, tm_pleW, tm_headW1;
+  CUtensorMap tm_seqW13, tm_seqW2, tm_tokI, tm_tokU, tm_qW[kMaxLayers], tm_tmW13, tm_tmW2, tm_pleW, tm_pleW8, tm_headW1;
   CUtensorMap tm_Xs, tm_I, tm_U, tm_x_Z, tm_x_Y, tm_full_Z, tm_full_Y, tm_Q, tm_H, tm_R, tm_Ex;
   // graphs, profiling
   bool use_graph = true, profile = false, pdl = true;
@@ -151,6 +154,20 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 8-bit rows [outer][inner] bytes (row stride `row_stride` bytes), unswizzled boxes of box_inner x box_outer
+bool encode_2d_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride,
+                  uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -431,6 +448,7 @@ FwdArgs make_args(cvr_handle* h, int R, int B, const int32_t* req_ids, const int
   a.tm_b2 = h->tm_b2;
   a.tm_gain = h->tm_gain;
   a.ple_b = h->ple_b;
+  a.ple_s8 = h->ple_int8 ? h->ple_s8 : nullptr;
   a.head_b1 = h->head_b1;
   a.head_w2 = h->head_w2;
   a.head_b2 = h->head_b2;
@@ -525,8 +543,8 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
     run(h->attn_tc ? launch_attention_tc(al, h->tm_Q, h->tm_H, zin, s) : launch_attention(al, zin, s), kStageNames[5]);
     run(launch_tm_mlp(a, l, zin, zout, h->tm_tmW13, h->tm_tmW2, s), kStageNames[6]);
   }
-  run(launch_ple_heads(a, zout == h->Z ? h->tm_full_Z : h->tm_full_Y, h->tm_pleW, h->tm_R, h->tm_Ex, h->tm_headW1,
-                       h->B_cap, s),
+  run(launch_ple_heads(a, zout == h->Z ? h->tm_full_Z : h->tm_full_Y, h->ple_int8 ? h->tm_pleW8 : h->tm_pleW,
+                       h->tm_R, h->tm_Ex, h->tm_headW1, h->B_cap, s),
       kStageNames[7]);
   if (a.cache_on) {
     run(launch_cache_admit(a, h->c_claim, s), kStageNames[8]);
@@ -793,6 +811,7 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
     std::memcpy(F + f_tm_b2 + l * kD, w->tm_b2[l], sizeof(float) * kD);
     std::memcpy(F + f_gain + l * kD, w->tm_gain[l], sizeof(float) * kD);
   }
+  std::vector<uint8_t> W8((size_t)kPleCols * kYD + (size_t)kPleCols * 4);
   // PLE rows in 4 slices of 208, one per CTA of a row block's cluster: slice n = units [64n, 64n + 64) of
   // experts 0, 1, 2, then the 6 gate rows (task-major), then 10 zero rows; biases in the same order
   for (int n = 0; n < 4; ++n) {
@@ -811,6 +830,16 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
       }
       for (int c = 0; c < kYD; ++c) B[o_pleW + row * kYD + c] = src ? f32_to_bf16_bits(src[c]) : 0;
       F[f_ple_b + row] = bias;
+      // the same row in 8 bits: q = round-half-even(w / scale) with scale = max|w| / 127 (a zero row: q = 0, scale 0)
+      double amax = 0.0;
+      for (int c = 0; src && c < kYD; ++c) amax = std::max(amax, std::fabs((double)src[c]));
+      const double sc = amax / 127.0;
+      int8_t* q = reinterpret_cast<int8_t*>(W8.data()) + row * kYD;
+      for (int c = 0; c < kYD; ++c) {
+        const double v = sc > 0.0 ? std::nearbyint((double)src[c] / sc) : 0.0;
+        q[c] = (int8_t)std::min(127.0, std::max(-127.0, v));
+      }
+      reinterpret_cast<float*>(W8.data() + (size_t)kPleCols * kYD)[row] = (float)sc;
     }
   }
   for (int t = 0; t < kNT; ++t) {
@@ -830,6 +859,8 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
   uint8_t* wb = static_cast<uint8_t*>(h->wblob);
   e = cudaMemcpy(wb, P.bf.data(), bf_bytes, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(wb + bf_bytes, P.f32.data(), f_bytes, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMalloc(&h->w8blob, W8.size());
+  if (e == cudaSuccess) e = cudaMemcpy(h->w8blob, W8.data(), W8.size(), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&h->err_host), 64, cudaHostAllocMapped);
   if (e == cudaSuccess) {
     *h->err_host = 0;
@@ -864,6 +895,7 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
   h->tm_b2 = wf + f_tm_b2;
   h->tm_gain = wf + f_gain;
   h->ple_b = wf + f_ple_b;
+  h->ple_s8 = reinterpret_cast<float*>(static_cast<uint8_t*>(h->w8blob) + (size_t)kPleCols * kYD);
   h->head_b1 = wf + f_hb1;
   h->head_w2 = wf + f_hw2;
   h->head_b2 = wf + f_hb2;
@@ -874,6 +906,7 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
        encode_2d(&h->tm_tmW13, h->tmW13, kD, (uint64_t)NL * 512, kD, 64, 256) &&
        encode_2d(&h->tm_tmW2, h->tmW2, kHid, (uint64_t)NL * kD, kHid, 64, 128) &&
        encode_2d(&h->tm_pleW, h->pleW, kYD, kPleCols, kYD, 64, 208) &&
+       encode_2d_u8(&h->tm_pleW8, h->w8blob, kYD, kPleCols, kYD, 64, 208) &&
        encode_2d(&h->tm_headW1, h->headW1, kDE, kNT * kHH, kDE, 64, 64);
   for (int l = 0; l < NL && ok; ++l)
     ok = encode_2d(&h->tm_qW[l], h->qX + (size_t)l * kG * kD * kXD, kXD, kG * kD, kXD, 64, 96);
@@ -1042,9 +1075,10 @@ cvr_status cvr_set_option(cvr_handle* h, int32_t option, int64_t value) {
     h->use_graph = value != 0;
     return CVR_OK;
   }
-  if (option == CVR_OPT_PDL || option == CVR_OPT_ATTENTION_TC) {
+  if (option == CVR_OPT_PDL || option == CVR_OPT_ATTENTION_TC || option == CVR_OPT_PLE_INT8) {
     if (option == CVR_OPT_PDL) h->pdl = value != 0;
-    else h->attn_tc = value != 0;
+    else if (option == CVR_OPT_ATTENTION_TC) h->attn_tc = value != 0;
+    else h->ple_int8 = value != 0;
     drop_graphs(h);
     return CVR_OK;
   }
@@ -1137,6 +1171,7 @@ void cvr_destroy(cvr_handle* h) {
   if (h->cache_ctl) cudaFree(h->cache_ctl);
   if (h->stage) cudaFree(h->stage);
   if (h->wblob) cudaFree(h->wblob);
+  if (h->w8blob) cudaFree(h->w8blob);
   if (h->err_host) cudaFreeHost(h->err_host);
   for (auto ev : h->events) cudaEventDestroy(ev);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
@@ -1297,7 +1332,7 @@ cvr_status cvr_predict_noalloc(cvr_handle* h, int32_t n_cand, const void* y, flo
   if (!encode_2d(&tmR, a.Rt, kDE, (uint64_t)2 * kNoAllocMaxCand, kDE, 64, 128) ||
       !encode_2d(&tmEx, a.Ex, kPleN, (uint64_t)kNoAllocMaxCand, kPleN, 64, 128))
     return fail(h, CVR_E_CUDA, "cuTensorMapEncodeTiled failed for the prediction scratch");
-  if (ce == cudaSuccess) ce = launch_ple_heads(a, tmY, h->tm_pleW, tmR, tmEx, h->tm_headW1, kNoAllocMaxCand, s);
+  if (ce == cudaSuccess) ce = launch_ple_heads(a, tmY, h->ple_int8 ? h->tm_pleW8 : h->tm_pleW, tmR, tmEx, h->tm_headW1, kNoAllocMaxCand, s);
   if (ce != cudaSuccess) return cuda_fail(h, ce, "prediction kernels");
   return sync_status(h);
 }

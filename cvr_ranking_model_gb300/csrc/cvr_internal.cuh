@@ -136,6 +136,7 @@ struct FwdArgs {
   const float* tm_b2;          // [layers][128]
   const float* tm_gain;        // [layers][128]
   const float* ple_b;          // [4][208]: biases of the PLE slices (3 x 64 expert units, 6 gates, zeros)
+  const float* ple_s8;         // [4][208]: row scales of the 8-bit PLE weights, or null (bf16 weights)
   const float* head_b1;        // [2][128]
   const float* head_w2;        // [2][128]
   const float* head_b2;        // [2]

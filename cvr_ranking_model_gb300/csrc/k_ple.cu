@@ -18,6 +18,11 @@
 // The kernel starts per row block instead of waiting for the whole Token Mixer grid: a CTA waits (bounded)
 // until the Token Mixer has counted every tile of its row block as written, so the first blocks run on the SMs
 // the Token Mixer's last round leaves free. The counters are cleared by the first kernel of every call.
+// INT8 weights (ple_kernel<true>): the expert and gate rows are held as signed 8-bit integers q with one fp32
+// scale per row (W ~ scale . q, scale = max|W_row| / 127). The scale is constant along K, so it comes out of the
+// dot product: the ring brings in q, the epilogue warps turn each stage into exact bf16 integers in the
+// B operand's swizzled layout while the MMAs of earlier stages run, and the epilogue multiplies the fp32 sums by
+// the row scales before the bias. The ring has 4 stages in this mode (the 8-bit staging takes the fifth's room).
 #include "cvr_internal.cuh"
 
 namespace cvr {
@@ -28,34 +33,60 @@ constexpr int kSlice = 64;                  // units of each expert per CTA
 constexpr int kSlices = kDE / kSlice;       // 4 CTAs per 128-row block
 constexpr int kBN = kNE * kSlice + 16;      // 208 columns per CTA: 3 x 64 expert units + 16 gate columns
 constexpr int kGateCol = kNE * kSlice;      // 192: the 6 gate logits (task-major), then zero columns
-constexpr int kBM = 128, kBK = 64, kStages = 5;
+constexpr int kBM = 128, kBK = 64;
 constexpr int kATile = kBM * kBK * 2;       // 16 KB
 constexpr int kBTile = kBN * kBK * 2;       // 26 KB
+constexpr int kW8Tile = kBN * kBK;          // 13 KB: one stage of 8-bit weights (rows of 64 bytes, unswizzled)
 constexpr int kNK = kYD / kBK;              // 32 k-blocks
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + kEpiWarps * 32;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..9 epilogue
 constexpr int kTmemCols = 256;
-static_assert(kPleCols == kSlices * kBN, "four 208-column slices");
-
-// shared memory (offsets from a 1024-byte aligned base)
-constexpr int kOffA = 0;
-constexpr int kOffB = kStages * kATile;
-constexpr int kRingBytes = kStages * (kATile + kBTile);   // 210 KB
-// output staging, in the ring once the main loop is done: r_t slices [task] then expert slices [k], each
-// [128 rows][64 units] bf16 with the 128-byte swizzle (the layout of a TMA box of 64 x 128)
-constexpr int kOffStage = 0;
-static_assert((kNT + kNE) * kATile <= kRingBytes, "output staging fits the ring");
-// heads, in the ring as well: r_t (4 K-blocks of [128][64]) then this CTA's W1 rows (4 K-blocks of [64][64])
 constexpr int kHN = kHH / 2;                // hidden units per CTA
 constexpr int kHOffW = 4 * kATile;
 constexpr int kHBytes = 4 * kATile + 4 * kHN * kBK * 2;  // 96 KB
-static_assert(kHBytes <= kRingBytes, "head operands fit the ring");
-constexpr int kOffBias = kRingBytes;                      // fp32 slice bias [208], head b1 / w2 of this half [64] each
-constexpr int kOffPlog = kOffBias + (kBN + 2 * kHN) * 4;  // fp32 [2 halves][128 rows]: partial logits (task's first CTA)
-constexpr int kOffBar = kOffPlog + 2 * kBM * 4;
-constexpr int kNBar = 2 * kStages + 1 + 2;
-constexpr int kSmemBytes = kOffBar + kNBar * 8 + 16 + 1024;  // + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
+static_assert(kPleCols == kSlices * kBN, "four 208-column slices");
+
+// shared memory (offsets from a 1024-byte aligned base)
+template <bool I8>
+struct Smem {
+  static constexpr int kStages = I8 ? 4 : 5;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kStages * kATile;
+  static constexpr int kOffW8 = kOffB + kStages * kBTile;  // (8-bit weights only)
+  static constexpr int kRingBytes = kStages * (kATile + kBTile + (I8 ? kW8Tile : 0));
+  // output staging, in the ring once the main loop is done: r_t slices [task] then expert slices [k], each
+  // [128 rows][64 units] bf16 with the 128-byte swizzle (the layout of a TMA box of 64 x 128); the heads' operands
+  // (r_t as 4 K-blocks of [128][64], then this CTA's W1 rows as 4 K-blocks of [64][64]) go there as well
+  static constexpr int kOffStage = 0;
+  static constexpr int kOffBias = kRingBytes;                   // fp32 slice bias [208], head b1 / w2 of this half [64] each
+  static constexpr int kOffScale = kOffBias + (kBN + 2 * kHN) * 4;  // fp32 row scales of the slice [208] (8-bit weights)
+  static constexpr int kOffPlog = kOffScale + (I8 ? kBN * 4 : 0);   // fp32 [2 halves][128 rows]: partial logits
+  static constexpr int kOffBar = kOffPlog + 2 * kBM * 4;
+  // per stage: full, empty (and for 8-bit weights: converted, weights landed); then acc_full, h_full, head_full
+  static constexpr int kNBar = 4 * kStages + 3;
+  static constexpr int kBytes = kOffBar + kNBar * 8 + 16 + 1024;  // + alignment slack
+  static_assert((kNT + kNE) * kATile <= kRingBytes, "output staging fits the ring");
+  static_assert(kHBytes <= kRingBytes, "head operands fit the ring");
+  static_assert(kOffB % 1024 == 0 && kBTile % 1024 == 0 && kOffW8 % 1024 == 0, "stage alignment");
+  static_assert(kBytes <= 232448, "shared memory budget of one CTA");
+};
+
+// 16 signed bytes (K order) -> 16 bf16 holding the same integers (exact: |q| <= 128 needs 8 significant bits).
+// Each byte, biased to unsigned, becomes the low mantissa byte of the fp32 2^23 + u; subtracting 2^23 + 128 gives q.
+__device__ __forceinline__ void s8x16_to_bf16(const uint4 v, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float f0 = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7440u + 2 * h)) - 8388736.f;
+      const float f1 = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7441u + 2 * h)) - 8388736.f;
+      o[2 * i + h] = pack_bf16(f0, f1);
+    }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
 
 // address of the same shared-memory location in CTA `rank` of the cluster
 __device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
@@ -85,24 +116,30 @@ __device__ __forceinline__ void wait_count(const unsigned* cnt, unsigned need, i
   }
 }
 
+template <bool I8>
 __global__ void __launch_bounds__(kThreads, 1)
     ple_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap tmY,
                const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmR,
                const __grid_constant__ CUtensorMap tmEx, const __grid_constant__ CUtensorMap tmW1, int r_rows) {
+  using S = Smem<I8>;
+  constexpr int kStages = S::kStages;
   extern __shared__ uint8_t smem_raw[];
   CVR_TL_BEGIN(TL_PLE_HEADS);
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* sbias = reinterpret_cast<float*>(smem + kOffBias);  // [208]
+  float* sbias = reinterpret_cast<float*>(smem + S::kOffBias);  // [208]
   float* sb1 = sbias + kBN;                                  // [64]
   float* sw2 = sb1 + kHN;                                    // [64]
-  float* plog = reinterpret_cast<float*>(smem + kOffPlog);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  float* sscale = reinterpret_cast<float*>(smem + S::kOffScale);  // [208] (8-bit weights)
+  float* plog = reinterpret_cast<float*>(smem + S::kOffPlog);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
   uint64_t* full = bar;
   uint64_t* empty = bar + kStages;
   uint64_t* acc_full = bar + 2 * kStages;  // the main loop's accumulator is complete
   uint64_t* h_full = acc_full + 1;         // heads: r_t and the W1 rows landed
   uint64_t* head_full = acc_full + 2;      // heads: hidden pre-activations complete
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + kNBar);
+  uint64_t* conv = acc_full + 3;           // 8-bit weights: stage s turned into bf16 by the epilogue warps
+  uint64_t* wfull = conv + kStages;        // 8-bit weights: stage s's bytes landed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + S::kNBar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -110,7 +147,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rb = (int)blockIdx.x / kSlices;           // row block
   const int m0 = rb * kBM;
   const int ht = n >> 1, hh = n & 1;                  // head task and hidden half of this CTA
-  for (int k = threadIdx.x; k < kBN; k += blockDim.x) sbias[k] = __ldg(a.ple_b + n * kBN + k);  // (constants)
+  for (int k = threadIdx.x; k < kBN; k += blockDim.x) {  // (constants)
+    sbias[k] = __ldg(a.ple_b + n * kBN + k);
+    if constexpr (I8) sscale[k] = __ldg(a.ple_s8 + n * kBN + k);
+  }
   for (int k = threadIdx.x; k < kHN; k += blockDim.x) {
     sb1[k] = __ldg(a.head_b1 + ht * kHH + hh * kHN + k);
     sw2[k] = __ldg(a.head_w2 + ht * kHH + hh * kHN + k);
@@ -119,6 +159,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      if constexpr (I8) {
+        mbar_init(&conv[s], kEpiWarps);
+        mbar_init(&wfull[s], 1);
+      }
     }
     mbar_init(acc_full, 1);
     mbar_init(h_full, 1);
@@ -140,11 +184,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // weights first: they do not depend on the Token Mixer
+      // weights first: they do not depend on the Token Mixer. 8-bit weights land in the staging area on their own
+      // barrier, so that the epilogue warps convert the first stages while the activations are awaited.
+      constexpr int kWBytes = I8 ? kW8Tile : kBTile;
+      uint8_t* wdst = smem + (I8 ? S::kOffW8 : S::kOffB);
+      uint64_t* wbar = I8 ? wfull : full;
       const int pre = kStages < kNK ? kStages : kNK;
       for (int kb = 0; kb < pre; ++kb) {
-        mbar_expect_tx(&full[kb], kATile + kBTile);
-        tma_load_2d(smem + kOffB + kb * kBTile, &tmW, &full[kb], kb * kBK, n * kBN);
+        mbar_expect_tx(&full[kb], I8 ? kATile : kATile + kBTile);
+        if constexpr (I8) mbar_expect_tx(&wfull[kb], kW8Tile);
+        tma_load_2d(wdst + kb * kWBytes, &tmW, &wbar[kb], kb * kBK, n * kBN);
       }
       // then this row block's activations, once the Token Mixer has written every one of its 8-candidate tiles;
       // without the counters (a caller's Y) the previous work in the stream is waited for
@@ -159,10 +208,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = kb % kStages;
         if (kb >= kStages) {
           if (!mbar_wait(&empty[s], ((kb / kStages) & 1) ^ 1, abort_flag, a.err)) break;
-          mbar_expect_tx(&full[s], kATile + kBTile);
-          tma_load_2d(smem + kOffB + s * kBTile, &tmW, &full[s], kb * kBK, n * kBN);
+          mbar_expect_tx(&full[s], I8 ? kATile : kATile + kBTile);
+          if constexpr (I8) mbar_expect_tx(&wfull[s], kW8Tile);
+          tma_load_2d(wdst + s * kWBytes, &tmW, &wbar[s], kb * kBK, n * kBN);
         }
-        tma_load_2d(smem + kOffA + s * kATile, &tmY, &full[s], kb * kBK, m0);
+        tma_load_2d(smem + S::kOffA + s * kATile, &tmY, &full[s], kb * kBK, m0);
       }
     }
   } else if (warp == 1) {
@@ -171,12 +221,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int kb = 0; kb < kNK; ++kb) {
         const int s = kb % kStages;
-        if (!mbar_wait(&full[s], (kb / kStages) & 1, abort_flag, a.err)) {
+        if (!mbar_wait(&full[s], (kb / kStages) & 1, abort_flag, a.err) ||
+            (I8 && !mbar_wait(&conv[s], (kb / kStages) & 1, abort_flag, a.err))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t aa = smem_u32(smem + kOffA + s * kATile), bb = smem_u32(smem + kOffB + s * kBTile);
+        const uint32_t aa = smem_u32(smem + S::kOffA + s * kATile), bb = smem_u32(smem + S::kOffB + s * kBTile);
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k)
           tc_mma(tbase, sdesc_sw128(aa + k * 32), sdesc_sw128(bb + k * 32), idesc, (kb | k) != 0);
@@ -189,6 +240,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3, grp = (warp - 2) >> 2;  // TMEM lane quarter; units [32 grp, 32 grp + 32) of the slice
     const int rl = q * 32 + lane, row = m0 + rl;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    if constexpr (I8) {
+      // 8-bit weights: stage s's [208][64] bytes -> the bf16 B tile in the layout a 128-byte-swizzled TMA load
+      // would give (row r at 128 r, 16-byte chunk c at chunk c ^ (r % 8)); one 16-byte chunk of a row per step
+      const int ct = threadIdx.x - 64;
+      for (int kb = 0; kb < kNK; ++kb) {
+        const int s = kb % kStages;
+        if (!mbar_wait_warp(&wfull[s], (kb / kStages) & 1, abort_flag, a.err)) break;
+        const uint8_t* src = smem + S::kOffW8 + s * kW8Tile;
+        uint8_t* dst = smem + S::kOffB + s * kBTile;
+        for (int c = ct; c < kBN * 4; c += kEpiWarps * 32) {
+          const int r = c >> 2, kq = c & 3;
+          uint4 lo, hi;
+          s8x16_to_bf16(*reinterpret_cast<const uint4*>(src + r * 64 + kq * 16), lo, hi);
+          *reinterpret_cast<uint4*>(dst + sw128_offset(r, 2 * kq)) = lo;
+          *reinterpret_cast<uint4*>(dst + sw128_offset(r, 2 * kq + 1)) = hi;
+        }
+        fence_proxy_async_smem();  // the tile is read by the tensor cores (async proxy)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&conv[s]);
+      }
+    }
     const bool ok = mbar_wait_warp(acc_full, 0, abort_flag, a.err);
     if (ok) {
       tc_fence_after();
@@ -204,7 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float l[kNE], mx = -INFINITY;
 #pragma unroll
         for (int k = 0; k < kNE; ++k) {
-          l[k] = __uint_as_float(gl[t * kNE + k]) + sbias[kGateCol + t * kNE + k];
+          const int c = kGateCol + t * kNE + k;
+          l[k] = (I8 ? __uint_as_float(gl[t * kNE + k]) * sscale[c] : __uint_as_float(gl[t * kNE + k])) + sbias[c];
           mx = fmaxf(mx, l[k]);
         }
         float sum = 0.f;
@@ -221,9 +294,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k < kNE; ++k) {
         const float* bk = sbias + k * kSlice + grp * 32;
+        const float* sk = sscale + k * kSlice + grp * 32;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) e[k][j] = __float_as_uint(fmaxf(__uint_as_float(e[k][j]) + bk[j], 0.f));
-        uint8_t* rowp = smem + kOffStage + (kNT + k) * kATile + rl * 128;
+        for (int j = 0; j < 32; ++j) {
+          const float v = I8 ? fmaf(__uint_as_float(e[k][j]), sk[j], bk[j]) : __uint_as_float(e[k][j]) + bk[j];
+          e[k][j] = __float_as_uint(fmaxf(v, 0.f));
+        }
+        uint8_t* rowp = smem + S::kOffStage + (kNT + k) * kATile + rl * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           *reinterpret_cast<uint4*>(rowp + (((4 * grp + c) ^ (rl & 7)) << 4)) =
@@ -240,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // r_t for this thread's 32 units, staged as task t's slice
 #pragma unroll
       for (int t = 0; t < kNT; ++t) {
-        uint8_t* rowp = smem + kOffStage + t * kATile + rl * 128;
+        uint8_t* rowp = smem + S::kOffStage + t * kATile + rl * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t p[4];
@@ -265,10 +342,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 64) {
       if (ok) {
         // r_t slices first (the heads wait for them), the expert outputs in a second group
-        for (int t = 0; t < kNT; ++t) tma_store_2d(&tmR, smem + kOffStage + t * kATile, n * kSlice, t * r_rows + m0);
+        for (int t = 0; t < kNT; ++t) tma_store_2d(&tmR, smem + S::kOffStage + t * kATile, n * kSlice, t * r_rows + m0);
         bulk_commit();
         for (int k = 0; k < kNE; ++k)
-          tma_store_2d(&tmEx, smem + kOffStage + (kNT + k) * kATile, k * kDE + n * kSlice, m0);
+          tma_store_2d(&tmEx, smem + S::kOffStage + (kNT + k) * kATile, k * kDE + n * kSlice, m0);
         bulk_commit();
         asm volatile("cp.async.bulk.wait_group 1;" ::: "memory");  // the r_t slices are written
         bulk_wait_read<0>();  // and the staging area has been read (the head operands reuse it)
@@ -349,7 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t prepare_ple_kernel() {
-  return cudaFuncSetAttribute(ple_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(ple_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<false>::kBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(ple_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<true>::kBytes);
+  return e;
 }
 
 cudaError_t launch_ple_heads(const FwdArgs& a, const CUtensorMap& tmY, const CUtensorMap& tmW, const CUtensorMap& tmR,
@@ -358,7 +438,8 @@ cudaError_t launch_ple_heads(const FwdArgs& a, const CUtensorMap& tmY, const CUt
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(blocks * kSlices);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  const bool i8 = a.ple_s8 != nullptr;
+  cfg.dynamicSmemBytes = i8 ? Smem<true>::kBytes : Smem<false>::kBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;  // the four CTAs of a row block
@@ -369,7 +450,8 @@ cudaError_t launch_ple_heads(const FwdArgs& a, const CUtensorMap& tmY, const CUt
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, ple_kernel, a, tmY, tmW, tmR, tmEx, tmW1, r_rows);
+  return i8 ? cudaLaunchKernelEx(&cfg, ple_kernel<true>, a, tmY, tmW, tmR, tmEx, tmW1, r_rows)
+            : cudaLaunchKernelEx(&cfg, ple_kernel<false>, a, tmY, tmW, tmR, tmEx, tmW1, r_rows);
 }
 
 }  // namespace cvr

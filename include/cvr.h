@@ -195,8 +195,15 @@ cvr_status cvr_debug_stage(cvr_handle* h, int32_t stage, void* dst, int64_t byte
  *   CVR_OPT_CUDA_GRAPH   1 = replay the call's kernel sequence from a CUDA graph captured per (n_req, n_cand)
  *                            (default 1); 0 = launch eagerly
  *   CVR_OPT_PDL          1 = launch each kernel with programmatic dependent launch, so its prologue overlaps
- *                            the previous kernel (default 1); 0 = plain stream order */
-enum { CVR_OPT_PROFILE = 0, CVR_OPT_CUDA_GRAPH = 1, CVR_OPT_PDL = 2, CVR_OPT_ATTENTION_TC = 3 };
+ *                            the previous kernel (default 1); 0 = plain stream order
+ *   CVR_OPT_PLE_INT8     1 = the PLE expert and gate GEMM reads its weights as 8-bit integers with one fp32 scale
+ *                            per output row (scale = max|w| / 127, q = round-half-even(w / scale), made from the
+ *                            fp32 weights at creation); activations stay bf16 and the scale is applied to the
+ *                            fp32 sums, so the integers enter the tensor cores exactly. Outputs stay inside the
+ *                            pCVR tolerance of the fp64 model on the production and two-layer workloads but
+ *                            differ from the bf16 weights' (default 0: bf16 weights). Mixed-precision inference,
+ *                            iQIYI ad-CVR article, outlook section. */
+enum { CVR_OPT_PROFILE = 0, CVR_OPT_CUDA_GRAPH = 1, CVR_OPT_PDL = 2, CVR_OPT_ATTENTION_TC = 3, CVR_OPT_PLE_INT8 = 4 };
 cvr_status cvr_set_option(cvr_handle* h, int32_t option, int64_t value);
 
 /* With CVR_OPT_PROFILE set: per-kernel device times of the last call, in launch order. Writes up to
