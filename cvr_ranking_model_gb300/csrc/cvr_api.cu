@@ -1228,9 +1228,9 @@ __global__ void selftest_wait_kernel(int* err, int* err_host) {
     abort_flag = 0;
     fence_mbar_init();
   }
-  __syncthreads();
+  cta_sync();
   mbar_wait(&bar, 0, &abort_flag, err);
-  __syncthreads();
+  cta_sync();
   if (threadIdx.x == 0) {
     __threadfence();
     const int e = atomicExch(err, 0);

@@ -99,7 +99,7 @@ struct FwdArgs {
   int q_add;               // 1: Q holds the first layer's queries without their mean-pooled sequence term, which
                            // the attention kernel adds (the tokeniser ran before the sequence side finished)
   int max_chunks;
-  float* xu;              // [R][2048] user half of the tokeniser and of the folded first-layer queries (+ bias)
+  float* xu;              // [R][2048] user half of the tokeniser and of the folded first-layer queries (no bias)
   unsigned* xu_ready;     // [R/128][16] user row-tiles of xu written by the tokeniser launch (zeroed every call)
   float* qb;              // [layers][R][384] per-request query term (+ bias)
   __nv_bfloat16* Z;       // [B][2048] interaction-layer buffers (ping-pong with Y)
@@ -410,6 +410,18 @@ __device__ __forceinline__ void ldcg32(const float* p, float* v) {
     v[4 * i + 2] = x.z;
     v[4 * i + 3] = x.w;
   }
+}
+// CTA barrier taken by converged warps: bar.sync expects every lane of a warp to arrive together, and single
+// lanes of a warp (a producer or MMA-issuing thread, a thread that publishes a counter) often arrive after a
+// branch of their own
+__device__ __forceinline__ void cta_sync() {
+  __syncwarp();
+  __syncthreads();
+}
+// counter publication: a release at GPU scope (orders this thread's earlier writes, and by cumulativity those of
+// threads it synchronised with through a CTA barrier, before the increment)
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;

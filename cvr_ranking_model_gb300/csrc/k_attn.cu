@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
     for (int j = 0; j < 4; ++j)
 #pragma unroll
       for (int i = 0; i < 4; ++i) o[j][i] = 0.f;
-    __syncthreads();  // the previous request's chunks have been read by every warp
+    cta_sync();  // the previous request's chunks have been read by every warp
     if (c_begin < c_end) load_chunk(c_begin, 0);
     cp_async_commit();
     for (int ch = c_begin; ch < c_end; ++ch) {
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
       if (ch + 1 < c_end) load_chunk(ch + 1, slot ^ 1);
       cp_async_commit();
       cp_async_wait1();
-      __syncthreads();  // chunk ch has landed for every warp
+      cta_sync();  // chunk ch has landed for every warp
       const __nv_bfloat16* Ks = buf + slot * (kChunk * kKStride);
       float s[8][4];
 #pragma unroll
@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
           mma_bf16_16816(o[2 * ntp + 1], pa, vb[2], vb[3]);
         }
       }
-      __syncthreads();  // every warp is done with chunk ch before it is refilled
+      cta_sync();  // every warp is done with chunk ch before it is refilled
     }
   };
   // row sums over the 4 threads of a row, then the decoded token of head h for the rows of request r
@@ -258,9 +258,9 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
   for (int j = 0; j < 4; ++j) st[1 + j] = make_float4(o[j][0], o[j][1], o[j][2], o[j][3]);
   __shared__ int last;
   __threadfence();
-  __syncthreads();
+  cta_sync();
   if (tid == 0) last = atomicAdd(a.attn_count + slot, 1u) == (unsigned)(n_split - 1);
-  __syncthreads();
+  cta_sync();
   if (!last) return;
   // merge in split order: M = max m_s, l = sum l_s 2^(m_s - M), o = sum o_s 2^(m_s - M)
   float4 hd[kMaxSplits];

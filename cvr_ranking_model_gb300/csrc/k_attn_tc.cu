@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_tc_kernel(const __grid_
   }
   if (warp == 1) tmem_alloc(tslot, 512);
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tbase = *tslot;
   pdl_wait();
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_tc_kernel(const __grid_
       if (lane == 0) *cnt = 0u;  // ready for the next call
     }
   }
-  __syncthreads();
+  cta_sync();
   if (*abort_flag && !skip && lane == 0) {
     // a wait gave up: let this CTA's own loads and MMAs land before its shared memory and TMEM are released
     if (warp == 0) {
@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_tc_kernel(const __grid_
     }
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);

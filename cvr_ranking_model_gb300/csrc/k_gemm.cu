@@ -10,9 +10,13 @@
 //                    (Wq_x Wtok precomputed). The per-request terms are computed once per request (iQIYI
 //                    3.4.5): the user half xu = U . [Wtok_user ; Wq_x Wtok_user]^T + biases is the same GEMM
 //                    over the pooled user rows, run as the first M-tiles of the launch (fp32 out); the item
-//                    tiles' epilogues wait (bounded) for the xu tile of their requests and N-range, and the
+//                    tiles' addends wait (bounded) for the xu tile of their requests and N-range, and the
 //                    mean-pool term qb comes from the column-sum kernel
 //    EPI_QUERY       Q = bf16(flat(X) . Wq_x^T + qb[request]) for stacked layers (iQIYI 3.2.3, item 1)
+//
+// The per-request addends of a tile are fetched one tile ahead by a warp of their own into shared memory (the
+// request of each of the tile's rows, and the addend rows of up to kSlots consecutive requests), so the epilogue
+// warps find them there instead of paying the request-id, flag and addend loads in series on every tile.
 #include "cvr_internal.cuh"
 
 namespace cvr {
@@ -22,10 +26,13 @@ namespace {
 enum { EPI_TOKENIZE = 0, EPI_QUERY = 1 };
 constexpr int kBM = 128, kBK = 64;
 constexpr int kATile = kBM * kBK * 2;  // 16 KB
+constexpr int kSlots = 8;              // requests per tile whose addends are staged (others: loaded by the row)
 
-// named barrier of the NEPI epilogue warps (the producer and MMA warps never take part)
+// named barrier of the NEPI epilogue warps (the producer and MMA warps never take part); each warp arrives
+// converged, since single lanes of it may have taken a branch of their own just before
 template <int NEPI>
 __device__ __forceinline__ void epi_bar() {
+  __syncwarp();
   asm volatile("bar.sync 1, %0;" ::"n"(NEPI * 32) : "memory");
 }
 
@@ -33,18 +40,49 @@ template <int BN>
 __host__ __device__ constexpr uint32_t tmem_cols() {
   return BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
 }
+// one addend buffer: the request of each row [128] int32, then kSlots addend rows [BN] fp32
+template <int BN>
+__host__ __device__ constexpr int add_buf_bytes() {
+  return kBM * 4 + kSlots * BN * 4;
+}
 template <int BN, int STAGES, int EPI>
 __host__ __device__ constexpr int gemm_smem_bytes() {
   return 1024 + STAGES * (kATile + BN * kBK * 2) + 256 +
-         (EPI == EPI_TOKENIZE ? 1024 + 2 * kBM * BN * 2 : 0);  // + output staging (aligned): two swizzled tiles
+         (EPI == EPI_TOKENIZE ? 1024 + 2 * kBM * BN * 2 : 0) +  // + output staging (aligned): two swizzled tiles
+         2 * add_buf_bytes<BN>();                               // + two addend buffers
+}
+
+// v[0..32) += the addends of columns [nb, nb + 32) of a row of request `req`, read through L2: the tokeniser's
+// xu + bias (+ the mean-pool term qb for the first layer's query columns), or the query GEMM's qb of the layer
+template <int EPI>
+__device__ __forceinline__ void add_row_addends(const FwdArgs& a, int req, int nb, int layer, float* v) {
+  float t[32];
+  if (EPI == EPI_TOKENIZE) {
+    ldcg32(a.xu + (int64_t)req * kTokN + nb, t);  // (written in this launch)
+#pragma unroll
+    for (int x = 0; x < 32; ++x) v[x] += t[x];
+    ldg32(a.tok_b + nb, t);
+#pragma unroll
+    for (int x = 0; x < 32; ++x) v[x] += t[x];
+    if (nb >= kXD && !a.q_add) {
+      ldg32(a.qb + (int64_t)req * (kG * kD) + (nb - kXD), t);
+#pragma unroll
+      for (int x = 0; x < 32; ++x) v[x] += t[x];
+    }
+  } else {
+    ldg32(a.qb + ((int64_t)layer * a.R + req) * (kG * kD) + nb, t);
+#pragma unroll
+    for (int x = 0; x < 32; ++x) v[x] += t[x];
+  }
 }
 
 // Persistent GEMM: CTAs loop over 128 x BN output tiles (n fastest, so co-running CTAs share A rows in L2).
 // Warp 0 streams A/B k-blocks through a STAGES-deep ring; warp 1 issues the MMAs into one of two TMEM
 // accumulators; NEPI epilogue warps drain the other one, so a tile's epilogue overlaps the next tile's
-// MMAs. With 8 epilogue warps the two warpgroups split the 32-column chunks of a tile.
+// MMAs. With 8 epilogue warps the two warpgroups split the 32-column chunks of a tile. The last warp stages
+// the next row-tile's per-request addends in one of two shared-memory buffers.
 template <int BN, int STAGES, int EPI, int NEPI>
-__global__ void __launch_bounds__(64 + NEPI * 32, 1)
+__global__ void __launch_bounds__(96 + NEPI * 32, 1)
     gemm_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap tmA,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmZo,
                 const __grid_constant__ CUtensorMap tmQo, const __grid_constant__ CUtensorMap tmU,
@@ -56,17 +94,25 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
   constexpr uint32_t TC = tmem_cols<BN>();
   constexpr int NCHUNK = (BN + 31) / 32;
   constexpr int NGRP = NEPI / 4;
+  static_assert(BN <= 128, "one float4 of a tile row per lane of the addend warp");
+  // TMEM accumulators: the tokeniser holds four (512 columns), so that the MMAs of a CTA's item tiles run on while
+  // the epilogue waits for the user tile its first item tile needs; the query GEMM two
+  constexpr int NACC = EPI == EPI_TOKENIZE ? 4 : 2;
+  static_assert(NACC * TC <= 512, "accumulators fit tensor memory");
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * kATile;
   uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_TILE);
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;
-  uint64_t* acc_empty = acc_full + 2;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* acc_empty = acc_full + NACC;
+  uint64_t* add_full = acc_empty + NACC;  // addend buffer b staged
+  uint64_t* add_empty = add_full + 2;   // addend buffer b read by every epilogue warp
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(add_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   // output staging for TMA stores (1024-byte aligned): tokeniser, two tiles [128][BN] bf16 as boxes of [128 rows]
   // [64 columns] with the 128-byte swizzle
   uint8_t* sOut = reinterpret_cast<uint8_t*>(((reinterpret_cast<uintptr_t>(full) + 256) + 1023) & ~uintptr_t(1023));
+  uint8_t* sAdd = EPI == EPI_TOKENIZE ? sOut + 2 * kBM * BN * 2 : reinterpret_cast<uint8_t*>(full) + 256;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles_n = N / BN;
@@ -78,18 +124,22 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NACC; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], NEPI);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&add_full[i], 1);
+      mbar_init(&add_empty[i], NEPI);
     }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  if (warp == 1) tmem_alloc(tslot, 2 * TC);
+  if (warp == 1) tmem_alloc(tslot, NACC * TC);
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tbase = *tslot;
   pdl_trigger();
@@ -122,8 +172,8 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
       int kc = 0, i = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++i) {
-        const int buf = i & 1;
-        if (i >= 2 && !mbar_wait(&acc_empty[buf], ((i >> 1) & 1) ^ 1, abort_flag, a.err)) break;
+        const int buf = i % NACC;
+        if (i >= NACC && !mbar_wait(&acc_empty[buf], ((i / NACC) & 1) ^ 1, abort_flag, a.err)) break;
         const uint32_t dacc = tbase + buf * TC;
         for (int kb = 0; kb < nk; ++kb, ++kc) {
           const int s = kc % STAGES;
@@ -141,55 +191,139 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
         if (ok) tc_commit(&acc_full[buf]);
       }
     }
+  } else if (warp == 2 + NEPI) {
+    // ---- addends of the row-tiles, ahead of the epilogue: the request of every row, then for the tile's first
+    // kSlots requests (rows are sorted by request) the addend row xu (+ qb for the first layer's query columns), or
+    // qb of the layer; the tokeniser waits (bounded) for the user tile that writes xu. Each step is one round trip
+    // to memory: the next tile's request ids are loaded while this tile's addends are, and a flag seen set is
+    // remembered.
+    auto next_item = [&](int t) {
+      while (t < n_tiles && EPI == EPI_TOKENIZE && t / tiles_n < mu) t += gridDim.x;
+      return t;
+    };
+    int rq[kBM / 32];  // request ids of this lane's rows of the next tile
+    auto load_req = [&](int t) {
+      const int m0 = (t / tiles_n - mu) * kBM;
+#pragma unroll
+      for (int k = 0; k < kBM / 32; ++k) {
+        const int row = m0 + lane + 32 * k;
+        rq[k] = row < M ? a.req_ids[row] : 0;
+      }
+    };
+    int tile = next_item(blockIdx.x), j = 0, flag_seen = -1;
+    if (tile < n_tiles) load_req(tile);
+    while (tile < n_tiles) {
+      const int mt = tile / tiles_n, nt = tile % tiles_n, n0 = nt * BN;
+      const int b = j & 1;
+      if (j >= 2 && !mbar_wait_warp(&add_empty[b], ((j >> 1) & 1) ^ 1, abort_flag, a.err)) break;
+      const int m0 = (mt - mu) * kBM;
+      int* sreq = reinterpret_cast<int*>(sAdd + b * add_buf_bytes<BN>());
+      float* sadd = reinterpret_cast<float*>(sreq + kBM);
+#pragma unroll
+      for (int k = 0; k < kBM / 32; ++k) sreq[lane + 32 * k] = min(max(rq[k], 0), a.R - 1);
+      __syncwarp();
+      const int nxt = next_item(tile + gridDim.x);
+      if (nxt < n_tiles) load_req(nxt);  // (in flight while this tile's addends load)
+      const int r_first = sreq[0];
+      const int n_slots = max(0, min(kSlots, sreq[min(M - m0, kBM) - 1] - r_first + 1));
+      bool ok = true;
+      if (EPI == EPI_TOKENIZE) {
+        for (int sl = 0; sl < n_slots && ok; ++sl) {
+          const int fi = ((r_first + sl) / kBM) * tiles_n + nt;  // one flag per 128 requests and column tile
+          if (fi == flag_seen) continue;
+          const unsigned* flag = a.xu_ready + fi;
+          if (ld_acquire_u32(flag) == 0u) {
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire_u32(flag) == 0u) {
+              if (*abort_flag || global_timer_ns() - t0 > 1000000000ull) {
+                atomicOr(a.err, kErrTimeout);
+                ok = false;
+                break;
+              }
+              __nanosleep(32);
+            }
+          }
+          flag_seen = fi;
+        }
+      }
+      if (!__all_sync(0xffffffffu, ok)) break;
+      for (int s0 = 0; s0 < n_slots; s0 += 4) {  // four addend rows in flight at a time
+      float4 v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int sl = s0 + k, r = r_first + sl, x = lane * 4;
+        if (sl >= n_slots || x >= BN) continue;
+        if (EPI == EPI_TOKENIZE) {
+          v[k] = __ldcg(reinterpret_cast<const float4*>(a.xu + (int64_t)r * kTokN + n0 + x));  // (written in this launch)
+          const float4 bv = __ldg(reinterpret_cast<const float4*>(a.tok_b + n0 + x));
+          v[k] = make_float4(v[k].x + bv.x, v[k].y + bv.y, v[k].z + bv.z, v[k].w + bv.w);
+          if (n0 >= kXD && !a.q_add) {  // first-layer query columns: + the mean-pool term of the request
+            const float4 qv = __ldg(reinterpret_cast<const float4*>(a.qb + (int64_t)r * (kG * kD) + (n0 - kXD) + x));
+            v[k] = make_float4(v[k].x + qv.x, v[k].y + qv.y, v[k].z + qv.z, v[k].w + qv.w);
+          }
+        } else {
+          v[k] = __ldg(reinterpret_cast<const float4*>(a.qb + ((int64_t)layer * a.R + r) * (kG * kD) + n0 + x));
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (s0 + k < n_slots && lane * 4 < BN) *reinterpret_cast<float4*>(sadd + (s0 + k) * BN + lane * 4) = v[k];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&add_full[b]);
+      tile = nxt;
+      ++j;
+    }
   } else {
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int grp = (warp - 2) >> 2;     // chunk group
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    int i = 0;
+    int i = 0, j = 0;  // tiles, row-tiles (addend buffers)
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++i) {
       const int mt = tile / tiles_n, nt = tile % tiles_n, n0 = nt * BN;
-      const int buf = i & 1;
+      const int buf = i % NACC;
       constexpr int NMY = (NCHUNK + NGRP - 1) / NGRP;
       if (EPI == EPI_TOKENIZE && mt < mu) {
-        // user row-tile: xu[r][n0 + ..] = acc + tokeniser bias, fp32; then the tile is published to the item tiles
+        // user row-tile: xu[r][n0 + ..] = acc, fp32 (the bias is added with it by the item tiles); then the tile is
+        // published to the item tiles
         const int r = mt * kBM + q * 32 + lane;
-        if (!mbar_wait(&acc_full[buf], (i >> 1) & 1, abort_flag, a.err)) break;
+        if (!mbar_wait(&acc_full[buf], (i / NACC) & 1, abort_flag, a.err)) break;
         tc_fence_after();
+        uint32_t acc[NMY][32];
+#pragma unroll
+        for (int m = 0; m < NMY; ++m)
+          if (grp + m * NGRP < NCHUNK) tmem_ld32_nowait(tbase + lane_off + buf * TC + (grp + m * NGRP) * 32, acc[m]);
+        tmem_ld_wait();
 #pragma unroll
         for (int m = 0; m < NMY; ++m) {
           const int c = grp + m * NGRP;
-          if (c >= NCHUNK) continue;
-          float v[32];
-          tmem_ld32(tbase + lane_off + buf * TC + c * 32, v);
-          if (r >= a.R) continue;
-          const float4* bias = reinterpret_cast<const float4*>(a.tok_b + n0 + c * 32);
+          if (c >= NCHUNK || r >= a.R) continue;
+          const float* v = reinterpret_cast<const float*>(acc[m]);
           float4* dst = reinterpret_cast<float4*>(a.xu + (int64_t)r * kTokN + n0 + c * 32);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 b = __ldg(bias + j);
-            dst[j] = make_float4(v[4 * j] + b.x, v[4 * j + 1] + b.y, v[4 * j + 2] + b.z, v[4 * j + 3] + b.w);
-          }
+          for (int x = 0; x < 8; ++x) dst[x] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
         epi_bar<NEPI>();
-        if (threadIdx.x == 64) {
-          __threadfence();
-          atomicAdd(a.xu_ready + mt * tiles_n + nt, 1u);
-        }
+        // the barrier orders every warp's xu stores before this release (cumulativity)
+        if (threadIdx.x == 64) red_release_add(a.xu_ready + mt * tiles_n + nt, 1u);
         continue;
       }
       const int m0 = (mt - mu) * kBM;
-      const int row = m0 + q * 32 + lane;
+      const int rl = q * 32 + lane, row = m0 + rl;
       const bool live = row < M;
-      int req = 0;
-      if (live) req = min(max(a.req_ids[row], 0), a.R - 1);
-      // the addends of this warp's chunks (per-request terms or biases) are loaded before waiting for the
-      // accumulator, so their latency hides under the tile's MMAs
-      float addv[NMY][32];
-      if (EPI == EPI_TOKENIZE && live) {
-        // the user half of this request's tokens: written by the user row-tile of this launch (bounded wait)
+      const int b = j & 1;
+      const bool staged_ok = mbar_wait_warp(&add_full[b], (j >> 1) & 1, abort_flag, a.err);
+      const int* sreq = reinterpret_cast<const int*>(sAdd + b * add_buf_bytes<BN>());
+      const float* sadd = reinterpret_cast<const float*>(sreq + kBM);
+      const int req = live ? sreq[rl] : 0;
+      const int n_slots = max(0, min(kSlots, sreq[min(M - m0, kBM) - 1] - sreq[0] + 1));
+      const int slot = req - sreq[0];
+      const bool staged = slot >= 0 && slot < n_slots;
+      if (EPI == EPI_TOKENIZE && live && !staged && staged_ok) {
+        // a request past the staged ones: its user tile is waited for here (bounded)
         const unsigned* flag = a.xu_ready + (req / kBM) * tiles_n + nt;
         if (ld_acquire_u32(flag) == 0u) {
           const uint64_t t0 = global_timer_ns();
@@ -202,23 +336,7 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
           }
         }
       }
-#pragma unroll
-      for (int m = 0; m < NMY; ++m) {
-        const int c = grp + m * NGRP, nb = n0 + c * 32;
-        if (c >= NCHUNK || !live) continue;
-        if (EPI == EPI_TOKENIZE) {
-          ldcg32(a.xu + (int64_t)req * kTokN + nb, addv[m]);  // (written in this launch: read through L2)
-          if (nb >= kXD && !a.q_add) {  // first-layer query columns: + the mean-pool term of the request
-            float qadd[32];
-            ldg32(a.qb + (int64_t)req * (kG * kD) + (nb - kXD), qadd);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) addv[m][x] += qadd[x];
-          }
-        } else if (EPI == EPI_QUERY) {
-          ldg32(a.qb + ((int64_t)layer * a.R + req) * (kG * kD) + nb, addv[m]);
-        }
-      }
-      if (!mbar_wait(&acc_full[buf], (i >> 1) & 1, abort_flag, a.err)) break;
+      if (!staged_ok || !mbar_wait_warp(&acc_full[buf], (i / NACC) & 1, abort_flag, a.err)) break;
       tc_fence_after();
       uint8_t* sb = sOut + (i & 1) * (kBM * BN * 2);
       if (EPI == EPI_TOKENIZE) {
@@ -231,38 +349,53 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
         const int c = grp + m * NGRP;
         if (c >= NCHUNK) continue;
         float v[32];
-        const float* add = addv[m];
-        const int nb = n0 + c * 32;
         tmem_ld32(tbase + lane_off + buf * TC + c * 32, v);
+        const int nb = n0 + c * 32;
         if (!live) continue;
+        // v += the row's addends: staged in shared memory, else (a request past the staged ones) read through L2
+        if (staged) {
+          const float4* ap = reinterpret_cast<const float4*>(sadd + slot * BN + c * 32);
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            const float4 t = ap[x];
+            v[4 * x] += t.x;
+            v[4 * x + 1] += t.y;
+            v[4 * x + 2] += t.z;
+            v[4 * x + 3] += t.w;
+          }
+        } else {
+          add_row_addends<EPI>(a, req, nb, layer, v);
+        }
         if (EPI == EPI_TOKENIZE) {
           // columns [32c, 32c + 32) of row rl into the staging tile: box c/2, 16-byte chunks 4 (c%2) + j, swizzled
-          const int rl = q * 32 + lane;
           uint8_t* rowp = sb + (c >> 1) * (kBM * 128) + rl * 128;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int j4 = 0; j4 < 4; ++j4) {
             uint4 p;
-            p.x = pack_bf16(v[8 * j + 0] + add[8 * j + 0], v[8 * j + 1] + add[8 * j + 1]);
-            p.y = pack_bf16(v[8 * j + 2] + add[8 * j + 2], v[8 * j + 3] + add[8 * j + 3]);
-            p.z = pack_bf16(v[8 * j + 4] + add[8 * j + 4], v[8 * j + 5] + add[8 * j + 5]);
-            p.w = pack_bf16(v[8 * j + 6] + add[8 * j + 6], v[8 * j + 7] + add[8 * j + 7]);
-            *reinterpret_cast<uint4*>(rowp + ((((c & 1) * 4 + j) ^ (rl & 7)) << 4)) = p;
+            p.x = pack_bf16(v[8 * j4 + 0], v[8 * j4 + 1]);
+            p.y = pack_bf16(v[8 * j4 + 2], v[8 * j4 + 3]);
+            p.z = pack_bf16(v[8 * j4 + 4], v[8 * j4 + 5]);
+            p.w = pack_bf16(v[8 * j4 + 6], v[8 * j4 + 7]);
+            *reinterpret_cast<uint4*>(rowp + ((((c & 1) * 4 + j4) ^ (rl & 7)) << 4)) = p;
           }
         } else if (EPI == EPI_QUERY) {
           __nv_bfloat16* out = a.Q + (int64_t)row * (kG * kD) + nb;
           uint4* dst = reinterpret_cast<uint4*>(out);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (c * 32 + j * 8 >= BN) break;
+          for (int j4 = 0; j4 < 4; ++j4) {
+            if (c * 32 + j4 * 8 >= BN) break;
             uint4 p;
-            p.x = pack_bf16(v[8 * j + 0] + add[8 * j + 0], v[8 * j + 1] + add[8 * j + 1]);
-            p.y = pack_bf16(v[8 * j + 2] + add[8 * j + 2], v[8 * j + 3] + add[8 * j + 3]);
-            p.z = pack_bf16(v[8 * j + 4] + add[8 * j + 4], v[8 * j + 5] + add[8 * j + 5]);
-            p.w = pack_bf16(v[8 * j + 6] + add[8 * j + 6], v[8 * j + 7] + add[8 * j + 7]);
-            dst[j] = p;
+            p.x = pack_bf16(v[8 * j4 + 0], v[8 * j4 + 1]);
+            p.y = pack_bf16(v[8 * j4 + 2], v[8 * j4 + 3]);
+            p.z = pack_bf16(v[8 * j4 + 4], v[8 * j4 + 5]);
+            p.w = pack_bf16(v[8 * j4 + 6], v[8 * j4 + 7]);
+            dst[j4] = p;
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&add_empty[b]);  // (this warp is done with the addend buffer)
+      ++j;
       if (EPI == EPI_TOKENIZE) {
         // the whole tile is staged: one thread stores it in boxes of 64 columns, tokens into Z and the first
         // layer's queries into Q
@@ -283,10 +416,10 @@ __global__ void __launch_bounds__(64 + NEPI * 32, 1)
     if (EPI == EPI_TOKENIZE && threadIdx.x == 64) bulk_wait_all();  // stores landed before exit
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tbase, 2 * TC);
+    tmem_dealloc(tbase, NACC * TC);
   }
 }
 
@@ -304,7 +437,7 @@ cudaError_t launch_gemm(const FwdArgs& a, const CUtensorMap& tmA, const CUtensor
   const int tiles = (mu + (M + kBM - 1) / kBM) * (N / BN);
   const int cap = max_grid > 0 && max_grid < a.num_sms ? max_grid : a.num_sms;
   const int grid = tiles < cap ? tiles : cap;
-  return launch_kernel(gemm_kernel<BN, STAGES, EPI, NEPI>, dim3(grid), dim3(64 + NEPI * 32), gemm_smem_bytes<BN, STAGES, EPI>(),
+  return launch_kernel(gemm_kernel<BN, STAGES, EPI, NEPI>, dim3(grid), dim3(96 + NEPI * 32), gemm_smem_bytes<BN, STAGES, EPI>(),
                        s, pdl && a.pdl != 0, a, tmA, tmB, tmZo, tmQo, tmU, tmWu, M, N, K, layer, mu);
 }
 

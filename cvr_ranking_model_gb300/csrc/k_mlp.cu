@@ -75,7 +75,10 @@ __device__ __forceinline__ TileInfo tile_info(const FwdArgs& a, int tile) {
 }
 
 // Named barrier among the epilogue warps only (the producer and MMA warps never take part).
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory"); }
+__device__ __forceinline__ void epi_sync() {
+  __syncwarp();  // (the warp arrives converged)
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) tmem_alloc(tslot, 512);
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tbase = *tslot;
   pdl_trigger();
@@ -496,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && kDefer && n_my > 0) finish(n_my - 1);
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);

@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) tmem_alloc(tslot, kTmemCols);
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tbase = *tslot;
   pdl_trigger();
@@ -338,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     fence_proxy_async_smem();  // the staged tiles are read by TMA stores (async proxy)
+    __syncwarp();
     asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
     if (threadIdx.x == 64) {
       if (ok) {
@@ -399,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 64) bulk_wait_all();  // (the expert outputs are written before the CTA exits)
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);

@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(256) cache_fill_kernel(const __grid_constant__
       c.p[t][slot] = 0u;
     }
   }
-  __syncthreads();
+  cta_sync();
   if (threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(a.cache_ctl + 2, 1u) == gridDim.x - 1) {  // every block has read the log's length
@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(kCsThreads) seq_colsum_kernel(const __grid_con
   __shared__ int last;
 #pragma unroll
   for (int e = 0; e < 8; ++e) part[rg][cg * 8 + e] = acc[e];
-  __syncthreads();
+  cta_sync();
   float colsum = 0.f;
   if (t < kD) {
 #pragma unroll
@@ -450,9 +450,9 @@ __global__ void __launch_bounds__(kCsThreads) seq_colsum_kernel(const __grid_con
     float* rgp = a.colsum + ((int64_t)r * kG + g) * a.max_chunks * kD;
     if (t < kD) rgp[chunk * kD + t] = colsum;
     __threadfence();
-    __syncthreads();
+    cta_sync();
     if (t == 0) last = atomicAdd(cnt, 1u) == (unsigned)(chunks - 1);
-    __syncthreads();
+    cta_sync();
     if (!last) return;
     if (t < kD) {
       colsum = 0.f;
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kCsThreads) seq_colsum_kernel(const __grid_con
     if (t == 0) *cnt = 0u;
   }
   if (t < kD) m[t] = len > 0 ? colsum / (float)len : 0.f;
-  __syncthreads();
+  cta_sync();
   // thread t: output row n = t % 128, half of K = t / 128; the two halves are added in a fixed order
   const int nrow = t & (kD - 1), half = t >> 7;
   for (int l = 0; l < a.n_layers; ++l) {
@@ -480,11 +480,11 @@ __global__ void __launch_bounds__(kCsThreads) seq_colsum_kernel(const __grid_con
       }
     }
     gpart[half][nrow] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-    __syncthreads();
+    cta_sync();
     if (t < kD)
       a.qb[((int64_t)l * a.R + r) * (kG * kD) + g * kD + t] =
           __ldg(a.q_b + l * kG * kD + g * kD + t) + (gpart[0][t] + gpart[1][t]);
-    __syncthreads();
+    cta_sync();
   }
 }
 
