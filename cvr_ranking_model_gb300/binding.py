@@ -16,7 +16,7 @@ from . import _build
 
 MAX_LAYERS, N_USER_FIELDS, N_ITEM_FIELDS, N_GROUPS, N_EXPERTS, N_TASKS = 4, 8, 8, 3, 3, 2
 STAGE_H, STAGE_Z, STAGE_Q, STAGE_Y, STAGE_EXPERTS, STAGE_GATES = range(6)
-OPT_PROFILE, OPT_CUDA_GRAPH, OPT_PDL, OPT_ATTENTION_TC, OPT_PLE_INT8 = 0, 1, 2, 3, 4
+OPT_PROFILE, OPT_CUDA_GRAPH, OPT_PDL, OPT_ATTENTION_TC, OPT_PLE_INT8, OPT_KEEP_STAGES = 0, 1, 2, 3, 4, 5
 NOALLOC_MAX_CAND = 1024  # CVR_NOALLOC_MAX_CAND
 TIMELINE_RECORDS = 10 * 8192 * 3  # CVR_TIMELINE_RECORDS
 TIMELINE_KERNELS = ["sparse", "seq_mlp", "seq_colsum", "tokenizer", "query", "attention", "token_mixer", "ple_heads",

@@ -114,6 +114,8 @@ struct cvr_handle {
   CUtensorMap tm_Xs, tm_I, tm_U, tm_x_Z, tm_x_Y, tm_full_Z, tm_full_Y, tm_Q, tm_H, tm_R, tm_Ex;
   // graphs, profiling
   bool use_graph = true, profile = false, pdl = true;
+  bool keep_stages = false;  // the PLE also writes the expert outputs and gates (for cvr_debug_stage)
+  bool last_kept = false;    // ... and the last call did
   bool attn_tc = false;  // cross-attention on the tcgen05 kernel instead of the register-tile one
   bool last_q_add = false;  // the last call left the first layer's queries without their mean-pooled term
   // hot-row caches in HBM, per table (slots == 0: none)
@@ -449,6 +451,7 @@ FwdArgs make_args(cvr_handle* h, int R, int B, const int32_t* req_ids, const int
   a.tm_gain = h->tm_gain;
   a.ple_b = h->ple_b;
   a.ple_s8 = h->ple_int8 ? h->ple_s8 : nullptr;
+  a.keep_stages = h->keep_stages ? 1 : 0;
   a.head_b1 = h->head_b1;
   a.head_w2 = h->head_w2;
   a.head_b2 = h->head_b2;
@@ -626,6 +629,7 @@ cvr_status run_forward(cvr_handle* h, int32_t R, int32_t B, const int32_t* req_i
     h->last_launches = launches;
   }
   h->last_R = R;
+  h->last_kept = h->keep_stages;
   h->last_B = B;
   h->last_q_add = fork_tokenizer(h, R, h->profile) && h->n_layers == 1;
   if (!sync) return CVR_OK;
@@ -1041,6 +1045,8 @@ cvr_status cvr_debug_stage(cvr_handle* h, int32_t stage, void* dst, int64_t byte
     case CVR_STAGE_GATES: src = h->gates; need = B * 8 * 4; break;
     default: return fail(h, CVR_E_ARG, "unknown stage");
   }
+  if ((stage == CVR_STAGE_EXPERTS || stage == CVR_STAGE_GATES) && !h->last_kept)
+    return fail(h, CVR_E_ARG, "the last call did not keep the expert outputs and gates (set CVR_OPT_KEEP_STAGES)");
   if (bytes != need) return fail(h, CVR_E_SHAPE, "stage size mismatch: expected " + std::to_string(need) + " bytes");
   cudaError_t ce = cudaSuccess;
   if (stage == CVR_STAGE_Q && h->last_q_add) {
@@ -1075,10 +1081,12 @@ cvr_status cvr_set_option(cvr_handle* h, int32_t option, int64_t value) {
     h->use_graph = value != 0;
     return CVR_OK;
   }
-  if (option == CVR_OPT_PDL || option == CVR_OPT_ATTENTION_TC || option == CVR_OPT_PLE_INT8) {
+  if (option == CVR_OPT_PDL || option == CVR_OPT_ATTENTION_TC || option == CVR_OPT_PLE_INT8 ||
+      option == CVR_OPT_KEEP_STAGES) {
     if (option == CVR_OPT_PDL) h->pdl = value != 0;
     else if (option == CVR_OPT_ATTENTION_TC) h->attn_tc = value != 0;
-    else h->ple_int8 = value != 0;
+    else if (option == CVR_OPT_PLE_INT8) h->ple_int8 = value != 0;
+    else h->keep_stages = value != 0;
     drop_graphs(h);
     return CVR_OK;
   }
@@ -1256,14 +1264,13 @@ extern "C" cvr_status cvr_selftest_wait_timeout(cvr_handle* h) {
 
 // ------------------------------------------------------------------------------------------
 // Prediction step without allocation: the PLE and prediction-head kernel on a caller's Token Mixer
-// output, its intermediates (expert outputs, gates) and the error word in one fixed file-scope device
-// array instead of the handle's growable workspace.
+// output, its intermediate (the gate-weighted expert sums r_t) and the error word in one fixed file-scope
+// device array instead of the handle's growable workspace.
 namespace {
 
 constexpr int kNoAllocMaxCand = CVR_NOALLOC_MAX_CAND;
-constexpr size_t kNaGatesOff = (size_t)kNoAllocMaxCand * kPleN * 2;       // expert outputs, bf16 [n][768]
-constexpr size_t kNaROff = kNaGatesOff + (size_t)kNoAllocMaxCand * 8 * 4;    // gates, fp32 [n][8]
-constexpr size_t kNaErrOff = kNaROff + (size_t)2 * kNoAllocMaxCand * kDE * 2;  // r_t, bf16 [2][n][256]
+constexpr size_t kNaROff = 0;                                                // r_t, bf16 [2][n][256]
+constexpr size_t kNaErrOff = kNaROff + (size_t)2 * kNoAllocMaxCand * kDE * 2;
 constexpr size_t kNaBytes = kNaErrOff + 512;                                 // error word (+0), CTA counter (+256)
 constexpr int kNaMaxDevices = 64;
 
@@ -1313,14 +1320,15 @@ cvr_status cvr_predict_noalloc(cvr_handle* h, int32_t n_cand, const void* y, flo
   if (!encode_2d(&tmY, y, kYD, (uint64_t)n_cand, kYD, 64, 128))
     return fail(h, CVR_E_CUDA, "cuTensorMapEncodeTiled failed for Y");
   FwdArgs a = make_args(h, 1, n_cand, nullptr, nullptr, nullptr, nullptr, out, nullptr, nullptr);
-  // nothing but the two prediction kernels' own buffers is reachable from these arguments
+  // nothing but the prediction kernel's own buffers is reachable from these arguments
   a.U = a.I = a.Xs = a.H = a.Z = a.Y = a.Q = nullptr;
   a.colsum = a.xu = a.qb = nullptr;
   a.cs_count = nullptr;
   a.attn_state = nullptr;
   a.attn_count = nullptr;
-  a.Ex = reinterpret_cast<bf16*>(sc);
-  a.gates = reinterpret_cast<float*>(sc + kNaGatesOff);
+  a.Ex = nullptr;  // the expert outputs and gates are not kept
+  a.gates = nullptr;
+  a.keep_stages = 0;
   a.Rt = reinterpret_cast<bf16*>(sc + kNaROff);
   a.ple_ready = nullptr;  // a caller's Y: the kernel waits for the preceding work in the stream instead
 
@@ -1328,11 +1336,12 @@ cvr_status cvr_predict_noalloc(cvr_handle* h, int32_t n_cand, const void* y, flo
   a.done = reinterpret_cast<unsigned*>(sc + kNaErrOff + 256);
   cudaStream_t s = h->stream;
   ce = cudaMemsetAsync(sc + kNaErrOff, 0, 512, s);  // the error word and the CTA counter start at zero
-  CUtensorMap tmR, tmEx;
-  if (!encode_2d(&tmR, a.Rt, kDE, (uint64_t)2 * kNoAllocMaxCand, kDE, 64, 128) ||
-      !encode_2d(&tmEx, a.Ex, kPleN, (uint64_t)kNoAllocMaxCand, kPleN, 64, 128))
+  CUtensorMap tmR;
+  if (!encode_2d(&tmR, a.Rt, kDE, (uint64_t)2 * kNoAllocMaxCand, kDE, 64, 128))
     return fail(h, CVR_E_CUDA, "cuTensorMapEncodeTiled failed for the prediction scratch");
-  if (ce == cudaSuccess) ce = launch_ple_heads(a, tmY, h->ple_int8 ? h->tm_pleW8 : h->tm_pleW, tmR, tmEx, h->tm_headW1, kNoAllocMaxCand, s);
+  // (the expert-output map is not used without keep_stages: r_t's map stands in for it)
+  if (ce == cudaSuccess)
+    ce = launch_ple_heads(a, tmY, h->ple_int8 ? h->tm_pleW8 : h->tm_pleW, tmR, tmR, h->tm_headW1, kNoAllocMaxCand, s);
   if (ce != cudaSuccess) return cuda_fail(h, ce, "prediction kernels");
   return sync_status(h);
 }

@@ -107,6 +107,7 @@ struct FwdArgs {
   __nv_bfloat16* Q;       // [B][384]
   __nv_bfloat16* Ex;      // [B][768] expert outputs (after ReLU)
   float* gates;           // [B][8] task gate probabilities (2 x 3, padded)
+  int keep_stages;        // 1: the PLE also writes Ex and gates (read back by cvr_debug_stage); 0: skipped
   __nv_bfloat16* Rt;      // [2][rows][256] gate-weighted expert sums r_t (task-major), the heads' A operand
   unsigned* ple_ready;    // [B/128] per 128-row block: 8-candidate tiles the last Token Mixer has written, or null
                           // (zeroed by the first kernel of each call; null: wait for the previous grid instead)

@@ -413,7 +413,9 @@ __global__ void __launch_bounds__(96 + NEPI * 32, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
-    if (EPI == EPI_TOKENIZE && threadIdx.x == 64) bulk_wait_all();  // stores landed before exit
+    // (the staging buffers have been read before the CTA exits; the stores complete with the grid, which the next
+    // kernel waits for)
+    if (EPI == EPI_TOKENIZE && threadIdx.x == 64) bulk_wait_read<0>();
   }
   tc_fence_before();
   cta_sync();

@@ -7,8 +7,8 @@
 //                of Y . W^T (Y [rows][2048] bf16, K = 2048) on tcgen05 with the accumulator in TMEM, A and B
 //                streamed by TMA through a 5-stage mbarrier ring. Every CTA has all gate logits, so each forms
 //                its 64-unit slice of r_t = sum_k g_t[k] ReLU(e_k + b_k) for both tasks (fp32, then bf16) and
-//                writes it with TMA stores into R [task][row][256], next to the expert outputs and the gates;
-//                then it counts its row block as done.
+//                writes it with TMA stores into R [task][row][256] (and, when the call keeps them, the expert
+//                outputs and the gates).
 //  heads         the four CTAs of a row block form a cluster. Once all four slices of R are written (one cluster
 //                barrier), CTA n computes hidden units [64 (n % 2), +64) of task n / 2's head, ReLU(W1_t r_t +
 //                b1) on tcgen05 (M=128, N=64, K=256) with r_t read back through L2 and its W1 rows loaded into the
@@ -300,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float v = I8 ? fmaf(__uint_as_float(e[k][j]), sk[j], bk[j]) : __uint_as_float(e[k][j]) + bk[j];
           e[k][j] = __float_as_uint(fmaxf(v, 0.f));
         }
+        if (!a.keep_stages) continue;
         uint8_t* rowp = smem + S::kOffStage + (kNT + k) * kATile + rl * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          pack_bf16(__uint_as_float(e[k][8 * c + 4]), __uint_as_float(e[k][8 * c + 5])),
                          pack_bf16(__uint_as_float(e[k][8 * c + 6]), __uint_as_float(e[k][8 * c + 7])));
       }
-      if (row < a.B && grp == 0 && n == 0) {
+      if (a.keep_stages && row < a.B && grp == 0 && n == 0) {
         float4* gd = reinterpret_cast<float4*>(a.gates + (int64_t)row * 8);
         gd[0] = make_float4(g[0][0], g[0][1], g[0][2], g[1][0]);
         gd[1] = make_float4(g[1][1], g[1][2], 0.f, 0.f);
@@ -342,11 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
     if (threadIdx.x == 64) {
       if (ok) {
-        // r_t slices first (the heads wait for them), the expert outputs in a second group
+        // r_t slices first (the heads wait for them), the expert outputs (when kept) in a second group
         for (int t = 0; t < kNT; ++t) tma_store_2d(&tmR, smem + S::kOffStage + t * kATile, n * kSlice, t * r_rows + m0);
         bulk_commit();
-        for (int k = 0; k < kNE; ++k)
-          tma_store_2d(&tmEx, smem + S::kOffStage + (kNT + k) * kATile, k * kDE + n * kSlice, m0);
+        if (a.keep_stages)
+          for (int k = 0; k < kNE; ++k)
+            tma_store_2d(&tmEx, smem + S::kOffStage + (kNT + k) * kATile, k * kDE + n * kSlice, m0);
         bulk_commit();
         asm volatile("cp.async.bulk.wait_group 1;" ::: "memory");  // the r_t slices are written
         bulk_wait_read<0>();  // and the staging area has been read (the head operands reuse it)
@@ -398,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float logit = (plog[rl] + plog[kBM + rl]) + a.head_b2[ht];
     if (row < a.B) a.out[(int64_t)row * kNT + ht] = 1.f / (1.f + expf(-logit));
   }
-  if (threadIdx.x == 64) bulk_wait_all();  // (the expert outputs are written before the CTA exits)
+  if (threadIdx.x == 64) bulk_wait_read<0>();  // (the stores' shared-memory source is read before the CTA exits)
   tc_fence_before();
   cta_sync();
   if (warp == 1) {

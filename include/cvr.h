@@ -181,7 +181,8 @@ cvr_status cvr_score_host(cvr_handle* h, int32_t n_req, int32_t n_cand, const in
  *   CVR_STAGE_Q   bf16 [n_cand][3][128]: queries of the last layer
  *   CVR_STAGE_Y   bf16 [n_cand][16][128]: output of the last Token Mixer
  *   CVR_STAGE_EXPERTS bf16 [n_cand][768]: PLE expert outputs (after ReLU)
- *   CVR_STAGE_GATES fp32 [n_cand][8]: task gates (2 x 3, padded to 8) */
+ *   CVR_STAGE_GATES fp32 [n_cand][8]: task gates (2 x 3, padded to 8)
+ * The last two are written only by calls made with CVR_OPT_KEEP_STAGES set (else CVR_E_ARG). */
 enum { CVR_STAGE_H = 0, CVR_STAGE_Z = 1, CVR_STAGE_Q = 2, CVR_STAGE_Y = 3, CVR_STAGE_EXPERTS = 4, CVR_STAGE_GATES = 5 };
 cvr_status cvr_debug_stage(cvr_handle* h, int32_t stage, void* dst, int64_t bytes);
 
@@ -202,8 +203,17 @@ cvr_status cvr_debug_stage(cvr_handle* h, int32_t stage, void* dst, int64_t byte
  *                            fp32 sums, so the integers enter the tensor cores exactly. Outputs stay inside the
  *                            pCVR tolerance of the fp64 model on the production and two-layer workloads but
  *                            differ from the bf16 weights' (default 0: bf16 weights). Mixed-precision inference,
- *                            iQIYI ad-CVR article, outlook section. */
-enum { CVR_OPT_PROFILE = 0, CVR_OPT_CUDA_GRAPH = 1, CVR_OPT_PDL = 2, CVR_OPT_ATTENTION_TC = 3, CVR_OPT_PLE_INT8 = 4 };
+ *                            iQIYI ad-CVR article, outlook section.
+ *   CVR_OPT_KEEP_STAGES  1 = calls also write the PLE expert outputs and gates, for CVR_STAGE_EXPERTS and
+ *                            CVR_STAGE_GATES (default 0: not written; they are not needed for the scores) */
+enum {
+  CVR_OPT_PROFILE = 0,
+  CVR_OPT_CUDA_GRAPH = 1,
+  CVR_OPT_PDL = 2,
+  CVR_OPT_ATTENTION_TC = 3,
+  CVR_OPT_PLE_INT8 = 4,
+  CVR_OPT_KEEP_STAGES = 5
+};
 cvr_status cvr_set_option(cvr_handle* h, int32_t option, int64_t value);
 
 /* With CVR_OPT_PROFILE set: per-kernel device times of the last call, in launch order. Writes up to
@@ -237,9 +247,9 @@ cvr_status cvr_selftest_wait_timeout(cvr_handle* h);
  * output, without allocating device memory. The papers have no counterpart: it serves callers that
  * cannot allocate mid-flight (a serving loop whose device memory is all pre-reserved by its own pool, or
  * one that cannot afford the device-wide synchronisation of cudaMalloc / cudaFree that a growing
- * cvr_score workspace would cost). Its intermediates (expert outputs, gates, error word) live in one
- * fixed device array of CVR_NOALLOC_MAX_CAND x 2,592 + 512 bytes (2.5 MB) inside this library (expert outputs,
- * gates and the gate-weighted expert sums of every candidate).
+ * cvr_score workspace would cost). Its intermediates live in one fixed device array of
+ * CVR_NOALLOC_MAX_CAND x 1,024 + 512 bytes (1 MB) inside this library: the gate-weighted expert sums of every
+ * candidate and the error word (the expert outputs and gates are not kept, whatever CVR_OPT_KEEP_STAGES says).
  *   y    DEVICE bf16 [n_cand][16][128]: the last Token Mixer's output (the layout of CVR_STAGE_Y), 16-byte
  *        aligned; read only.
  *   out  DEVICE fp32 [n_cand][2]: pCVR per task, written by the call (caller-owned).

@@ -55,6 +55,36 @@ def test_tiny_every_candidate_and_stage():
     _check_full(wl, w, stages=True)
 
 
+def test_expert_and_gate_stages_when_kept():
+    """CVR_OPT_KEEP_STAGES: the PLE also writes its expert outputs and task gates, which match the PLE of
+    iQIYI CVR 3.2.4 recomputed in fp64 from the oracle's last Token Mixer output; the scores are the same
+    bits with and without the option, and without it the two stages are refused."""
+    import torch
+    import cvr_ranking_model_gb300 as cvr
+    wl = synth.make_workload("tiny", n_req=3, cand_per_req=[100, 1, 60])
+    w = synth.make_weights(wl.n_layers, wl.seed, bias_scale=0.05)
+    g = GpuRun(wl, w, debug=False)
+    g.run()
+    plain = g.out()
+    with pytest.raises(cvr.CvrError):
+        g.stage(cvr.STAGE_EXPERTS, (wl.n_cand, 768), torch.bfloat16)
+    g.sc.set_option(cvr.OPT_KEEP_STAGES, 1)
+    g.run()
+    assert np.array_equal(g.out(), plain)
+    ref = oracle.score(wl, w, dumps=True)
+    y = ref.dumps["Y"][-1].reshape(wl.n_cand, -1)
+    e = np.maximum(0.0, y @ np.concatenate([w[f"ple{k}_w"] for k in range(3)]).T +
+                   np.concatenate([w[f"ple{k}_b"] for k in range(3)]))
+    rel_close(g.stage(cvr.STAGE_EXPERTS, (wl.n_cand, 768), torch.bfloat16), e, 0.03, "expert outputs")
+    gates = g.stage(cvr.STAGE_GATES, (wl.n_cand, 8), torch.float32)
+    for t in range(2):
+        gl = y @ w[f"gate{t}_w"].T + w[f"gate{t}_b"]
+        p = np.exp(gl - gl.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        assert np.max(np.abs(gates[:, 3 * t:3 * t + 3] - p)) < 0.02, t
+    assert not gates[:, 6:].any()
+
+
 def test_tiny_with_biases_and_gains():
     wl = synth.make_workload("tiny")
     w = synth.make_weights(wl.n_layers, wl.seed, bias_scale=0.05, gain_jitter=0.1)
