@@ -506,8 +506,8 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
   for (int g = 0; g < kG; ++g) seq_tiles += (int)(((int64_t)a.R * a.L[g] + 127) / 128);
   const int seq_grid = std::min(seq_tiles, a.num_sms);
   // Two branches after the sparse kernel when the sequence encoder leaves at least half the SMs free. Side
-  // stream: the user half of the tokeniser, then the tokeniser itself (it needs the pooled embeddings only),
-  // on the SMs the encoder does not use. This stream: the sequence encoder and its column sums. The first
+  // stream: the tokeniser with its user row-tiles (it needs the pooled embeddings only), on the SMs the encoder
+  // does not use. This stream: the sequence encoder and its column sums. The first
   // layer's queries then lack their mean-pooled sequence term, which the attention kernel adds (the tcgen05
   // attention reads Q by TMA and keeps the one-stream order).
   const bool fork = fork_tokenizer(h, a.R, events);
