@@ -244,7 +244,11 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
     const int64_t n_events = (int64_t)a.R * a.SL;
     const int c = lane >> 3, part = lane & 7;
     const int64_t stride = nw * kEvU;
-    int64_t ev = gw;
+    // the warps that walked one bag unit fewer (gw >= n_units % nw) take the first events, so that the
+    // warps with the most work are not also the ones with an event round
+    const int64_t n_units = ((int64_t)a.R * kFu + (int64_t)a.B * kFi + 3) / 4;
+    const int64_t extra = n_units % nw;
+    int64_t ev = gw >= extra ? gw - extra : gw + (nw - extra);
     int64_t id_next[kEvU];
 #pragma unroll
     for (int u = 0; u < kEvU; ++u) {
