@@ -718,6 +718,7 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
     if (pe == cudaSuccess) pe = prepare_attention_kernel();
     if (pe == cudaSuccess) pe = prepare_attention_tc_kernel();
     if (pe == cudaSuccess) pe = prepare_ple_kernel();
+    if (pe == cudaSuccess) pe = prepare_sparse_kernel();
     if (pe != cudaSuccess) {
       fprintf(stderr, "cvr_create: kernel attribute setup failed: %s\n", cudaGetErrorString(pe));
       cudaGetLastError();

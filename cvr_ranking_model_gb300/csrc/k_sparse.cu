@@ -21,6 +21,22 @@ constexpr int kSparseBlocksPerSm = 3;  // persistent grid
 
 __device__ __forceinline__ float clampf(float v, float c) { return fminf(fmaxf(v, -c), c); }
 
+// The gather's landing slots for embedding rows: per warp 2 units x [4 bags][8 rows][8 x 16 bytes] (dynamic
+// shared memory, 64 KB per block).
+constexpr int kSparseSmem = kSparseThreads / 32 * 2 * 4 * 8 * 8 * 16;
+__device__ __forceinline__ float4* sparse_slots() {
+  extern __shared__ float4 sparse_smem[];
+  return sparse_smem;
+}
+__device__ __forceinline__ void sparse_cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void sparse_cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void sparse_cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float4 v) {
   uint2 p;
   p.x = pack_bf16(v.x, v.y);
@@ -127,32 +143,22 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
     const int64_t n_units = (n_bags + 3) / 4;
     const int grp = lane >> 3, sub = lane & 7;  // bag of this lane within the unit, its 4 columns
     auto bag_of = [&](int64_t u) { return min(u * 4 + grp, n_bags - 1); };
-    // A bag's [s, e) from the offsets, checked where it is loaded: a negative start or an end before the start
+    // A bag's [s, e) from the offsets. They are loaded two units ahead and checked one unit ahead, where they
+    // are first used (so that the check does not wait for the load): a negative start or an end before the start
     // is reported and the bag is read as empty, so no id is ever read outside bag_ids.
     auto load_bag = [&](int64_t b, int64_t& s, int64_t& e) {
       s = a.bag_offsets[b];
       e = a.bag_offsets[b + 1];
+    };
+    auto check_bag = [&](int64_t& s, int64_t& e) {
       if (s < 0 || e < s) {
         errbits |= kErrOffsets;
         s = e = 0;
       }
     };
-    int64_t u0 = gw, s0 = 0, e0 = 0, id0 = 0, s1 = 0, e1 = 0;
-    if (u0 < n_units) load_bag(bag_of(u0), s0, e0);
-    if (u0 + nw < n_units) load_bag(bag_of(u0 + nw), s1, e1);
-    if (u0 < n_units && s0 + sub < e0) id0 = a.bag_ids[s0 + sub];
-    while (u0 < n_units) {  // warp-uniform
-      const int64_t u1 = u0 + nw, u2 = u1 + nw;
-      // stage A: offsets of unit k+2; stage B: first ids of unit k+1 (raw; checked when used)
-      int64_t s2 = 0, e2 = 0, id1 = 0;
-      if (u2 < n_units) load_bag(bag_of(u2), s2, e2);
-      if (u1 < n_units && s1 + sub < e1) id1 = a.bag_ids[s1 + sub];
-      // stage C: the rows of unit k
-      const int64_t bag_raw = u0 * 4 + grp;
-      const bool live = bag_raw < n_bags;  // dead lanes still take part in the shuffles
-      const int64_t bag = live ? bag_raw : n_bags - 1;
-      int field;
-      __nv_bfloat16* dst;
+    // Where a bag's rows go: field, table rows, output row, for the bag of this lane in unit u.
+    auto bag_place = [&](int64_t u, int& field, __nv_bfloat16*& dst) {
+      const int64_t bag = bag_of(u);
       if (bag < n_user_bags) {
         field = (int)(bag % kFu);
         dst = a.U + (bag / kFu) * kUD + field * kE;
@@ -162,50 +168,119 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
         field = kFu + f;
         dst = a.I + (ib / kFi) * kID + f * kE;
       }
-      const int64_t rows = a.table_rows[field];
-      const int64_t s = s0, e = e0;  // (checked when loaded)
-      // The 8 lanes of a bag hold 8 ids at once (one each), share them by shuffle, then have all 8 rows in
-      // flight; the fp32 sum still runs in bag order from 0 (bit-exact with the definition). The loop count
-      // is the warp's largest bag, so every lane reaches every shuffle.
+    };
+    // The address this lane's row slot reads (its id j = s + base + sub, checked; cache slot or table row),
+    // or null when the bag has no row there. Counts and logs the cache's hits and misses (warp-collective).
+    auto row_addr = [&](int64_t u, int64_t j, int64_t e, int64_t id, bool& bad) -> const float* {
+      const bool live = u * 4 + grp < n_bags;
+      int field;
+      __nv_bfloat16* dst;
+      bag_place(u, field, dst);
+      const float* src = nullptr;
+      bool hit = false, miss = false;
+      int64_t mine = 0;
+      if (j < e) {
+        mine = id;
+        if (mine < 0 || mine >= a.table_rows[field]) {
+          if (live) bad = true;
+          mine = 0;
+        }
+        if (a.dbg_rows && live) a.dbg_rows[j] = mine;
+        src = kCache ? row_src(a, field, mine, epoch, live, hit, miss) : a.tables[field] + mine * kE;
+      }
+      if (cached) {
+        miss = miss && live;
+        n_hit += hit && live;
+        n_miss += miss;
+        log_misses(a, miss, field, mine, lane);
+      }
+      return src;
+    };
+    // Rows [s, s + 8) of each bag of unit u into one of this warp's two landing slots: lane `sub` copies the
+    // 16-byte part `sub` of each row (the 8 lanes of a bag exchange the row addresses), so every lane later
+    // reads only what it copied itself. One cp.async group per unit.
+    float4* my_slots = sparse_slots() + (tid >> 5) * (2 * 4 * 8 * 8);
+    auto issue_rows = [&](int64_t u, int64_t s, int64_t e, int64_t id, int slot) {
+      bool bad = false;
+      const float* src = u < n_units ? row_addr(u, s + sub, e, id, bad) : nullptr;
+      if (bad) errbits |= kErrIdRange;
+      float4* dst = my_slots + slot * (4 * 8 * 8) + grp * 64 + sub;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float* p = reinterpret_cast<const float*>(__shfl_sync(0xffffffffu, (long long)src, r, 8));
+        if (s + r < e) sparse_cp_async16(dst + r * 8, p + sub * 4);
+      }
+      sparse_cp_async_commit();
+    };
+    // Pipeline per warp, unit k of its grid-stride sequence: offsets of k+3 load (raw), k+2's are checked and
+    // its first ids load, k+1's rows are copied into a landing slot, and k's rows (copied one unit earlier) are
+    // summed -- so two units of rows are in flight at once, without holding them in registers.
+    int64_t s0 = 0, e0 = 0, s1 = 0, e1 = 0, s2 = 0, e2 = 0, id1 = 0;
+    int64_t u0 = gw;
+    if (u0 < n_units) load_bag(bag_of(u0), s0, e0);
+    if (u0 + nw < n_units) load_bag(bag_of(u0 + nw), s1, e1);
+    if (u0 + 2 * nw < n_units) load_bag(bag_of(u0 + 2 * nw), s2, e2);
+    check_bag(s0, e0);
+    check_bag(s1, e1);
+    {
+      int64_t id0 = 0;
+      if (u0 < n_units && s0 + sub < e0) id0 = a.bag_ids[s0 + sub];
+      if (u0 + nw < n_units && s1 + sub < e1) id1 = a.bag_ids[s1 + sub];
+      if (u0 < n_units) issue_rows(u0, s0, e0, id0, 0);
+    }
+    int slot = 0;
+    while (u0 < n_units) {  // warp-uniform
+      const int64_t u1 = u0 + nw, u2 = u1 + nw, u3 = u2 + nw;
+      int64_t s3 = 0, e3 = 0, id2 = 0;
+      if (u3 < n_units) load_bag(bag_of(u3), s3, e3);
+      check_bag(s2, e2);
+      if (u2 < n_units && s2 + sub < e2) id2 = a.bag_ids[s2 + sub];
+      if (u1 < n_units) issue_rows(u1, s1, e1, id1, slot ^ 1);
+      // the rows of unit k: every group but the one just committed has landed
+      if (u1 < n_units) sparse_cp_async_wait<1>();
+      else sparse_cp_async_wait<0>();
+      const bool live = u0 * 4 + grp < n_bags;
+      int field;
+      __nv_bfloat16* dst;
+      bag_place(u0, field, dst);
+      const int64_t bag = bag_of(u0);
+      const int64_t s = s0, e = e0;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4* land = my_slots + slot * (4 * 8 * 8) + grp * 64 + sub;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if (s + r < e) {  // the fp32 sum runs in bag order from 0 (bit-exact with the definition)
+          const float4 v = land[r * 8];
+          acc.x = __fadd_rn(acc.x, v.x);
+          acc.y = __fadd_rn(acc.y, v.y);
+          acc.z = __fadd_rn(acc.z, v.z);
+          acc.w = __fadd_rn(acc.w, v.w);
+        }
+      }
+      // bags of more than 8 ids: the rest in rounds of 8 read directly (the loop count is the warp's largest
+      // bag, so every lane reaches every shuffle)
       int64_t nmax = e - s;
       nmax = max(nmax, (int64_t)__shfl_xor_sync(0xffffffffu, (long long)nmax, 8));
       nmax = max(nmax, (int64_t)__shfl_xor_sync(0xffffffffu, (long long)nmax, 16));
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int64_t base = 0; base < nmax; base += 8) {
+      for (int64_t base = 8; base < nmax; base += 8) {
         const int64_t j = s + base + sub;
-        int64_t mine = 0;
-        const float* src = a.tables[field];
-        bool hit = false, miss = false;
-        if (j < e) {
-          mine = base == 0 ? id0 : a.bag_ids[j];
-          if (mine < 0 || mine >= rows) {
-            if (live) errbits |= kErrIdRange;
-            mine = 0;
-          }
-          if (a.dbg_rows && live) a.dbg_rows[j] = mine;
-          src = kCache ? row_src(a, field, mine, epoch, live, hit, miss) : src + mine * kE;
-        }
-        if (cached) {
-          miss = miss && live;
-          n_hit += hit && live;
-          n_miss += miss;
-          log_misses(a, miss, field, mine, lane);
-        }
-        // the 8 lanes of a bag exchange row addresses (cache slot or table row) instead of ids
+        bool bad = false;
+        const float* src = row_addr(u0, j, e, j < e ? a.bag_ids[j] : 0, bad);
+        if (bad) errbits |= kErrIdRange;
         float4 v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float* p = reinterpret_cast<const float*>(__shfl_sync(0xffffffffu, (long long)src, u, 8));
-          v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (s + base + u < e) v[u] = ld_row(p, sub, cached);
+        for (int r = 0; r < 8; ++r) {
+          const float* p = reinterpret_cast<const float*>(__shfl_sync(0xffffffffu, (long long)src, r, 8));
+          v[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (s + base + r < e) v[r] = ld_row(p, sub, cached);
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          if (s + base + u < e) {
-            acc.x = __fadd_rn(acc.x, v[u].x);
-            acc.y = __fadd_rn(acc.y, v[u].y);
-            acc.z = __fadd_rn(acc.z, v[u].z);
-            acc.w = __fadd_rn(acc.w, v[u].w);
+        for (int r = 0; r < 8; ++r) {
+          if (s + base + r < e) {
+            acc.x = __fadd_rn(acc.x, v[r].x);
+            acc.y = __fadd_rn(acc.y, v[r].y);
+            acc.z = __fadd_rn(acc.z, v[r].z);
+            acc.w = __fadd_rn(acc.w, v[r].w);
           }
         }
       }
@@ -226,12 +301,16 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
         store_bf16x4(dst + sub * 4, m);
         if (a.dbg_pooled) reinterpret_cast<float4*>(a.dbg_pooled + bag * kE)[sub] = m;
       }
+      __syncwarp();  // (the slot just read is the next unit's landing slot)
       u0 = u1;
       s0 = s1;
       e0 = e1;
-      id0 = id1;
       s1 = s2;
       e1 = e2;
+      id1 = id2;
+      s2 = s3;
+      e2 = e3;
+      slot ^= 1;
     }
   }
 
@@ -494,9 +573,16 @@ __global__ void __launch_bounds__(kCsThreads) seq_colsum_kernel(const __grid_con
 
 }  // namespace
 
+cudaError_t prepare_sparse_kernel() {
+  cudaError_t e = cudaFuncSetAttribute(sparse_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSparseSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(sparse_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSparseSmem);
+  return e;
+}
+
 cudaError_t launch_sparse(const FwdArgs& a, cudaStream_t s) {
   return launch_kernel(a.cache_on ? sparse_kernel<true> : sparse_kernel<false>, dim3(a.num_sms * kSparseBlocksPerSm),
-                       dim3(kSparseThreads), 0, s, false, a);
+                       dim3(kSparseThreads), kSparseSmem, s, false, a);
 }
 
 cudaError_t launch_cache_admit(const FwdArgs& a, unsigned* const* claims, cudaStream_t s) {
