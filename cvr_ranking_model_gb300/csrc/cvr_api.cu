@@ -72,7 +72,7 @@ struct cvr_handle {
   // the tokeniser's token columns run on a second stream, next to the sequence encoder (fork after the
   // sparse kernel, join before the query columns)
   cudaStream_t side = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_tail = nullptr;
   cvr_config cfg{};
   int n_layers = 1, SL = 0;
   int L[kG] = {0, 0, 0};
@@ -507,12 +507,15 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
   const int seq_grid = std::min(seq_tiles, a.num_sms);
   // Two branches after the sparse kernel when the sequence encoder leaves at least half the SMs free. Side
   // stream: the tokeniser with its user row-tiles (it needs the pooled embeddings only), on the SMs the encoder
-  // does not use. This stream: the sequence encoder and its column sums. The first
-  // layer's queries then lack their mean-pooled sequence term, which the attention kernel adds (the tcgen05
-  // attention reads Q by TMA and keeps the one-stream order).
+  // does not use. This stream: the sequence encoder and its column sums. The rest of the call then follows the
+  // tokeniser on the side stream (the tokeniser ends last, so the attention launches on a programmatic edge from
+  // it, with the column sums as a plain dependency) and joins this stream at the end. The first layer's queries
+  // lack their mean-pooled sequence term, which the attention kernel adds (the tcgen05 attention reads Q by TMA
+  // and keeps the one-stream order).
   const bool fork = fork_tokenizer(h, a.R, events);
   FwdArgs af = a;
   af.q_add = fork ? 1 : 0;
+  cudaStream_t t = s;  // the stream of the attention and everything after it
   if (fork) {
     if (e == cudaSuccess) e = cudaEventRecord(h->ev_fork, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
@@ -520,14 +523,15 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
     run(launch_tokenizer(af, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, h->tm_U, h->tm_tokU, a.num_sms - seq_grid,
                          false, h->side),
         kStageNames[3]);
-    if (e == cudaSuccess) e = cudaEventRecord(h->ev_join, h->side);
     run(launch_seq_mlp(af, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, s), kStageNames[1]);
-    // the column sums and the attention wait for their inputs where they are launched, not on an SM: CTAs launched
-    // early would sit on the SMs the tokeniser's CTAs need (a tokeniser CTA needs an SM's whole shared memory)
+    // the column sums wait for the encoder where they are launched, not on an SM: CTAs launched early would sit
+    // on the SMs the tokeniser's CTAs need (a tokeniser CTA needs an SM's whole shared memory)
     FwdArgs an = af;
     an.pdl = 0;
     run(launch_seq_colsum(an, s), kStageNames[2]);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_join, 0);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_join, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_join, 0);
+    t = h->side;
   } else {
     run(launch_seq_mlp(a, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, s), kStageNames[1]);
     run(launch_seq_colsum(a, s), kStageNames[2]);
@@ -539,19 +543,22 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
     if (l > 0) std::swap(zin, zout);  // layer l reads the previous output (its first 13 tokens) in place
     const bool in_is_Z = zin == h->Z;
     // the first layer's queries come out of the tokeniser
-    if (l > 0) run(launch_query(a, l, in_is_Z ? h->tm_x_Z : h->tm_x_Y, h->tm_qW[l], s), kStageNames[4]);
+    if (l > 0) run(launch_query(a, l, in_is_Z ? h->tm_x_Z : h->tm_x_Y, h->tm_qW[l], t), kStageNames[4]);
     FwdArgs al = a;  // the first layer's queries may still lack their mean-pooled term (stacked layers' have it)
     al.q_add = l == 0 ? af.q_add : 0;
-    if (l == 0 && fork) al.pdl = 0;  // (after the join: see the column sums above)
-    run(h->attn_tc ? launch_attention_tc(al, h->tm_Q, h->tm_H, zin, s) : launch_attention(al, zin, s), kStageNames[5]);
-    run(launch_tm_mlp(a, l, zin, zout, h->tm_tmW13, h->tm_tmW2, s), kStageNames[6]);
+    run(h->attn_tc ? launch_attention_tc(al, h->tm_Q, h->tm_H, zin, t) : launch_attention(al, zin, t), kStageNames[5]);
+    run(launch_tm_mlp(a, l, zin, zout, h->tm_tmW13, h->tm_tmW2, t), kStageNames[6]);
   }
   run(launch_ple_heads(a, zout == h->Z ? h->tm_full_Z : h->tm_full_Y, h->ple_int8 ? h->tm_pleW8 : h->tm_pleW,
-                       h->tm_R, h->tm_Ex, h->tm_headW1, h->B_cap, s),
+                       h->tm_R, h->tm_Ex, h->tm_headW1, h->B_cap, t),
       kStageNames[7]);
   if (a.cache_on) {
-    run(launch_cache_admit(a, h->c_claim, s), kStageNames[8]);
+    run(launch_cache_admit(a, h->c_claim, t), kStageNames[8]);
     ++n;  // (two kernels)
+  }
+  if (fork) {  // the call ends on the handle's stream
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_tail, t);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_tail, 0);
   }
   h->last_zin = zin;
   h->last_zout = zout;
@@ -875,6 +882,7 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_tail, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     cvr_destroy(h);
     cudaGetLastError();
@@ -1187,6 +1195,7 @@ void cvr_destroy(cvr_handle* h) {
   if (h->side) cudaStreamDestroy(h->side);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);
   if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->ev_tail) cudaEventDestroy(h->ev_tail);
   delete h;
 }
 
