@@ -53,8 +53,8 @@ constexpr int kErrOffsets = 2;      // bag offsets not non-decreasing
 constexpr int kErrReqIds = 4;       // request ids out of range or decreasing
 constexpr int kErrTimeout = 8;      // a bounded wait in a tensor-core kernel gave up
 constexpr int kErrDebugCap = 16;
-constexpr int kErrLayout = 32;
-constexpr int kErrSeqLens = 64;     // a sequence length outside [0, L[g]]      // a kernel found its shared-memory window misaligned and did nothing
+constexpr int kErrLayout = 32;      // a kernel found its shared-memory window misaligned and did nothing
+constexpr int kErrSeqLens = 64;     // a sequence length outside [0, L[g]]
 
 // ---- arguments of the forward pass, one copy per call ----
 struct FwdArgs {
