@@ -920,7 +920,7 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
        encode_2d(&h->tm_tmW2, h->tmW2, kHid, (uint64_t)NL * kD, kHid, 64, 128) &&
        encode_2d(&h->tm_pleW, h->pleW, kYD, kPleCols, kYD, 64, 208) &&
        encode_2d_u8(&h->tm_pleW8, h->w8blob, kYD, kPleCols, kYD, 64, 208) &&
-       encode_2d(&h->tm_headW1, h->headW1, kDE, kNT * kHH, kDE, 64, 64);
+       encode_2d(&h->tm_headW1, h->headW1, kDE, kNT * kHH, kDE, 64, 128);
   for (int l = 0; l < NL && ok; ++l)
     ok = encode_2d(&h->tm_qW[l], h->qX + (size_t)l * kG * kD * kXD, kXD, kG * kD, kXD, 64, 96);
   if (!ok) {

@@ -517,7 +517,7 @@ cudaError_t prepare_ple_kernel();
 cudaError_t prepare_sparse_kernel();
 // PLE experts, gates and r_t (four CTAs per 128-row block), then the heads of each block in its last CTA;
 // tmW = packed PLE slices [832][2048], tmR = R viewed as [2 * r_rows][256], tmEx = expert outputs [rows][768],
-// tmW1 = head first layers [2 * 128][256] (boxes of 64 x 64; the others 64 x 128; all 128-byte swizzle); launched as
+// tmW1 = head first layers [2 * 128][256] (boxes of 64 x 128 like the others; all 128-byte swizzle); launched as
 // clusters of four CTAs
 cudaError_t launch_ple_heads(const FwdArgs& a, const CUtensorMap& tmY, const CUtensorMap& tmW, const CUtensorMap& tmR,
                              const CUtensorMap& tmEx, const CUtensorMap& tmW1, int r_rows, cudaStream_t s);

@@ -10,10 +10,10 @@
 //                writes it with TMA stores into R [task][row][256] (and, when the call keeps them, the expert
 //                outputs and the gates).
 //  heads         the four CTAs of a row block form a cluster. Once all four slices of R are written (one cluster
-//                barrier), CTA n computes hidden units [64 (n % 2), +64) of task n / 2's head, ReLU(W1_t r_t +
-//                b1) on tcgen05 (M=128, N=64, K=256) with r_t read back through L2 and its W1 rows loaded into the
-//                ring, applies its half of the 128 -> 1 layer and sends the partial logits to the task's first
-//                CTA over distributed shared memory, which adds the two halves in order, the bias and the sigmoid.
+//                barrier), CTAs 2t and 2t + 1 both compute task t's hidden layer ReLU(W1_t r_t + b1) on tcgen05
+//                (M=128, N=128, K=256) with r_t read back through L2 and W1_t loaded into the ring, apply the
+//                128 -> 1 layer in two halves of 64 units added in shared memory, and finish (bias, sigmoid) rows
+//                [0, 64) and [64, 128) of the block respectively: no partial sum crosses CTAs.
 //
 // The kernel starts per row block instead of waiting for the whole Token Mixer grid: a CTA waits (bounded)
 // until the Token Mixer has counted every tile of its row block as written, so the first blocks run on the SMs
@@ -41,9 +41,10 @@ constexpr int kNK = kYD / kBK;              // 32 k-blocks
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + kEpiWarps * 32;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..9 epilogue
 constexpr int kTmemCols = 256;
-constexpr int kHN = kHH / 2;                // hidden units per CTA
+constexpr int kHN = kHH;                    // hidden units per CTA: all of its task's (the CTA pair of a task
+                                            // computes them twice and finishes half the rows each)
 constexpr int kHOffW = 4 * kATile;
-constexpr int kHBytes = 4 * kATile + 4 * kHN * kBK * 2;  // 96 KB
+constexpr int kHBytes = 4 * kATile + 4 * kHN * kBK * 2;  // 128 KB
 static_assert(kPleCols == kSlices * kBN, "four 208-column slices");
 
 // shared memory (offsets from a 1024-byte aligned base)
@@ -88,15 +89,6 @@ __device__ __forceinline__ void s8x16_to_bf16(const uint4 v, uint4& lo, uint4& h
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-// address of the same shared-memory location in CTA `rank` of the cluster
-__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
 // every thread of every CTA of the cluster arrives; memory before it (shared and global) is visible after it
 __device__ __forceinline__ void cluster_sync() {
   __syncwarp();
@@ -127,8 +119,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   CVR_TL_BEGIN(TL_PLE_HEADS);
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* sbias = reinterpret_cast<float*>(smem + S::kOffBias);  // [208]
-  float* sb1 = sbias + kBN;                                  // [64]
-  float* sw2 = sb1 + kHN;                                    // [64]
+  float* sb1 = sbias + kBN;                                  // [128]
+  float* sw2 = sb1 + kHN;                                    // [128]
   float* sscale = reinterpret_cast<float*>(smem + S::kOffScale);  // [208] (8-bit weights)
   float* plog = reinterpret_cast<float*>(smem + S::kOffPlog);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
@@ -146,14 +138,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = (int)blockIdx.x % kSlices;            // slice of this CTA (= its rank in the cluster)
   const int rb = (int)blockIdx.x / kSlices;           // row block
   const int m0 = rb * kBM;
-  const int ht = n >> 1, hh = n & 1;                  // head task and hidden half of this CTA
+  const int ht = n >> 1, hh = n & 1;                  // head task of this CTA and the half of the rows it finishes
   for (int k = threadIdx.x; k < kBN; k += blockDim.x) {  // (constants)
     sbias[k] = __ldg(a.ple_b + n * kBN + k);
     if constexpr (I8) sscale[k] = __ldg(a.ple_s8 + n * kBN + k);
   }
   for (int k = threadIdx.x; k < kHN; k += blockDim.x) {
-    sb1[k] = __ldg(a.head_b1 + ht * kHH + hh * kHN + k);
-    sw2[k] = __ldg(a.head_w2 + ht * kHH + hh * kHN + k);
+    sb1[k] = __ldg(a.head_b1 + ht * kHH + k);
+    sw2[k] = __ldg(a.head_w2 + ht * kHH + k);
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -363,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_expect_tx(h_full, kHBytes);
     for (int kb = 0; kb < 4; ++kb) {
       tma_load_2d(smem + kb * kATile, &tmR, h_full, kb * kBK, ht * r_rows + m0);
-      tma_load_2d(smem + kHOffW + kb * (kHN * kBK * 2), &tmW1, h_full, kb * kBK, ht * kHH + hh * kHN);
+      tma_load_2d(smem + kHOffW + kb * (kHN * kBK * 2), &tmW1, h_full, kb * kBK, ht * kHH);
     }
   } else if (warp == 1 && lane == 0) {
     if (mbar_wait(h_full, 0, abort_flag, a.err)) {
@@ -379,26 +371,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_drain(h_full, 0);  // (gave up: the loads land before the shared memory is released)
     }
   }
-  if (warp >= 2 && warp < 6) {
-    // ReLU(h + b1) . w2 over this CTA's 64 hidden units: the partial logit of each row goes to the task's first CTA
-    const int q = warp & 3, rl = q * 32 + lane;
+  if (warp >= 2) {
+    // ReLU(h + b1) . w2: warp group grp sums hidden units [64 grp, 64 grp + 64) of each row; the two partial logits
+    // meet in shared memory, and the rows [64 hh, 64 hh + 64) of this CTA's half are finished (bias, sigmoid)
+    const int q = warp & 3, grp = (warp - 2) >> 2, rl = q * 32 + lane;
     float part = 0.f;
     if (mbar_wait_warp(head_full, 0, abort_flag, a.err)) {
       tc_fence_after();
-      uint32_t v[kHN];
-      tmem_ld32_nowait(tbase + ((uint32_t)(q * 32) << 16), v);
-      tmem_ld32_nowait(tbase + ((uint32_t)(q * 32) << 16) + 32, v + 32);
+      uint32_t v[64];
+      tmem_ld32_nowait(tbase + ((uint32_t)(q * 32) << 16) + grp * 64, v);
+      tmem_ld32_nowait(tbase + ((uint32_t)(q * 32) << 16) + grp * 64 + 32, v + 32);
       tmem_ld_wait();
+      const float* b1 = sb1 + grp * 64;
+      const float* w2 = sw2 + grp * 64;
 #pragma unroll
-      for (int j = 0; j < kHN; ++j) part = fmaf(fmaxf(__uint_as_float(v[j]) + sb1[j], 0.f), sw2[j], part);
+      for (int j = 0; j < 64; ++j) part = fmaf(fmaxf(__uint_as_float(v[j]) + b1[j], 0.f), w2[j], part);
     }
-    st_cluster_f32(peer_addr(smem_u32(plog + hh * kBM + rl), (uint32_t)(2 * ht)), part);
-  }
-  cluster_sync();
-  if (hh == 0 && warp >= 2 && warp < 6) {
-    const int q = warp & 3, rl = q * 32 + lane, row = m0 + rl;
-    const float logit = (plog[rl] + plog[kBM + rl]) + a.head_b2[ht];
-    if (row < a.B) a.out[(int64_t)row * kNT + ht] = 1.f / (1.f + expf(-logit));
+    plog[grp * kBM + rl] = part;
+    __syncwarp();
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+    const int row = m0 + rl;
+    if (grp == 0 && (rl >> 6) == hh) {
+      const float logit = (plog[rl] + plog[kBM + rl]) + a.head_b2[ht];
+      if (row < a.B) a.out[(int64_t)row * kNT + ht] = 1.f / (1.f + expf(-logit));
+    }
   }
   if (threadIdx.x == 64) bulk_wait_read<0>();  // (the stores' shared-memory source is read before the CTA exits)
   tc_fence_before();
