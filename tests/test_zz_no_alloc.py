@@ -49,6 +49,26 @@ def test_noalloc_prediction_matches_scoring_entry_point(name, kw):
         _close(out.cpu().numpy().astype(np.float64), ref, f"{name} call {call}")
 
 
+@pytest.mark.parametrize("name,kw", [
+    ("tiny", dict(n_req=3, cand_per_req=[150, 2, 33])),
+    ("prod", dict(n_req=2)),
+])
+def test_noalloc_prediction_on_8bit_weights(name, kw):
+    """With CVR_OPT_PLE_INT8 both entry points run the PLE on the 8-bit rows: the same pCVR within tolerance."""
+    import torch
+    import cvr_ranking_model_gb300 as cvr
+    wl = synth.make_workload(name, **kw)
+    w = synth.make_weights(wl.n_layers, wl.seed, bias_scale=0.02)
+    g = GpuRun(wl, w, debug=False)
+    g.sc.set_option(cvr.OPT_PLE_INT8, 1)
+    g.run()
+    ref = g.out()
+    y = _y_of_last_call(g)
+    out = torch.full((wl.n_cand, 2), float("nan"), dtype=torch.float32, device="cuda:0")
+    g.sc.predict_noalloc(wl.n_cand, y.data_ptr(), out.data_ptr())
+    _close(out.cpu().numpy().astype(np.float64), ref, f"{name} int8")
+
+
 def test_noalloc_rejects_oversize_and_misaligned_and_accepts_empty():
     import torch
     import cvr_ranking_model_gb300 as cvr
