@@ -111,7 +111,7 @@ struct cvr_handle {
   size_t stage_bytes = 0;
   // tensor maps
   CUtensorMap tm_seqW13, tm_seqW2, tm_tokI, tm_tokU, tm_qW[kMaxLayers], tm_tmW13, tm_tmW2, tm_pleW, tm_pleW8, tm_headW1;
-  CUtensorMap tm_Xs, tm_I, tm_U, tm_x_Z, tm_x_Y, tm_full_Z, tm_full_Y, tm_Q, tm_H, tm_R, tm_Ex;
+  CUtensorMap tm_Xs, tm_I, tm_U, tm_U32, tm_x_Z, tm_x_Y, tm_full_Z, tm_full_Y, tm_Q, tm_H, tm_R, tm_Ex;
   // graphs, profiling
   bool use_graph = true, profile = false, pdl = true;
   bool keep_stages = false;  // the PLE also writes the expert outputs and gates (for cvr_debug_stage)
@@ -329,6 +329,7 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   bool ok = encode_2d(&h->tm_Xs, h->Xs, kD, (uint64_t)seq_rows, kD, 64, 128) &&
             encode_2d(&h->tm_I, h->I, kID, B_cap, kID, 64, 128) &&
             encode_2d(&h->tm_U, h->U, kUD, R_pad, kUD, 64, 128) &&
+            encode_2d(&h->tm_U32, h->U, kUD, R_pad, kUD, 64, 32) &&
             encode_2d(&h->tm_x_Z, h->Z, kXD, B_cap, kYD, 64, 128) &&
             encode_2d(&h->tm_x_Y, h->Y, kXD, B_cap, kYD, 64, 128) &&
             encode_2d(&h->tm_full_Z, h->Z, kYD, B_cap, kYD, 64, 128) &&
@@ -520,12 +521,12 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
     if (e == cudaSuccess) e = cudaEventRecord(h->ev_fork, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
     // (without a programmatic edge: its CTAs must not queue ahead of the encoder's for the SMs the gather frees)
-    run(launch_tokenizer(af, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, h->tm_U, h->tm_tokU, a.num_sms - seq_grid,
+    run(launch_tokenizer(af, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, h->tm_U, h->tm_U32, h->tm_tokU, a.num_sms - seq_grid,
                          false, h->side),
         kStageNames[3]);
     run(launch_seq_mlp(af, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, s), kStageNames[1]);
     // the column sums wait for the encoder where they are launched, not on an SM: CTAs launched early would sit
-    // on the SMs the tokeniser's CTAs need (a tokeniser CTA needs an SM's whole shared memory)
+    // on the SMs the tokeniser's CTAs need (a tokeniser CTA needs most of an SM's shared memory)
     FwdArgs an = af;
     an.pdl = 0;
     run(launch_seq_colsum(an, s), kStageNames[2]);
@@ -535,7 +536,8 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
   } else {
     run(launch_seq_mlp(a, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, s), kStageNames[1]);
     run(launch_seq_colsum(a, s), kStageNames[2]);
-    run(launch_tokenizer(a, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, h->tm_U, h->tm_tokU, 0, true, s), kStageNames[3]);
+    run(launch_tokenizer(a, h->tm_I, h->tm_tokI, h->tm_full_Z, h->tm_Q, h->tm_U, h->tm_U32, h->tm_tokU, 0, true, s),
+        kStageNames[3]);
   }
   bf16* zin = h->Z;
   bf16* zout = h->Y;

@@ -503,12 +503,16 @@ cudaError_t launch_seq_mlp(const FwdArgs& a, const CUtensorMap& tmXs, const CUte
 // the Token Mixer of layer `layer`: zin [B][16][128] -> yout
 cudaError_t launch_tm_mlp(const FwdArgs& a, int layer, const __nv_bfloat16* zin, __nv_bfloat16* yout,
                           const CUtensorMap& tmW13, const CUtensorMap& tmW2, cudaStream_t s);
-// the tokeniser GEMM (13 tokens + the first layer's queries, 2048 packed columns; its first M-tiles compute the
-// user half xu from U = tmU with the user weights tmWu) on at most max_grid CTAs (0: one per SM); pdl = false
-// launches it after the previous work in the stream has completed (the first kernel of the side stream)
+// the tokeniser GEMM (13 tokens + the first layer's queries, 2048 packed columns) on at most max_grid CTAs (0: one
+// per SM). The user half xu comes from U with the user weights tmWu: with at most 32 requests every CTA computes
+// its own column tile's slice (tmU32: U in boxes of 32 rows, tmWu as the A operand); else the launch's first
+// M-tiles compute it (tmU: boxes of 128 rows). pdl = false launches it after the previous work in the stream has
+// completed (the first kernel of the side stream).
 cudaError_t launch_tokenizer(const FwdArgs& a, const CUtensorMap& tmI, const CUtensorMap& tmW, const CUtensorMap& tmZo,
-                             const CUtensorMap& tmQo, const CUtensorMap& tmU, const CUtensorMap& tmWu, int max_grid,
-                             bool pdl, cudaStream_t s);
+                             const CUtensorMap& tmQo, const CUtensorMap& tmU, const CUtensorMap& tmU32,
+                             const CUtensorMap& tmWu, int max_grid, bool pdl, cudaStream_t s);
+// Requests up to which each tokeniser CTA computes its own column tile's user half.
+constexpr int kTokOwnXuMaxR = 32;
 cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, const CUtensorMap& tmW, cudaStream_t s);
 cudaError_t launch_attention(const FwdArgs& a, __nv_bfloat16* zin, cudaStream_t s);
 cudaError_t launch_attention_tc(const FwdArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmH, __nv_bfloat16* zin,

@@ -425,6 +425,280 @@ __global__ void __launch_bounds__(96 + NEPI * 32, 1)
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// The tokeniser for batches of at most kLuMaxR requests. The grid is a multiple of the 16 column tiles, so each
+// CTA owns one column tile n0 for all of its row-tiles:
+//  - its weight slice Wtok_item[n0, n0 + 128) (K = 256, 64 KB) is loaded once and stays in shared memory; only the
+//    A k-blocks (16 KB) stream through the stage ring (the main loop is bound by shared-memory bandwidth, not by
+//    the tensor pipe, so every byte that does not pass through shared memory counts);
+//  - it computes the user half of its column tile for every request itself, transposed:
+//    xu^T = Wu[n0 ..] . U^T (M = 128 output columns, N = 32 requests, K = 256) into 32 TMEM columns, adds the bias
+//    (and the first layer's mean-pool term qb when the attention does not add it) and keeps it in shared memory,
+//    so no item tile waits on another CTA (iQIYI 3.4.5: the user side once per request, here once per CTA). Its
+//    MMAs follow the first row-tile's, whose operands are loaded first.
+// Warp 0: TMA; warp 1: MMA issue; warps 2..2+NEPI-1: epilogue; the last warp stages each row-tile's request ids.
+// Output: one 128B-swizzled staging tile stored by TMA (it holds the user rows until the user half is done).
+constexpr int kLuMaxR = kTokOwnXuMaxR;
+constexpr int kLuStages = 7;
+constexpr int kLuEpi = 8;
+constexpr int kLuUBytes = kLuMaxR * kBK * 2;  // one k-block of the user rows: [32][64] bf16
+
+struct LuSmem {  // byte offsets from the 1024-aligned base
+  static constexpr int kA = 0;                                  // kLuStages x [128][64] bf16
+  static constexpr int kB = kA + kLuStages * kATile;            // the CTA's weight slice: 4 x [128][64] bf16
+  static constexpr int kOut = kB + (kID / kBK) * kATile;        // staging [128][128] bf16 (two 64-column boxes);
+                                                                 // first the user rows: 4 x [32][64] bf16
+  static constexpr int kXu = kOut + kBM * 128 * 2;              // xu + bias (+ qb) [kLuMaxR][128] fp32
+  static constexpr int kReq = kXu + kLuMaxR * 128 * 4;          // request ids of two row-tiles [2][128] int32
+  static constexpr int kBar = kReq + 2 * kBM * 4;
+  static constexpr int kNBar = 2 * kLuStages + 2 * 4 + 1 + 2 + 2;
+  static constexpr int kBytes = 1024 + kBar + kNBar * 8 + 16;
+};
+static_assert(LuSmem::kBytes <= 232448, "shared memory budget of one CTA");
+static_assert((kUD / kBK) * kLuUBytes <= kBM * 128 * 2, "the user rows fit the staging tile");
+
+template <int NEPI>
+__global__ void __launch_bounds__(96 + NEPI * 32, 1)
+    tokenize_lu_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmZo,
+                       const __grid_constant__ CUtensorMap tmQo, const __grid_constant__ CUtensorMap tmU32,
+                       const __grid_constant__ CUtensorMap tmWu) {
+  extern __shared__ uint8_t smem_raw[];
+  CVR_TL_BEGIN(TL_TOKENIZER);
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int BN = 128, NCHUNK = BN / 32, NGRP = NEPI / 4, NMY = NCHUNK / NGRP, NACC = 4, nk = kID / kBK;
+  static_assert(NEPI == 8 && 16 * NGRP == kLuMaxR, "each epilogue warpgroup drains 16 requests of the user half");
+  static_assert(kUD == kID, "the user half and the item tiles share the k-block count");
+  uint8_t* sA = smem + LuSmem::kA;
+  uint8_t* sB = smem + LuSmem::kB;
+  uint8_t* sOut = smem + LuSmem::kOut;
+  uint8_t* sU = sOut;  // (until the user half's MMAs are done)
+  float* sXu = reinterpret_cast<float*>(smem + LuSmem::kXu);
+  int* sReq = reinterpret_cast<int*>(smem + LuSmem::kReq);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + LuSmem::kBar);
+  uint64_t* empty = full + kLuStages;
+  uint64_t* acc_full = empty + kLuStages;
+  uint64_t* acc_empty = acc_full + NACC;
+  uint64_t* bres_full = acc_empty + NACC;  // the weight slice landed
+  uint64_t* req_full = bres_full + 1;      // request ids of row-tile buffer b staged
+  uint64_t* req_empty = req_full + 2;      // ... and read by every epilogue warp
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(req_empty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int M = a.B;
+  constexpr int tiles_n = kTokN / BN;
+  const int n_tiles = (M + kBM - 1) / kBM * tiles_n;
+  const int n0 = (int)(blockIdx.x % tiles_n) * BN;  // (gridDim.x % tiles_n == 0)
+  // Jobs in ring and MMA order: the first row-tile (if any), the user half, the other row-tiles. Accumulator use u
+  // (buffer u % NACC): the user half u = 0, the k-th row-tile u = k + 1.
+  const int n_items = (int)blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int xu_job = n_items > 0 ? 1 : 0;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kLuStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < NACC; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], NEPI);
+    }
+    mbar_init(bres_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&req_full[i], 1);
+      mbar_init(&req_empty[i], NEPI);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmU32);
+    tma_prefetch_desc(&tmWu);
+  }
+  if (warp == 1) tmem_alloc(tslot, NACC * BN);
+  tc_fence_before();
+  cta_sync();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  pdl_trigger();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // the weights are constant: the slice's copies start before the wait for the previous kernel
+      mbar_expect_tx(bres_full, nk * kATile);
+      for (int kb = 0; kb < nk; ++kb) tma_load_2d(sB + kb * kATile, &tmB, bres_full, kb * kBK, n0);
+      pdl_wait();
+      CVR_TL_WAITED();
+      int kc = 0;
+      bool ok = true;
+      for (int job = 0; job < n_items + 1 && ok; ++job) {
+        const bool xu = job == xu_job;
+        const int m0 = ((int)blockIdx.x + (job - (job > xu_job)) * (int)gridDim.x) / tiles_n * kBM;
+        for (int kb = 0; kb < nk; ++kb, ++kc) {
+          const int s = kc % kLuStages;
+          if (kc >= kLuStages && !mbar_wait(&empty[s], ((kc / kLuStages) & 1) ^ 1, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          if (xu) {  // A = Wu rows [n0, n0 + 128), B = U rows [0, 32)
+            mbar_expect_tx(&full[s], kATile + kLuUBytes);
+            tma_load_2d(sA + s * kATile, &tmWu, &full[s], kb * kBK, n0);
+            tma_load_2d(sU + kb * kLuUBytes, &tmU32, &full[s], kb * kBK, 0);
+          } else {
+            mbar_expect_tx(&full[s], kATile);
+            tma_load_2d(sA + s * kATile, &tmA, &full[s], kb * kBK, m0);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t id_xu = idesc_bf16(kBM, kLuMaxR), id_it = idesc_bf16(kBM, BN);
+      bool ok = mbar_wait(bres_full, 0, abort_flag, a.err);
+      int kc = 0;
+      for (int job = 0; job < n_items + 1 && ok; ++job) {
+        const bool xu = job == xu_job;
+        const int u = xu ? 0 : job + (job < xu_job), buf = u % NACC;
+        if (u >= NACC && !mbar_wait(&acc_empty[buf], ((u / NACC) & 1) ^ 1, abort_flag, a.err)) break;
+        const uint32_t dacc = tbase + buf * BN;
+        for (int kb = 0; kb < nk; ++kb, ++kc) {
+          const int s = kc % kLuStages;
+          if (!mbar_wait(&full[s], (kc / kLuStages) & 1, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t aa = smem_u32(sA + s * kATile);
+          const uint32_t bb = xu ? smem_u32(sU + kb * kLuUBytes) : smem_u32(sB + kb * kATile);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            tc_mma(dacc, sdesc_sw128(aa + k * 32), sdesc_sw128(bb + k * 32), xu ? id_xu : id_it, (kb | k) != 0);
+          tc_commit(&empty[s]);
+        }
+        if (ok) tc_commit(&acc_full[buf]);
+      }
+    }
+  } else if (warp == 2 + NEPI) {
+    // ---- request ids of each row-tile (clamped into [0, R); the sparse kernel reports bad ones), one tile ahead
+    pdl_wait();
+    int rq[kBM / 32];
+    auto load_req = [&](int t) {
+      const int m0 = (t / tiles_n) * kBM;
+#pragma unroll
+      for (int k = 0; k < kBM / 32; ++k) {
+        const int row = m0 + lane + 32 * k;
+        rq[k] = row < M ? a.req_ids[row] : 0;
+      }
+    };
+    int tile = blockIdx.x, j = 0;
+    if (tile < n_tiles) load_req(tile);
+    for (; tile < n_tiles; tile += gridDim.x, ++j) {
+      const int b = j & 1;
+      if (j >= 2 && !mbar_wait_warp(&req_empty[b], ((j >> 1) & 1) ^ 1, abort_flag, a.err)) break;
+#pragma unroll
+      for (int k = 0; k < kBM / 32; ++k) sReq[b * kBM + lane + 32 * k] = min(max(rq[k], 0), a.R - 1);
+      __syncwarp();
+      if (tile + (int)gridDim.x < n_tiles) load_req(tile + gridDim.x);  // (in flight until the next tile)
+      if (lane == 0) mbar_arrive(&req_full[b]);
+    }
+  } else {
+    const int q = warp & 3;           // TMEM lane quarter this warp may access
+    const int grp = (warp - 2) >> 2;  // chunk group
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    // user half: TMEM lane n = output column n0 + n, column r = request r; this warpgroup drains requests
+    // [16 grp, 16 grp + 16). Its addends are loaded before the wait. Every warp arrives and meets at the barrier,
+    // whatever its wait returned.
+    const int n = q * 32 + lane, nb = n0 + n;
+    const float bias = __ldg(a.tok_b + nb);
+    pdl_wait();  // (qb, when it is added here, comes from the column-sum kernel)
+    const bool addq = nb >= kXD && !a.q_add;
+    float qv[16];
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+      const int r = grp * 16 + x;
+      qv[x] = addq && r < a.R ? __ldg(a.qb + (int64_t)r * (kG * kD) + (nb - kXD)) : 0.f;
+    }
+    bool ok = mbar_wait_warp(&acc_full[0], 0, abort_flag, a.err);
+    if (ok) {
+      tc_fence_after();
+      uint32_t v[16];
+      tmem_ld16_nowait(tbase + lane_off + grp * 16, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int x = 0; x < 16; ++x) {
+        const int r = grp * 16 + x;
+        float t = __uint_as_float(v[x]) + bias;
+        if (addq) t += qv[x];
+        if (r < a.R) sXu[r * BN + n] = t;
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&acc_empty[0]);
+    epi_bar<NEPI>();
+    int u = 1, j = 0;
+    for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x, ++u, ++j) {
+      const int m0 = (tile / tiles_n) * kBM;
+      const int rl = q * 32 + lane, row = m0 + rl;
+      const bool live = row < M;
+      const int buf = u % NACC, b = j & 1;
+      if (!mbar_wait_warp(&req_full[b], (j >> 1) & 1, abort_flag, a.err) ||
+          !mbar_wait_warp(&acc_full[buf], (u / NACC) & 1, abort_flag, a.err))
+        break;
+      tc_fence_after();
+      const float* xr = sXu + sReq[b * kBM + rl] * BN;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&req_empty[b]);
+      // the previous tile's TMA store has finished reading the staging tile (before the first tile, the user half's
+      // MMAs, which read the user rows kept there, have completed: its accumulator was drained above)
+      if (threadIdx.x == 64) bulk_wait_read<0>();
+      epi_bar<NEPI>();
+#pragma unroll
+      for (int m = 0; m < NMY; ++m) {
+        const int c = grp + m * NGRP;
+        float v[32];
+        tmem_ld32(tbase + lane_off + buf * BN + c * 32, v);
+        if (m == NMY - 1) {  // the accumulator is read: the MMAs may reuse it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+        if (!live) continue;
+        const float4* ap = reinterpret_cast<const float4*>(xr + c * 32);
+        // columns [32c, 32c + 32) of row rl into the staging tile: box c/2, 16-byte chunks 4 (c%2) + j4, swizzled
+        uint8_t* rowp = sOut + (c >> 1) * (kBM * 128) + rl * 128;
+#pragma unroll
+        for (int j4 = 0; j4 < 4; ++j4) {
+          const float4 t0 = ap[2 * j4], t1 = ap[2 * j4 + 1];
+          uint4 p;
+          p.x = pack_bf16(v[8 * j4 + 0] + t0.x, v[8 * j4 + 1] + t0.y);
+          p.y = pack_bf16(v[8 * j4 + 2] + t0.z, v[8 * j4 + 3] + t0.w);
+          p.z = pack_bf16(v[8 * j4 + 4] + t1.x, v[8 * j4 + 5] + t1.y);
+          p.w = pack_bf16(v[8 * j4 + 6] + t1.z, v[8 * j4 + 7] + t1.w);
+          *reinterpret_cast<uint4*>(rowp + ((((c & 1) * 4 + j4) ^ (rl & 7)) << 4)) = p;
+        }
+      }
+      fence_proxy_async_smem();
+      epi_bar<NEPI>();
+      if (threadIdx.x == 64) {
+        const bool qcols = n0 >= kXD;
+#pragma unroll
+        for (int bx = 0; bx < BN / 64; ++bx)
+          tma_store_2d(qcols ? &tmQo : &tmZo, sOut + bx * (kBM * 128), (qcols ? n0 - kXD : n0) + bx * 64, m0);
+        bulk_commit();
+      }
+    }
+    // (the staging tile has been read before the CTA exits; the stores complete with the grid)
+    if (threadIdx.x == 64) bulk_wait_read<0>();
+  }
+  tc_fence_before();
+  cta_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, NACC * BN);
+  }
+}
+
 template <int BN, int STAGES, int EPI, int NEPI>
 cudaError_t prepare_gemm() {
   return cudaFuncSetAttribute(gemm_kernel<BN, STAGES, EPI, NEPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -451,14 +725,25 @@ constexpr int kQryBN = 96, kQryStages = 6, kQryEpi = 8;
 cudaError_t prepare_gemm_kernels() {
   cudaError_t e = prepare_gemm<kTokBN, kTokStages, EPI_TOKENIZE, kTokEpi>();
   if (e == cudaSuccess) e = prepare_gemm<kQryBN, kQryStages, EPI_QUERY, kQryEpi>();
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tokenize_lu_kernel<kLuEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize, LuSmem::kBytes);
   return e;
 }
 
 cudaError_t launch_tokenizer(const FwdArgs& a, const CUtensorMap& tmI, const CUtensorMap& tmW, const CUtensorMap& tmZo,
-                             const CUtensorMap& tmQo, const CUtensorMap& tmU, const CUtensorMap& tmWu, int max_grid,
-                             bool pdl, cudaStream_t s) {
+                             const CUtensorMap& tmQo, const CUtensorMap& tmU, const CUtensorMap& tmU32,
+                             const CUtensorMap& tmWu, int max_grid, bool pdl, cudaStream_t s) {
   static_assert(kXD % kTokBN == 0 && kTokN % kTokBN == 0, "token and query columns fall in separate tiles");
   static_assert(kTokBN % 64 == 0 && gemm_smem_bytes<kTokBN, kTokStages, EPI_TOKENIZE>() <= 232448, "staging fits");
+  constexpr int tiles_n = kTokN / 128;
+  const int cap = max_grid > 0 && max_grid < a.num_sms ? max_grid : a.num_sms;
+  if (a.R <= kLuMaxR && cap >= tiles_n) {  // each CTA one column tile, its own user half
+    const int tiles = (a.B + kBM - 1) / kBM * tiles_n;
+    int grid = tiles < cap ? tiles : cap;
+    grid -= grid % tiles_n;
+    return launch_kernel(tokenize_lu_kernel<kLuEpi>, dim3(grid), dim3(96 + kLuEpi * 32), LuSmem::kBytes, s,
+                         pdl && a.pdl != 0, a, tmI, tmW, tmZo, tmQo, tmU32, tmWu);
+  }
   return launch_gemm<kTokBN, kTokStages, EPI_TOKENIZE, kTokEpi>(a, tmI, tmW, tmZo, tmQo, tmU, tmWu, a.B, kTokN, kID, 0,
                                                                 (a.R + kBM - 1) / kBM, s, max_grid, pdl);
 }

@@ -120,6 +120,8 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
   if (a.xu_ready)  // and so do the tokeniser's user row-tile flags
     for (int i = blockIdx.x * kSparseThreads + tid; i < (a.R + 127) / 128 * (kTokN / 128); i += gridDim.x * kSparseThreads)
       a.xu_ready[i] = 0u;
+  if (a.cs_count)  // and the mean pool's per-(request, group) counters (also zeroed by whoever completes one)
+    for (int i = blockIdx.x * kSparseThreads + tid; i < a.R * kG; i += gridDim.x * kSparseThreads) a.cs_count[i] = 0u;
   // request ids: in range and non-decreasing (checked once per candidate), and copied to the workspace for
   // the later kernels (the caller's array may be host memory read over the C2C link)
   for (int64_t cand = (int64_t)blockIdx.x * kSparseThreads + tid; cand < a.B;

@@ -120,6 +120,17 @@ def test_ragged_requests_and_odd_lengths():
     _check_full(wl, w, stages=True)
 
 
+@pytest.mark.parametrize("n_req", [32, 33, 150])
+def test_request_counts_around_the_tokeniser_user_paths(n_req):
+    # up to 32 requests each tokeniser CTA computes the user half of its own column tile for every request;
+    # above that the user rows are row-tiles of the launch that the item tiles wait for (150 requests: two)
+    cand = [1 + (r * 7) % 5 for r in range(n_req)]
+    wl = synth.make_workload("tiny", n_req=n_req, cand_per_req=cand, seq_len=(5, 9, 17), user_rows=5000,
+                             item_rows=5000)
+    w = synth.make_weights(wl.n_layers, wl.seed, bias_scale=0.02)
+    _check_full(wl, w, stages=True)
+
+
 def test_two_layers_small():
     wl = synth.make_workload("deep", n_req=3, n_cand=40, seq_len=(17, 33, 65), user_rows=1000, item_rows=1000,
                              seq_rows=10_000)
