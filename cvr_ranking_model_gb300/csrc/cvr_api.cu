@@ -525,11 +525,9 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
                          false, h->side),
         kStageNames[3]);
     run(launch_seq_mlp(af, h->tm_Xs, h->tm_seqW13, h->tm_seqW2, seq_tiles, s), kStageNames[1]);
-    // the column sums wait for the encoder where they are launched, not on an SM: CTAs launched early would sit
-    // on the SMs the tokeniser's CTAs need (a tokeniser CTA needs most of an SM's shared memory)
-    FwdArgs an = af;
-    an.pdl = 0;
-    run(launch_seq_colsum(an, s), kStageNames[2]);
+    // the column sums follow the encoder on a programmatic edge, which the encoder opens only as its last tiles
+    // end: their CTAs wait for the SMs the encoder leaves, not on the SMs the tokeniser's CTAs need
+    run(launch_seq_colsum(af, s), kStageNames[2]);
     if (e == cudaSuccess) e = cudaEventRecord(h->ev_join, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_join, 0);
     t = h->side;

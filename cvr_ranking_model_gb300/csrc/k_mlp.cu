@@ -135,7 +135,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   cta_sync();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  pdl_trigger();
+  // The Token Mixer lets the next kernel (the PLE, which starts row block by row block) launch at once. The sequence
+  // encoder lets its dependents launch only when its epilogue has finished its tiles: their CTAs then take the SMs
+  // this kernel leaves, instead of SMs that a kernel on another stream is about to need.
+  if (MODE == MODE_TM) pdl_trigger();
   const int n_my = (int)blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / n_cta + 1 : 0;
 
   if (warp == 0) {
@@ -497,6 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && !kDefer) ok = finish(i);
     }
     if (ok && kDefer && n_my > 0) finish(n_my - 1);
+    if (MODE == MODE_SEQ) pdl_trigger();
   }
   tc_fence_before();
   cta_sync();

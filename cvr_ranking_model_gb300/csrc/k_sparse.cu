@@ -466,27 +466,30 @@ __global__ void __launch_bounds__(256) cache_fill_kernel(const __grid_constant__
   }
 }
 
-// Column sums of H over chunks of kCsRows positions; grid (chunks, G, R), 256 threads. A (request, group) that
+// Column sums of H over chunks of kCsRows positions; grid (chunks, G, R), 512 threads. A (request, group) that
 // fits one chunk (every one at the usual lengths) is summed by one block, which goes on directly; longer
 // sequences write one partial sum per chunk and the last of their blocks -- found with a counter, nobody waits --
 // adds the partials up in chunk order. That block then forms the mean-pooled sequence vector m_g (iQIYI 3.2.3,
 // Query Decoding item 1: mean over positions of the encoded states) and that group's per-request query term
 // for every layer, qb[l][r][g*128 + n] = q_b[l][g*128 + n] + sum_k Wq[l][g][n][1664 + k] * m_g[k].
 constexpr int kCsRows = 512;
-constexpr int kCsThreads = 256;
+constexpr int kCsThreads = 512;
 
 __global__ void __launch_bounds__(kCsThreads) seq_colsum_kernel(const __grid_constant__ FwdArgs a) {
   CVR_TL_BEGIN(TL_COLSUM);
   const int chunk = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
   const int L = a.L[g];
   const int t = threadIdx.x;
-  // the mean-pool weight rows of this group (every layer) go to L2 while the encoder still runs
-  if (chunk == 0 && r == 0 && t < kD)
-    for (int l = 0; l < a.n_layers; ++l) {
-      const uint8_t* wrow = reinterpret_cast<const uint8_t*>(a.qm + (((int64_t)l * kG + g) * kD + t) * kD);
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(wrow));
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(wrow + 128));
-    }
+  // matvec thread t: output row n = t % 128, quarter t / 128 of K. The first layer's weights are constant: they
+  // load while the encoder still runs
+  const int nrow = t & (kD - 1), quarter = t >> 7;
+  auto load_w = [&](uint4* wv, int l) {
+    const uint4* wrow = reinterpret_cast<const uint4*>(a.qm + (((int64_t)l * kG + g) * kD + nrow) * kD + quarter * 32);
+#pragma unroll
+    for (int x = 0; x < 4; ++x) wv[x] = __ldg(wrow + x);
+  };
+  uint4 w0[4];
+  load_w(w0, 0);
   pdl_trigger();
   pdl_wait();
   if (t == 0) CVR_TL_WAITED();
@@ -497,15 +500,15 @@ __global__ void __launch_bounds__(kCsThreads) seq_colsum_kernel(const __grid_con
   if (chunk >= chunks) return;
   const __nv_bfloat16* base = a.H + (a.goff[g] + (int64_t)r * L) * kD;
   const int l0 = chunk * kCsRows, l_end = min(len, l0 + kCsRows);
-  // thread t sums columns [8 (t % 16), +8) over rows l0 + t/16 + 16 i, eight 16-byte loads in flight, in a fixed
+  // thread t sums columns [8 (t % 16), +8) over rows l0 + t/16 + 32 i, eight 16-byte loads in flight, in a fixed
   // order (the result does not depend on timing)
   const int cg = t & 15, rg = t >> 4;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int lb = l0 + rg; lb < l_end; lb += 16 * 8) {
+  for (int lb = l0 + rg; lb < l_end; lb += 32 * 8) {
     uint4 v[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int l = lb + 16 * i;
+      const int l = lb + 32 * i;
       v[i] = l < l_end ? __ldg(reinterpret_cast<const uint4*>(base + (int64_t)l * kD) + cg) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
@@ -518,9 +521,9 @@ __global__ void __launch_bounds__(kCsThreads) seq_colsum_kernel(const __grid_con
       }
     }
   }
-  __shared__ float part[16][kD];
+  __shared__ float part[32][kD];
   __shared__ float m[kD];
-  __shared__ float gpart[2][kD];
+  __shared__ float gpart[4][kD];
   __shared__ int last;
 #pragma unroll
   for (int e = 0; e < 8; ++e) part[rg][cg * 8 + e] = acc[e];
@@ -528,7 +531,7 @@ __global__ void __launch_bounds__(kCsThreads) seq_colsum_kernel(const __grid_con
   float colsum = 0.f;
   if (t < kD) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) colsum += part[j][t];
+    for (int j = 0; j < 32; ++j) colsum += part[j][t];
   }
   unsigned* cnt = a.cs_count + r * kG + g;
   if (chunks > 1) {
@@ -547,28 +550,31 @@ __global__ void __launch_bounds__(kCsThreads) seq_colsum_kernel(const __grid_con
   }
   if (t < kD) m[t] = len > 0 ? colsum / (float)len : 0.f;
   cta_sync();
-  // thread t: output row n = t % 128, half of K = t / 128; the two halves are added in a fixed order
-  const int nrow = t & (kD - 1), half = t >> 7;
+  // the four quarters of K are added in a fixed order
   for (int l = 0; l < a.n_layers; ++l) {
-    uint4 wv[8];
-    const uint4* wrow = reinterpret_cast<const uint4*>(a.qm + (((int64_t)l * kG + g) * kD + nrow) * kD + half * 64);
+    uint4 wv[4];
+    if (l == 0) {
 #pragma unroll
-    for (int x = 0; x < 8; ++x) wv[x] = __ldg(wrow + x);
-    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int x = 0; x < 4; ++x) wv[x] = w0[x];
+    } else {
+      load_w(wv, l);
+    }
+    float s2[2] = {0.f, 0.f};
 #pragma unroll
-    for (int x = 0; x < 8; ++x) {
+    for (int x = 0; x < 4; ++x) {
       const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&wv[x]);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        s4[q] += __low2float(e[q]) * m[half * 64 + x * 8 + 2 * q];
-        s4[q] += __high2float(e[q]) * m[half * 64 + x * 8 + 2 * q + 1];
+        const int k = quarter * 32 + x * 8 + 2 * q;
+        s2[q & 1] += __low2float(e[q]) * m[k];
+        s2[q & 1] += __high2float(e[q]) * m[k + 1];
       }
     }
-    gpart[half][nrow] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    gpart[quarter][nrow] = s2[0] + s2[1];
     cta_sync();
     if (t < kD)
       a.qb[((int64_t)l * a.R + r) * (kG * kD) + g * kD + t] =
-          __ldg(a.q_b + l * kG * kD + g * kD + t) + (gpart[0][t] + gpart[1][t]);
+          __ldg(a.q_b + l * kG * kD + g * kD + t) + ((gpart[0][t] + gpart[1][t]) + (gpart[2][t] + gpart[3][t]));
     cta_sync();
   }
 }
@@ -579,6 +585,11 @@ cudaError_t prepare_sparse_kernel() {
   cudaError_t e = cudaFuncSetAttribute(sparse_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSparseSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(sparse_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSparseSmem);
+  // the column sums start on SMs the encoder has just left, which run with the largest shared-memory split: ask
+  // for the same split, so that no SM has to change it first
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(seq_colsum_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
   return e;
 }
 
