@@ -6,8 +6,9 @@
 // w / 4 and head w % 4 for the whole sequence, so its online-softmax state never needs merging within the
 // CTA. A group longer than 512 positions is split over several CTAs (when the tile holds one request); the
 // last of them to finish -- found with a counter, nobody waits -- merges their states. All warps
-// share the K/V chunks of 64 positions, staged by the whole CTA with cp.async into a double buffer; every
-// K/V row is read once per 32 candidates. Logits and P.V run on mma.sync m16n8k16 (bf16 in, fp32
+// share the K/V chunks of 64 positions, staged by the whole CTA with cp.async into a ring of 5 slots with
+// 3 chunks in flight ahead of the one in use (a 200-position sequence is in flight at once); every K/V row
+// is read once per 32 candidates. Logits and P.V run on mma.sync m16n8k16 (bf16 in, fp32
 // accumulate) with the softmax on exp2, and the decoded tokens are written straight into slots 13..15 of
 // the Token Mixer input.
 #include "cvr_internal.cuh"
@@ -21,7 +22,10 @@ constexpr int kWarps = 8;
 constexpr int kChunk = 64;                        // positions per step
 constexpr int kKStride = kD + 8;                  // padded smem row (272 B): conflict-free fragment loads
 constexpr int kBufBytes = kChunk * kKStride * 2;  // 17408 B
-constexpr int kSmemBytes = 2 * kBufBytes;         // 34816 B
+constexpr int kNBuf = 5;                          // ring slots
+constexpr int kAhead = 3;                         // chunks in flight ahead of the one in use
+constexpr int kSmemBytes = kNBuf * kBufBytes;     // 87040 B: two CTAs per SM
+static_assert(kAhead <= kNBuf - 2, "a refilled slot was read two chunks ago, before the last barrier");
 static_assert(kChunk == kAttnChunk, "split sizing uses the same chunk");
 
 __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
@@ -43,14 +47,15 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_b
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
-__global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_constant__ FwdArgs a,
+__global__ void __launch_bounds__(kWarps * 32, 2) attention_kernel(const __grid_constant__ FwdArgs a,
                                                                 __nv_bfloat16* __restrict__ zin) {
   extern __shared__ __align__(16) uint8_t smem[];
   CVR_TL_BEGIN(TL_ATTENTION);
@@ -62,7 +67,7 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
   const int L = a.L[g];
   const int R = a.R, B = a.B;
   const int n_split = split_count(L);  // this group's splits of the sequence
-  __nv_bfloat16* buf = reinterpret_cast<__nv_bfloat16*>(smem);  // 2 chunks of [64][136]
+  __nv_bfloat16* buf = reinterpret_cast<__nv_bfloat16*>(smem);  // kNBuf chunks of [64][136]
   pdl_trigger();
   if (sp >= n_split) return;
   pdl_wait();
@@ -140,13 +145,17 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
 #pragma unroll
       for (int i = 0; i < 4; ++i) o[j][i] = 0.f;
     cta_sync();  // the previous request's chunks have been read by every warp
-    if (c_begin < c_end) load_chunk(c_begin, 0);
-    cp_async_commit();
-    for (int ch = c_begin; ch < c_end; ++ch) {
-      const int slot = (ch - c_begin) & 1;
-      if (ch + 1 < c_end) load_chunk(ch + 1, slot ^ 1);
+#pragma unroll
+    for (int i = 0; i < kAhead; ++i) {  // (one commit group per chunk, empty past the last)
+      if (c_begin + i < c_end) load_chunk(c_begin + i, i);
       cp_async_commit();
-      cp_async_wait1();
+    }
+    for (int ch = c_begin; ch < c_end; ++ch) {
+      const int j = ch - c_begin, slot = j % kNBuf;
+      // the slot of chunk ch - 2: every warp finished it before it met the barrier of chunk ch - 1
+      if (ch + kAhead < c_end) load_chunk(ch + kAhead, (j + kAhead) % kNBuf);
+      cp_async_commit();
+      cp_async_wait<kAhead>();
       cta_sync();  // chunk ch has landed for every warp
       const __nv_bfloat16* Ks = buf + slot * (kChunk * kKStride);
       float s[8][4];
@@ -216,7 +225,6 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const __grid_con
           mma_bf16_16816(o[2 * ntp + 1], pa, vb[2], vb[3]);
         }
       }
-      cta_sync();  // every warp is done with chunk ch before it is refilled
     }
   };
   // row sums over the 4 threads of a row, then the decoded token of head h for the rows of request r
