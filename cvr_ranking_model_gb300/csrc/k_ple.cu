@@ -63,8 +63,9 @@ struct Smem {
   static constexpr int kOffScale = kOffBias + (kBN + 2 * kHN) * 4;  // fp32 row scales of the slice [208] (8-bit weights)
   static constexpr int kOffPlog = kOffScale + (I8 ? kBN * 4 : 0);   // fp32 [2 halves][128 rows]: partial logits
   static constexpr int kOffBar = kOffPlog + 2 * kBM * 4;
-  // per stage: full, empty (and for 8-bit weights: converted, weights landed); then acc_full, h_full, head_full
-  static constexpr int kNBar = 4 * kStages + 3;
+  // per stage: full, empty (and for 8-bit weights: converted, weights landed); then acc_full, h_full, head_full,
+  // w1_full
+  static constexpr int kNBar = 4 * kStages + 4;
   static constexpr int kBytes = kOffBar + kNBar * 8 + 16 + 1024;  // + alignment slack
   static_assert((kNT + kNE) * kATile <= kRingBytes, "output staging fits the ring");
   static_assert(kHBytes <= kRingBytes, "head operands fit the ring");
@@ -127,9 +128,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = bar;
   uint64_t* empty = bar + kStages;
   uint64_t* acc_full = bar + 2 * kStages;  // the main loop's accumulator is complete
-  uint64_t* h_full = acc_full + 1;         // heads: r_t and the W1 rows landed
+  uint64_t* h_full = acc_full + 1;         // heads: r_t (and the W1 rows when they come late) landed
   uint64_t* head_full = acc_full + 2;      // heads: hidden pre-activations complete
-  uint64_t* conv = acc_full + 3;           // 8-bit weights: stage s turned into bf16 by the epilogue warps
+  uint64_t* w1_full = acc_full + 3;        // heads: the W1 rows landed (loaded right after the main loop)
+  uint64_t* conv = acc_full + 4;           // 8-bit weights: stage s turned into bf16 by the epilogue warps
   uint64_t* wfull = conv + kStages;        // 8-bit weights: stage s's bytes landed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + S::kNBar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
@@ -139,6 +141,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rb = (int)blockIdx.x / kSlices;           // row block
   const int m0 = rb * kBM;
   const int ht = n >> 1, hh = n & 1;                  // head task of this CTA and the half of the rows it finishes
+  const bool w1_early = !a.keep_stages;
+  static_assert(kNT * kATile <= kHOffW, "the staged r_t slices end before the W1 rows");
+  bool w1_issued = false;  // (warp 0, lane 0)
   for (int k = threadIdx.x; k < kBN; k += blockDim.x) {  // (constants)
     sbias[k] = __ldg(a.ple_b + n * kBN + k);
     if constexpr (I8) sscale[k] = __ldg(a.ple_s8 + n * kBN + k);
@@ -159,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(acc_full, 1);
     mbar_init(h_full, 1);
     mbar_init(head_full, 1);
+    mbar_init(w1_full, 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmY);
@@ -205,6 +211,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(wdst + s * kWBytes, &tmW, &wbar[s], kb * kBK, n * kBN);
         }
         tma_load_2d(smem + S::kOffA + s * kATile, &tmY, &full[s], kb * kBK, m0);
+      }
+      // the heads' W1 rows: into the ring as soon as the main loop's MMAs have read it, so that they land during
+      // the epilogue and the r_t exchange (the staged r_t slices use the ring's first 32 KB only; staged expert
+      // outputs would reach the W1 area, so with those the rows come after the cluster barrier)
+      if (w1_early && mbar_wait(acc_full, 0, abort_flag, a.err)) {
+        mbar_expect_tx(w1_full, 4 * kHN * kBK * 2);
+        for (int kb = 0; kb < 4; ++kb)
+          tma_load_2d(smem + kHOffW + kb * (kHN * kBK * 2), &tmW1, w1_full, kb * kBK, ht * kHH);
+        w1_issued = true;
       }
     }
   } else if (warp == 1) {
@@ -352,13 +367,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();
   if (warp == 0 && lane == 0) {
     asm volatile("fence.proxy.async.global;" ::: "memory");  // R is read by TMA, as it was written
-    mbar_expect_tx(h_full, kHBytes);
+    mbar_expect_tx(h_full, w1_early ? 4 * kATile : kHBytes);
     for (int kb = 0; kb < 4; ++kb) {
       tma_load_2d(smem + kb * kATile, &tmR, h_full, kb * kBK, ht * r_rows + m0);
-      tma_load_2d(smem + kHOffW + kb * (kHN * kBK * 2), &tmW1, h_full, kb * kBK, ht * kHH);
+      if (!w1_early) tma_load_2d(smem + kHOffW + kb * (kHN * kBK * 2), &tmW1, h_full, kb * kBK, ht * kHH);
     }
+    if (w1_early && !w1_issued) mbar_arrive(w1_full);  // (gave up before issuing them: nothing will land)
   } else if (warp == 1 && lane == 0) {
-    if (mbar_wait(h_full, 0, abort_flag, a.err)) {
+    if (mbar_wait(h_full, 0, abort_flag, a.err) && (!w1_early || mbar_wait(w1_full, 0, abort_flag, a.err))) {
       tc_fence_after();
       constexpr uint32_t idesc = idesc_bf16(kBM, kHN);
       for (int kb = 0; kb < 4; ++kb)
@@ -369,6 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(head_full);
     } else {
       mbar_drain(h_full, 0);  // (gave up: the loads land before the shared memory is released)
+      if (w1_early) mbar_drain(w1_full, 0);
     }
   }
   if (warp >= 2) {
