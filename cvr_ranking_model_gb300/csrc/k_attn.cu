@@ -169,33 +169,36 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attention_kernel(const __grid_
                          *reinterpret_cast<const uint32_t*>(kp + 8));
         }
       }
+      // the row maxima on the raw logits (the scale is positive); only the sequence's last chunk has keys to mask
+      if ((ch + 1) * kChunk > Lr) {
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (ch * kChunk + nt * 8 + 2 * tig + (i & 1) >= Lr) s[nt][i] = -INFINITY;
+      }
       float cA = -INFINITY, cB = -INFINITY;
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int key = ch * kChunk + nt * 8 + 2 * tig + (i & 1);
-          s[nt][i] = key < Lr ? s[nt][i] * sl2 : -INFINITY;
-          if (i < 2)
-            cA = fmaxf(cA, s[nt][i]);
-          else
-            cB = fmaxf(cB, s[nt][i]);
-        }
+      for (int nt = 0; nt < 8; ++nt) {
+        cA = fmaxf(cA, fmaxf(s[nt][0], s[nt][1]));
+        cB = fmaxf(cB, fmaxf(s[nt][2], s[nt][3]));
+      }
       cA = fmaxf(cA, __shfl_xor_sync(0xffffffffu, cA, 1));
       cA = fmaxf(cA, __shfl_xor_sync(0xffffffffu, cA, 2));
       cB = fmaxf(cB, __shfl_xor_sync(0xffffffffu, cB, 1));
       cB = fmaxf(cB, __shfl_xor_sync(0xffffffffu, cB, 2));
-      const float nA = fmaxf(mA, cA), nB = fmaxf(mB, cB);
+      // running maxima in the scaled (log2) domain; p = 2^(s sl2 - m), the scale folded into one FMA per logit
+      const float nA = fmaxf(mA, cA * sl2), nB = fmaxf(mB, cB * sl2);
       const float fA = ex2(mA - nA), fB = ex2(mB - nB);
       mA = nA;
       mB = nB;
       float sumA = 0.f, sumB = 0.f;
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
-        s[nt][0] = ex2(s[nt][0] - nA);
-        s[nt][1] = ex2(s[nt][1] - nA);
-        s[nt][2] = ex2(s[nt][2] - nB);
-        s[nt][3] = ex2(s[nt][3] - nB);
+        s[nt][0] = ex2(fmaf(s[nt][0], sl2, -nA));
+        s[nt][1] = ex2(fmaf(s[nt][1], sl2, -nA));
+        s[nt][2] = ex2(fmaf(s[nt][2], sl2, -nB));
+        s[nt][3] = ex2(fmaf(s[nt][3], sl2, -nB));
         sumA += s[nt][0] + s[nt][1];
         sumB += s[nt][2] + s[nt][3];
       }
