@@ -317,23 +317,27 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
   }
 
   // ---------------------------------------------------------------- sequence events
-  // a warp takes four events per iteration (events ev + u * nw): per event 4 id columns -> 4 rows of the shared
-  // table -> one 128-wide row, 8 lanes per row; each lane has its four events' rows in flight at once, and the
-  // next iteration's ids load meanwhile
+  // a warp takes four events per round: per event 4 id columns -> 4 rows of the shared table -> one 128-wide row,
+  // 8 lanes per row; each lane has its four events' rows in flight at once, and the next round's ids load
+  // meanwhile
   {
     constexpr int kEvU = 4;
     const int64_t n_events = (int64_t)a.R * a.SL;
     const int c = lane >> 3, part = lane & 7;
     const int64_t stride = nw * kEvU;
-    // the warps that walked one bag unit fewer (gw >= n_units % nw) take the first events, so that the
-    // warps with the most work are not also the ones with an event round
+    // The warps that walked one bag unit fewer (gw >= n_units % nw) come first. When the events fit in one round
+    // of theirs (four each), they take them all and the warps with the most units take none; otherwise the
+    // events go round-robin over all warps, those warps first, four per round. Events of a round: ev + u * step,
+    // then ev += rstep.
     const int64_t n_units = ((int64_t)a.R * kFu + (int64_t)a.B * kFi + 3) / 4;
     const int64_t extra = n_units % nw;
-    int64_t ev = gw >= extra ? gw - extra : gw + (nw - extra);
+    const bool one_round = extra > 0 && n_events <= kEvU * (nw - extra);
+    int64_t ev = gw >= extra ? gw - extra : (one_round ? n_events : gw + (nw - extra));
+    const int step = (int)(one_round ? nw - extra : nw), rstep = (int)(one_round ? n_events : stride);
     int64_t id_next[kEvU];
 #pragma unroll
     for (int u = 0; u < kEvU; ++u) {
-      const int64_t e = ev + u * nw;
+      const int64_t e = ev + u * step;
       id_next[u] = e < n_events ? a.seq_ids[e * kCols + c] : 0;
     }
     while (ev < n_events) {  // warp-uniform
@@ -341,14 +345,14 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
 #pragma unroll
       for (int u = 0; u < kEvU; ++u) {
         id[u] = id_next[u];
-        const int64_t e1 = ev + stride + u * nw;
+        const int64_t e1 = ev + rstep + u * step;
         id_next[u] = e1 < n_events ? a.seq_ids[e1 * kCols + c] : 0;
       }
       __nv_bfloat16* out[kEvU];
       const float* src[kEvU];
 #pragma unroll
       for (int u = 0; u < kEvU; ++u) {
-        const int64_t e = ev + u * nw;
+        const int64_t e = ev + u * step;
         out[u] = nullptr;
         src[u] = nullptr;  // null: padding (stored as zeros) or past the last event
         bool hit = false, miss = false;
@@ -397,7 +401,7 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
         v[u].w = clampf(v[u].w, a.clamp);
         store_bf16x4(out[u], v[u]);
       }
-      ev += stride;
+      ev += rstep;
     }
   }
   if (errbits) atomicOr(a.err, errbits);
