@@ -371,6 +371,8 @@ def main():
                          "per-kernel region, end-to-end leg, gather roofline or CPU baseline")
     ap.add_argument("--ple-int8", action="store_true",
                     help="time the PLE on 8-bit weights (CVR_OPT_PLE_INT8) in the headline region as well")
+    ap.add_argument("--attention-tc", action="store_true",
+                    help="time the cross-attention on its tcgen05 kernel (CVR_OPT_ATTENTION_TC) in the headline region")
     ap.add_argument("--varlen", action="store_true",
                     help="variable-length sequences: every request's length per group uniform in [1, L_g]")
     args = ap.parse_args()
@@ -408,6 +410,7 @@ def main():
     sc = make_scorer(dw, w, stream=stream.cuda_stream)
     sc.set_option(cvr.OPT_CUDA_GRAPH, 1)
     sc.set_option(cvr.OPT_PLE_INT8, int(args.ple_int8))
+    sc.set_option(cvr.OPT_ATTENTION_TC, int(args.attention_tc))
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     r, b, o, s, out = dw.ptrs()
     B = wl.n_cand
@@ -611,6 +614,7 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 (PLE weights int8)" if args.ple_int8 else "bf16", "data": "synthetic",
+            **({"attention": "tcgen05 kernel (CVR_OPT_ATTENTION_TC)"} if args.attention_tc else {}),
             "config": {"workload": f"{args.config}: R={wl.n_req} requests x C={B // wl.n_req} candidates, "
                                    f"L={Lstr}, {wl.n_layers} interaction layer(s), tables {wl.user_rows}/"
                                    f"{wl.item_rows}/{wl.seq_rows} rows x 32 fp32, bags 1-8, Zipf({wl.zipf_s})",
