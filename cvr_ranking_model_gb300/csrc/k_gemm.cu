@@ -17,6 +17,10 @@
 // The per-request addends of a tile are fetched one tile ahead by a warp of their own into shared memory (the
 // request of each of the tile's rows, and the addend rows of up to kSlots consecutive requests), so the epilogue
 // warps find them there instead of paying the request-id, flag and addend loads in series on every tile.
+//
+//  tokenize_lu_kernel  the tokeniser for batches of at most 32 requests ("lu": local user half): each CTA owns one
+//                    column tile, keeps its weight slice in shared memory and computes that tile's user half for
+//                    every request itself, so no CTA waits on another (used instead of gemm_kernel<EPI_TOKENIZE>)
 #include "cvr_internal.cuh"
 
 namespace cvr {
