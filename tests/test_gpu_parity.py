@@ -131,6 +131,15 @@ def test_request_counts_around_the_tokeniser_user_paths(n_req):
     _check_full(wl, w, stages=True)
 
 
+def test_sequence_lengths_on_chunk_boundaries():
+    # every group's length a multiple of the attention's 64-position chunk (1, 2 and 3 chunks): no chunk has keys
+    # to mask
+    wl = synth.make_workload("tiny", n_req=3, cand_per_req=[40, 7, 25], seq_len=(64, 128, 192), user_rows=3000,
+                             item_rows=3000)
+    w = synth.make_weights(wl.n_layers, wl.seed, bias_scale=0.02)
+    _check_full(wl, w, stages=True)
+
+
 def test_two_layers_small():
     wl = synth.make_workload("deep", n_req=3, n_cand=40, seq_len=(17, 33, 65), user_rows=1000, item_rows=1000,
                              seq_rows=10_000)
