@@ -98,6 +98,7 @@ struct cvr_handle {
   unsigned* done = nullptr;
   unsigned* cs_count = nullptr;
   unsigned* ple_ready = nullptr;  // per 128-row block: Token Mixer tiles written
+  unsigned* attn_ready = nullptr;  // per 32-candidate block: attention groups written (same allocation)
   bf16* Rt = nullptr;             // [2][B_cap][256] gate-weighted expert sums
   unsigned* xu_ready = nullptr;   // [R_cap/128][16] user row-tiles of the tokeniser written
   int32_t* req_copy = nullptr;  // the call's request ids in the workspace
@@ -249,6 +250,11 @@ size_t attn_count_bytes(int B_cap) {
   return std::max((size_t)(B_cap + 31) / 32 * kG, (size_t)(B_cap + 127) / 128 * kG * kAttnCounters) * 4;
 }
 
+// the per-block ready counters, one array: Token Mixer tiles per 128-row block, then attention groups per
+// 32-candidate block
+size_t ple_ready_words(int B_cap) { return (size_t)(B_cap + 127) / 128; }
+size_t ready_bytes_of(int B_cap) { return (ple_ready_words(B_cap) + (size_t)(B_cap + 31) / 32) * 4; }
+
 cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   if (R <= h->R_cap && B <= h->B_cap) return CVR_OK;
   free_workspace(h);
@@ -272,7 +278,7 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   const size_t oQ = take((size_t)B_cap * kG * kD * 2), oEx = take((size_t)B_cap * kPleN * 2);
   const size_t oG = take((size_t)B_cap * 8 * 4), oErr = take(1024), oCnt = take((size_t)R_cap * kG * 4);
   const size_t oReq = take((size_t)B_cap * 4);
-  const size_t ready_bytes = (size_t)(B_cap + 127) / 128 * 4;  // Token Mixer tiles written per 128-row block
+  const size_t ready_bytes = ready_bytes_of(B_cap);  // Token Mixer tiles and attention groups written per block
   const size_t oRdy = take(ready_bytes);
   const size_t oR = take((size_t)2 * B_cap * kDE * 2);
   const size_t oXr = take((size_t)R_pad / 128 * (kTokN / 128) * 4);
@@ -310,6 +316,7 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   h->cs_count = (unsigned*)(b + oCnt);
   h->req_copy = (int32_t*)(b + oReq);
   h->ple_ready = (unsigned*)(b + oRdy);
+  h->attn_ready = h->ple_ready + ple_ready_words(B_cap);
   h->Rt = (bf16*)(b + oR);
   h->xu_ready = (unsigned*)(b + oXr);
   h->attn_splits = splits;
@@ -435,6 +442,8 @@ FwdArgs make_args(cvr_handle* h, int R, int B, const int32_t* req_ids, const int
   a.Ex = h->Ex;
   a.gates = h->gates;
   a.ple_ready = h->ple_ready;
+  // the register-tile attention counts its blocks for the Token Mixer (the tcgen05 one is waited for whole)
+  a.attn_ready = h->attn_tc ? nullptr : h->attn_ready;
   a.Rt = h->Rt;
   a.err = h->err;
   a.done = h->done;
@@ -654,7 +663,7 @@ cvr_status sync_status(cvr_handle* h) {
     // a CTA that gave up may have left a group or split counter part-way; the next call starts from zero
     if (h->cs_count) cudaMemset(h->cs_count, 0, (size_t)h->R_cap * kG * 4);
     if (h->attn_count) cudaMemset(h->attn_count, 0, attn_count_bytes(h->B_cap));
-    if (h->ple_ready) cudaMemset(h->ple_ready, 0, (size_t)(h->B_cap + 127) / 128 * 4);
+    if (h->ple_ready) cudaMemset(h->ple_ready, 0, ready_bytes_of(h->B_cap));
     return fail(h, CVR_E_TIMEOUT, "a bounded device-side wait gave up");
   }
   if (ew & kErrLayout) return fail(h, CVR_E_CUDA, "a kernel's shared-memory window was not 1024-byte aligned");
@@ -1341,6 +1350,7 @@ cvr_status cvr_predict_noalloc(cvr_handle* h, int32_t n_cand, const void* y, flo
   a.keep_stages = 0;
   a.Rt = reinterpret_cast<bf16*>(sc + kNaROff);
   a.ple_ready = nullptr;  // a caller's Y: the kernel waits for the preceding work in the stream instead
+  a.attn_ready = nullptr;
 
   a.err = reinterpret_cast<int*>(sc + kNaErrOff);
   a.done = reinterpret_cast<unsigned*>(sc + kNaErrOff + 256);

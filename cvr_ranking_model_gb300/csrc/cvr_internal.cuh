@@ -111,6 +111,9 @@ struct FwdArgs {
   __nv_bfloat16* Rt;      // [2][rows][256] gate-weighted expert sums r_t (task-major), the heads' A operand
   unsigned* ple_ready;    // [B/128] per 128-row block: 8-candidate tiles the last Token Mixer has written, or null
                           // (zeroed by the first kernel of each call; null: wait for the previous grid instead)
+  unsigned* attn_ready;   // [B/32] per 32-candidate block: groups whose decoded tokens the attention has written,
+                          // summed over the layers (3 per layer), or null: the Token Mixer then waits for the whole
+                          // attention grid (zeroed by the first kernel of each call)
   int* err;               // device error word (bits below), reset by the last kernel of each call
   unsigned* done;         // CTA counter of the last kernel (finds the CTA that publishes the error word)
   int* err_host;          // device view of a pinned host word: the call's error bits are OR-ed into it
@@ -428,6 +431,19 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+// Waits (at most ~1 s) until *cnt >= need; a wait that gives up is reported and the caller goes on (every access
+// stays in bounds whatever the data), so nothing can hang on a producer that never finishes.
+__device__ __forceinline__ void wait_count(const unsigned* cnt, unsigned need, int* err) {
+  if (ld_acquire_u32(cnt) >= need) return;
+  const uint64_t t0 = global_timer_ns();
+  while (ld_acquire_u32(cnt) < need) {
+    if (global_timer_ns() - t0 > 1000000000ull) {
+      atomicOr(err, kErrTimeout);
+      return;
+    }
+    __nanosleep(64);
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {

@@ -247,6 +247,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attention_kernel(const __grid_
     }
   };
 
+  // this group's tokens of the tile are written: count them for the Token Mixer, whose tiles of these candidates
+  // start once every group is in (a CTA barrier, then one release at GPU scope covers all the CTA's writes)
+  auto publish = [&]() {
+    if (!a.attn_ready) return;
+    cta_sync();
+    if (tid == 0) red_release_add(a.attn_ready + blockIdx.x, 1u);
+  };
   if (!split) {
     for (int r = r_first; r <= r_last; ++r) {
       // keys: the request's real events (variable-length sequences mask the padding out); none -> zero token
@@ -254,6 +261,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attention_kernel(const __grid_
       run_chunks(r, Lr, 0, (Lr + kChunk - 1) / kChunk);
       finish(r, Lr);
     }
+    publish();
     return;
   }
   // ---- split: this CTA's positions, its state to the workspace, the last split of the tile merges them
@@ -310,6 +318,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attention_kernel(const __grid_
   }
   if (tid == 0) a.attn_count[slot] = 0u;  // ready for the next call
   finish(r, Lr);
+  publish();
 }
 
 }  // namespace

@@ -174,7 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sA + kATile / 2, &tmA, a_full, 64, (int)ti.row0);
       }
     }
-    if (!waited) pdl_wait();
+    // (TM with the attention's block counters: every tile it publishes has waited for its own blocks)
+    if (!waited && !(MODE == MODE_TM && a.attn_ready)) pdl_wait();
     if (MODE == MODE_TM && lane == 0 && a.ple_ready && layer == a.n_layers - 1) {
       // publish each tile once its 16 epilogue warps have written it: count it for its 128-row block, which the
       // PLE starts when all of the block's tiles are in (bounded wait, as every wait here)
@@ -297,20 +298,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         gj2[e] = f2pack(g.x, g.y);
       }
     }
-    pdl_wait();
-    if (threadIdx.x == 64) CVR_TL_WAITED();
+    // TM: each tile waits for the attention's groups of its 8 candidates (a 32-candidate block) instead of the
+    // whole attention grid, when the attention counts them
+    const bool by_block = MODE == MODE_TM && a.attn_ready != nullptr;
+    if (!by_block) {
+      pdl_wait();
+      if (threadIdx.x == 64) CVR_TL_WAITED();
+    }
+    // true once the attention has written every group of the tile's block; block: wait (bounded) for it. Lane 0
+    // reads the counter with acquire semantics and the warp barrier orders the other lanes' loads after it.
+    auto z_ready = [&](int tile, bool block) -> bool {
+      if (!by_block) return true;
+      const unsigned need = (unsigned)(kG * (layer + 1));  // the counters sum over the layers
+      int ready = 1;
+      if (lane == 0) {
+        if (block)
+          wait_count(a.attn_ready + tile / 4, need, a.err);
+        else
+          ready = ld_acquire_u32(a.attn_ready + tile / 4) >= need;
+      }
+      ready = __shfl_sync(0xffffffffu, ready, 0);
+      __syncwarp();
+      return ready != 0;
+    };
     // TM: this thread's 4 pieces Z[b][t][8j..8j+8) (tokens t = 4 grp.. of its column quarter), written into
     // TMEM lane (b, j) at columns 4t.., form the mixed activation row (b, j) (K slot t holds head j of token t)
     // that the up projection reads as its A operand; the same TMEM columns later give the residual back.
     const int bl = rl >> 4, j = rl & 15;
     auto load_z = [&](uint4* z, int tile) {
       // unconditional loads (rows past the batch read the last candidate and are never stored), so the
-      // loads stay in flight until the registers are consumed
+      // loads stay in flight until the registers are consumed; through L2, as the attention grid that wrote
+      // the decoded tokens may still be running
       const int64_t bc = (int64_t)tile * (128 / kT) + bl;
       const int64_t bsrc = bc < a.B ? bc : a.B - 1;
 #pragma unroll
       for (int tt = 0; tt < 4; ++tt)
-        z[tt] = __ldg(reinterpret_cast<const uint4*>(zin + bsrc * kYD + (grp * 4 + tt) * kD + j * 8));
+        z[tt] = __ldcg(reinterpret_cast<const uint4*>(zin + bsrc * kYD + (grp * 4 + tt) * kD + j * 8));
     };
     auto store_a = [&](const uint4* z, int buf) {
       uint32_t w[16];
@@ -328,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(a_full);
     };
     uint4 znext[4];
+    int z_late = -1;  // TM: the next tile, when its block was not ready at the prefetch (loaded before it is stored)
     // chunk cc of tile i: silu(a) * g of this warp's 32 units, stored as the down projection's A operand
     auto chunk = [&](int i, int c, bool has_next) -> bool {
       const int cc = i * kChunks + c;
@@ -348,7 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(up_empty);
           // every up projection of this tile has completed: the next tile's activations may be written
-          if (MODE == MODE_TM && c == kChunks - 1 && has_next) store_a(znext, (i + 1) & 1);
+          if (MODE == MODE_TM && c == kChunks - 1 && has_next) {
+            if (z_late >= 0) {
+              z_ready(z_late, true);
+              load_z(znext, z_late);
+              z_late = -1;
+            }
+            store_a(znext, (i + 1) & 1);
+          }
         }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -472,6 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (MODE == MODE_TM && n_my > 0) {
       uint4 z0[4];
+      z_ready(blockIdx.x, true);
+      if (by_block && threadIdx.x == 64) CVR_TL_WAITED();
       load_z(z0, blockIdx.x);
       store_a(z0, 0);
     }
@@ -493,7 +526,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         bias_group = ti.g;
       }
       const bool has_next = i + 1 < n_my;
-      if (MODE == MODE_TM && has_next) load_z(znext, blockIdx.x + (i + 1) * n_cta);
+      if (MODE == MODE_TM && has_next) {
+        const int nt = blockIdx.x + (i + 1) * n_cta;
+        if (z_ready(nt, false))
+          load_z(znext, nt);
+        else
+          z_late = nt;
+      }
       ok = chunk(i, 0, has_next);
       if (ok && kDefer && i >= 1) ok = finish(i - 1);
       if (ok) ok = chunk(i, 1, has_next);
@@ -508,6 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+  // (TM on the block counters: the kernel still completes only after the attention grid, so that whatever waits
+  // for it waits for every earlier kernel too)
+  if (MODE == MODE_TM && a.attn_ready && threadIdx.x == 0) pdl_wait();
 }
 
 }  // namespace

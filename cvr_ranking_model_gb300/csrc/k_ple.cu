@@ -95,19 +95,6 @@ __device__ __forceinline__ void cluster_sync() {
   __syncwarp();
   asm volatile("barrier.cluster.arrive.release;\nbarrier.cluster.wait.acquire;" ::: "memory");
 }
-// Waits (at most ~1 s) until *cnt >= need; a wait that gives up is reported and the kernel goes on (every access
-// stays in bounds whatever the data), so nothing can hang on a producer that never finishes.
-__device__ __forceinline__ void wait_count(const unsigned* cnt, unsigned need, int* err) {
-  if (ld_acquire_u32(cnt) >= need) return;
-  const uint64_t t0 = global_timer_ns();
-  while (ld_acquire_u32(cnt) < need) {
-    if (global_timer_ns() - t0 > 1000000000ull) {
-      atomicOr(err, kErrTimeout);
-      return;
-    }
-    __nanosleep(64);
-  }
-}
 
 template <bool I8>
 __global__ void __launch_bounds__(kThreads, 1)

@@ -117,6 +117,9 @@ __global__ void __launch_bounds__(kSparseThreads, kSparseBlocksPerSm) sparse_ker
       a.ple_ready[i] = 0u;
     }
   }
+  if (a.attn_ready)  // and those that start the Token Mixer's tiles
+    for (int i = blockIdx.x * kSparseThreads + tid; i < (a.B + 31) / 32; i += gridDim.x * kSparseThreads)
+      a.attn_ready[i] = 0u;
   if (a.xu_ready)  // and so do the tokeniser's user row-tile flags
     for (int i = blockIdx.x * kSparseThreads + tid; i < (a.R + 127) / 128 * (kTokN / 128); i += gridDim.x * kSparseThreads)
       a.xu_ready[i] = 0u;

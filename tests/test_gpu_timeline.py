@@ -41,5 +41,9 @@ def test_timeline_build_orders_the_kernels():
         assert np.isnan(w_med) or s_min <= w_med <= e_max, name
     # each kernel's data dependency: its wait returns after its producer's last CTA has finished
     for prod, cons in (("sparse", "seq_mlp"), ("sparse", "tokenizer"), ("seq_mlp", "seq_colsum"),
-                       ("seq_colsum", "attention"), ("tokenizer", "attention"), ("attention", "token_mixer")):
+                       ("seq_colsum", "attention"), ("tokenizer", "attention")):
         assert rows[cons][4] >= rows[prod][6] - 0.05, (prod, cons)
+    # the Token Mixer's tiles wait for the attention blocks of their own candidates (the attention counts each
+    # block as its groups are written), so its first tile starts after attention CTAs have run, not after all
+    assert rows["token_mixer"][4] >= rows["attention"][1] - 0.05
+    assert rows["token_mixer"][6] >= rows["attention"][6] - 0.05
