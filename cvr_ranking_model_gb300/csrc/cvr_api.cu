@@ -95,7 +95,6 @@ struct cvr_handle {
   bf16 *U = nullptr, *I = nullptr, *Xs = nullptr, *H = nullptr, *Z = nullptr, *Y = nullptr, *Q = nullptr, *Ex = nullptr;
   float *colsum = nullptr, *xu = nullptr, *qb = nullptr, *gates = nullptr;
   int* err = nullptr;
-  unsigned* done = nullptr;
   unsigned* cs_count = nullptr;
   unsigned* ple_ready = nullptr;  // per 128-row block: Token Mixer tiles written
   unsigned* attn_ready = nullptr;  // per 32-candidate block: attention groups written (same allocation)
@@ -312,7 +311,6 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   h->Ex = (bf16*)(b + oEx);
   h->gates = (float*)(b + oG);
   h->err = (int*)(b + oErr);
-  h->done = (unsigned*)(b + oErr + 256);
   h->cs_count = (unsigned*)(b + oCnt);
   h->req_copy = (int32_t*)(b + oReq);
   h->ple_ready = (unsigned*)(b + oRdy);
@@ -322,7 +320,7 @@ cvr_status ensure_workspace(cvr_handle* h, int R, int B) {
   h->attn_splits = splits;
   h->attn_state = splits > 1 ? (float*)(b + oAst) : nullptr;
   h->attn_count = (unsigned*)(b + oAcnt);
-  e = cudaMemset(h->err, 0, 1024);  // error word and CTA counter start at zero; the last kernel resets them
+  e = cudaMemset(h->err, 0, 1024);  // the error word starts at zero; the host clears it after an error
   if (e == cudaSuccess) e = cudaMemset(h->cs_count, 0, (size_t)R_cap * kG * 4);  // reset by their last block
   if (e == cudaSuccess) e = cudaMemset(h->attn_count, 0, cnt_bytes);  // reset by the merging CTA or warp
   if (e == cudaSuccess) e = cudaMemset(h->ple_ready, 0, ready_bytes);  // (also cleared by every call's first kernel)
@@ -446,7 +444,6 @@ FwdArgs make_args(cvr_handle* h, int R, int B, const int32_t* req_ids, const int
   a.attn_ready = h->attn_tc ? nullptr : h->attn_ready;
   a.Rt = h->Rt;
   a.err = h->err;
-  a.done = h->done;
   a.err_host = h->err_host_dev;
   a.wblob = static_cast<const uint8_t*>(h->wblob);
   a.wblob_bytes = (int64_t)h->wblob_bytes;
@@ -659,6 +656,8 @@ cvr_status sync_status(cvr_handle* h) {
   volatile int* hw = h->err_host;
   const int ew = *hw;
   *hw = 0;
+  // the device word keeps its bits (every later call of the window reported them too): clear it for the next call
+  if (ew && h->err) cudaMemset(h->err, 0, 4);
   if (ew & kErrTimeout) {
     // a CTA that gave up may have left a group or split counter part-way; the next call starts from zero
     if (h->cs_count) cudaMemset(h->cs_count, 0, (size_t)h->R_cap * kG * 4);
@@ -1290,7 +1289,7 @@ namespace {
 constexpr int kNoAllocMaxCand = CVR_NOALLOC_MAX_CAND;
 constexpr size_t kNaROff = 0;                                                // r_t, bf16 [2][n][256]
 constexpr size_t kNaErrOff = kNaROff + (size_t)2 * kNoAllocMaxCand * kDE * 2;
-constexpr size_t kNaBytes = kNaErrOff + 512;                                 // error word (+0), CTA counter (+256)
+constexpr size_t kNaBytes = kNaErrOff + 512;                                 // error word (+0)
 constexpr int kNaMaxDevices = 64;
 
 std::mutex g_na_mu;
@@ -1353,9 +1352,8 @@ cvr_status cvr_predict_noalloc(cvr_handle* h, int32_t n_cand, const void* y, flo
   a.attn_ready = nullptr;
 
   a.err = reinterpret_cast<int*>(sc + kNaErrOff);
-  a.done = reinterpret_cast<unsigned*>(sc + kNaErrOff + 256);
   cudaStream_t s = h->stream;
-  ce = cudaMemsetAsync(sc + kNaErrOff, 0, 512, s);  // the error word and the CTA counter start at zero
+  ce = cudaMemsetAsync(sc + kNaErrOff, 0, 512, s);  // the error word starts at zero
   CUtensorMap tmR;
   if (!encode_2d(&tmR, a.Rt, kDE, (uint64_t)2 * kNoAllocMaxCand, kDE, 64, 128))
     return fail(h, CVR_E_CUDA, "cuTensorMapEncodeTiled failed for the prediction scratch");

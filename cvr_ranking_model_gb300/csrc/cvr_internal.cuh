@@ -114,9 +114,9 @@ struct FwdArgs {
   unsigned* attn_ready;   // [B/32] per 32-candidate block: groups whose decoded tokens the attention has written,
                           // summed over the layers (3 per layer), or null: the Token Mixer then waits for the whole
                           // attention grid (zeroed by the first kernel of each call)
-  int* err;               // device error word (bits below), reset by the last kernel of each call
-  unsigned* done;         // CTA counter of the last kernel (finds the CTA that publishes the error word)
-  int* err_host;          // device view of a pinned host word: the call's error bits are OR-ed into it
+  int* err;               // device error word (bits below), OR-ed by any kernel that finds an error; it keeps its
+                          // bits until the host clears it after reporting them
+  int* err_host;          // device view of a pinned host word: the last kernel's CTAs OR the error bits into it
   // hot-row cache in HBM in front of embedding tables (per table; null tags = no cache for that table)
   int cache_on;                      // any table has a cache
   const float* cache_rows[kNTab];      // [slots][32] fp32 copies of table rows

@@ -131,14 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool w1_early = !a.keep_stages;
   static_assert(kNT * kATile <= kHOffW, "the staged r_t slices end before the W1 rows");
   bool w1_issued = false;  // (warp 0, lane 0)
-  for (int k = threadIdx.x; k < kBN; k += blockDim.x) {  // (constants)
-    sbias[k] = __ldg(a.ple_b + n * kBN + k);
-    if constexpr (I8) sscale[k] = __ldg(a.ple_s8 + n * kBN + k);
-  }
-  for (int k = threadIdx.x; k < kHN; k += blockDim.x) {
-    sb1[k] = __ldg(a.head_b1 + ht * kHH + k);
-    sw2[k] = __ldg(a.head_w2 + ht * kHH + k);
-  }
+  int err_seen = 0;        // (thread 0) the error word after every earlier kernel has completed
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -234,6 +227,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3, grp = (warp - 2) >> 2;  // TMEM lane quarter; units [32 grp, 32 grp + 32) of the slice
     const int rl = q * 32 + lane, row = m0 + rl;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    // the biases and head constants, staged by the epilogue warps themselves while the first copies and MMAs run
+    // (only these warps read them, all after this barrier)
+    for (int k = threadIdx.x - 64; k < kBN; k += kEpiWarps * 32) {
+      sbias[k] = __ldg(a.ple_b + n * kBN + k);
+      if constexpr (I8) sscale[k] = __ldg(a.ple_s8 + n * kBN + k);
+    }
+    for (int k = threadIdx.x - 64; k < kHN; k += kEpiWarps * 32) {
+      sb1[k] = __ldg(a.head_b1 + ht * kHH + k);
+      sw2[k] = __ldg(a.head_w2 + ht * kHH + k);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
     if constexpr (I8) {
       // 8-bit weights: stage s's [208][64] bytes -> the bf16 B tile in the layout a 128-byte-swizzled TMA load
       // would give (row r at 128 r, 16-byte chunk c at chunk c ^ (r % 8)); one 16-byte chunk of a row per step
@@ -360,6 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!w1_early) tma_load_2d(smem + kHOffW + kb * (kHN * kBK * 2), &tmW1, h_full, kb * kBK, ht * kHH);
     }
     if (w1_early && !w1_issued) mbar_arrive(w1_full);  // (gave up before issuing them: nothing will land)
+    // the error bits of every earlier kernel of the call (complete once the wait returns) and of this CTA's own
+    // waits so far, read while the head MMAs run
+    pdl_wait();
+    err_seen = *reinterpret_cast<volatile int*>(a.err);
   } else if (warp == 1 && lane == 0) {
     if (mbar_wait(h_full, 0, abort_flag, a.err) && (!w1_early || mbar_wait(w1_full, 0, abort_flag, a.err))) {
       tc_fence_after();
@@ -407,22 +415,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
-  // This is the last kernel of a call: the last of its CTAs to finish moves the call's error bits (once every
-  // earlier kernel has completed) into the host word and resets the device word for the next call. The host word
-  // is touched only when there is an error (the host reads it after waiting for the stream, which makes the write
-  // visible), so an error-free call ends without a round trip to host memory.
+  // This is the last kernel of a call. Each CTA ORs what it read of the error word, and a timeout of its own later
+  // waits (they raise the CTA's abort flag), into the pinned host word, which the host reads after waiting for the
+  // stream. An error-free call ends without an atomic or a round trip to host memory. The device word keeps its
+  // bits until the host, having found an error, clears it.
   if (threadIdx.x == 0) {
-    pdl_wait();
-    __threadfence();
-    if (atomicAdd(a.done, 1u) == gridDim.x - 1) {
-      __threadfence();
-      const int ew = atomicExch(a.err, 0);
-      if (ew) {
-        volatile int* hw = a.err_host;
-        *hw = *hw | ew;
-      }
-      atomicExch(a.done, 0u);
-    }
+    const int ew = err_seen | (*abort_flag ? kErrTimeout : 0);
+    if (ew) atomicOr(a.err_host, ew);
   }
 }
 

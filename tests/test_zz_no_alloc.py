@@ -2,8 +2,7 @@
 
 cvr_score runs the whole forward pass; its last Token Mixer output (CVR_STAGE_Y) is handed to
 cvr_predict_noalloc, whose PLE + heads must give the same pCVR within the scoring path's tolerance, on
-two calls in a row (the fixed scratch array is reused: its error word and CTA counter must come back
-clean). The file is named to be collected last, so it also runs after every other GPU test.
+two calls in a row (the fixed scratch array is reused: its error word must come back clean). The file is named to be collected last, so it also runs after every other GPU test.
 """
 import numpy as np
 import pytest
