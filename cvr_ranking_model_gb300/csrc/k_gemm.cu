@@ -528,11 +528,12 @@ __global__ void __launch_bounds__(96 + NEPI * 32, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // the weights are constant: the slice's copies start before the wait for the previous kernel
+      // The copies need no wait for the previous kernel: the weights are constant, and the item and user rows
+      // come from the gather kernel, which has completed before this grid can launch (the side stream starts
+      // after it; on one stream the sequence encoder opens its edge only after its own wait for it). Only the
+      // epilogue, which adds the column sums' qb, waits for the previous grid; the MMAs run meanwhile.
       mbar_expect_tx(bres_full, nk * kATile);
       for (int kb = 0; kb < nk; ++kb) tma_load_2d(sB + kb * kATile, &tmB, bres_full, kb * kBK, n0);
-      pdl_wait();
-      CVR_TL_WAITED();
       int kc = 0;
       bool ok = true;
       for (int job = 0; job < n_items + 1 && ok; ++job) {
@@ -584,7 +585,7 @@ __global__ void __launch_bounds__(96 + NEPI * 32, 1)
     }
   } else if (warp == 2 + NEPI) {
     // ---- request ids of each row-tile (clamped into [0, R); the sparse kernel reports bad ones), one tile ahead
-    pdl_wait();
+    // (the gather kernel's copy: complete before this grid launches, as the rows above)
     int rq[kBM / 32];
     auto load_req = [&](int t) {
       const int m0 = (t / tiles_n) * kBM;
@@ -615,6 +616,7 @@ __global__ void __launch_bounds__(96 + NEPI * 32, 1)
     const int n = q * 32 + lane, nb = n0 + n;
     const float bias = __ldg(a.tok_b + nb);
     pdl_wait();  // (qb, when it is added here, comes from the column-sum kernel)
+    if (threadIdx.x == 64) CVR_TL_WAITED();
     const bool addq = nb >= kXD && !a.q_add;
     float qv[16];
 #pragma unroll
