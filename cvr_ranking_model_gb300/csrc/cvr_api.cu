@@ -110,7 +110,7 @@ struct cvr_handle {
   void* stage = nullptr;
   size_t stage_bytes = 0;
   // tensor maps
-  CUtensorMap tm_seqW13, tm_seqW2, tm_tokI, tm_tokU, tm_qW[kMaxLayers], tm_tmW13, tm_tmW2, tm_pleW, tm_pleW8, tm_headW1;
+  CUtensorMap tm_seqW13, tm_seqW2, tm_tokI, tm_tokU, tm_qW[kMaxLayers], tm_qWw[kMaxLayers], tm_tmW13, tm_tmW2, tm_pleW, tm_pleW8, tm_headW1;
   CUtensorMap tm_Xs, tm_I, tm_U, tm_U32, tm_x_Z, tm_x_Y, tm_full_Z, tm_full_Y, tm_Q, tm_H, tm_R, tm_Ex;
   // graphs, profiling
   bool use_graph = true, profile = false, pdl = true;
@@ -549,7 +549,7 @@ cudaError_t enqueue_forward(cvr_handle* h, const FwdArgs& a, cudaStream_t s, boo
     if (l > 0) std::swap(zin, zout);  // layer l reads the previous output (its first 13 tokens) in place
     const bool in_is_Z = zin == h->Z;
     // the first layer's queries come out of the tokeniser
-    if (l > 0) run(launch_query(a, l, in_is_Z ? h->tm_x_Z : h->tm_x_Y, h->tm_qW[l], t), kStageNames[4]);
+    if (l > 0) run(launch_query(a, l, in_is_Z ? h->tm_x_Z : h->tm_x_Y, h->tm_qW[l], h->tm_qWw[l], t), kStageNames[4]);
     FwdArgs al = a;  // the first layer's queries may still lack their mean-pooled term (stacked layers' have it)
     al.q_add = l == 0 ? af.q_add : 0;
     run(h->attn_tc ? launch_attention_tc(al, h->tm_Q, h->tm_H, zin, t) : launch_attention(al, zin, t), kStageNames[5]);
@@ -930,7 +930,8 @@ cvr_status cvr_create(const cvr_weights* w, const cvr_config* cfg, void* cuda_st
        encode_2d_u8(&h->tm_pleW8, h->w8blob, kYD, kPleCols, kYD, 64, 208) &&
        encode_2d(&h->tm_headW1, h->headW1, kDE, kNT * kHH, kDE, 64, 128);
   for (int l = 0; l < NL && ok; ++l)
-    ok = encode_2d(&h->tm_qW[l], h->qX + (size_t)l * kG * kD * kXD, kXD, kG * kD, kXD, 64, 96);
+    ok = encode_2d(&h->tm_qW[l], h->qX + (size_t)l * kG * kD * kXD, kXD, kG * kD, kXD, 64, kQryBNNarrow) &&
+         encode_2d(&h->tm_qWw[l], h->qX + (size_t)l * kG * kD * kXD, kXD, kG * kD, kXD, 64, kQryBNWide);
   if (!ok) {
     cvr_destroy(h);
     return CVR_E_CUDA;

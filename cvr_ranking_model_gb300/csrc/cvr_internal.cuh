@@ -529,7 +529,12 @@ cudaError_t launch_tokenizer(const FwdArgs& a, const CUtensorMap& tmI, const CUt
                              const CUtensorMap& tmWu, int max_grid, bool pdl, cudaStream_t s);
 // Requests up to which each tokeniser CTA computes its own column tile's user half.
 constexpr int kTokOwnXuMaxR = 32;
-cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, const CUtensorMap& tmW, cudaStream_t s);
+// Columns of Q per tile of the stacked layers' query GEMM, narrow or wide (launch_query picks one per batch); also
+// the row counts of the boxes of its two weight tensor maps.
+constexpr int kQryBNNarrow = 96, kQryBNWide = 128;
+// tmW: the layer's weights with boxes of kQryBNNarrow rows, tmWw with boxes of kQryBNWide rows
+cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                         const CUtensorMap& tmWw, cudaStream_t s);
 cudaError_t launch_attention(const FwdArgs& a, __nv_bfloat16* zin, cudaStream_t s);
 cudaError_t launch_attention_tc(const FwdArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmH, __nv_bfloat16* zin,
                                 cudaStream_t s);

@@ -724,13 +724,15 @@ cudaError_t launch_gemm(const FwdArgs& a, const CUtensorMap& tmA, const CUtensor
 }
 
 constexpr int kTokBN = 128, kTokStages = 4, kTokEpi = 8;
-constexpr int kQryBN = 96, kQryStages = 6, kQryEpi = 8;
+constexpr int kQryStages = 6, kQryEpi = 8;
+static_assert((kG * kD) % kQryBNNarrow == 0 && (kG * kD) % kQryBNWide == 0, "both query tile widths divide Q's columns");
 
 }  // namespace
 
 cudaError_t prepare_gemm_kernels() {
   cudaError_t e = prepare_gemm<kTokBN, kTokStages, EPI_TOKENIZE, kTokEpi>();
-  if (e == cudaSuccess) e = prepare_gemm<kQryBN, kQryStages, EPI_QUERY, kQryEpi>();
+  if (e == cudaSuccess) e = prepare_gemm<kQryBNNarrow, kQryStages, EPI_QUERY, kQryEpi>();
+  if (e == cudaSuccess) e = prepare_gemm<kQryBNWide, kQryStages, EPI_QUERY, kQryEpi>();
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(tokenize_lu_kernel<kLuEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize, LuSmem::kBytes);
   return e;
@@ -754,8 +756,21 @@ cudaError_t launch_tokenizer(const FwdArgs& a, const CUtensorMap& tmI, const CUt
                                                                 (a.R + kBM - 1) / kBM, s, max_grid, pdl);
 }
 
-cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, const CUtensorMap& tmW, cudaStream_t s) {
-  return launch_gemm<kQryBN, kQryStages, EPI_QUERY, kQryEpi>(a, tmX, tmW, tmX, tmX, tmX, tmX, a.B, kG * kD, kXD, layer, 0, s);
+cudaError_t launch_query(const FwdArgs& a, int layer, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                         const CUtensorMap& tmWw, cudaStream_t s) {
+  // The main loop is bound by shared memory: a k-block moves A (16 KB) and B (BN rows x 128 B) through it. Wide
+  // tiles move fewer bytes per column but make fewer, longer tiles: take the width whose rounds of tiles over the
+  // persistent grid cost fewer bytes (wide from 512 candidates per 152 SMs upwards).
+  auto cost = [&](int bn) {
+    const int64_t tiles = (int64_t)((a.B + kBM - 1) / kBM) * (kG * kD / bn);
+    const int64_t grid = tiles < a.num_sms ? tiles : a.num_sms;
+    return (tiles + grid - 1) / grid * (int64_t)(kATile + bn * kBK * 2);
+  };
+  if (cost(kQryBNWide) < cost(kQryBNNarrow))
+    return launch_gemm<kQryBNWide, kQryStages, EPI_QUERY, kQryEpi>(a, tmX, tmWw, tmX, tmX, tmX, tmX, a.B, kG * kD, kXD,
+                                                                    layer, 0, s);
+  return launch_gemm<kQryBNNarrow, kQryStages, EPI_QUERY, kQryEpi>(a, tmX, tmW, tmX, tmX, tmX, tmX, a.B, kG * kD, kXD,
+                                                                    layer, 0, s);
 }
 
 }  // namespace cvr
