@@ -147,8 +147,12 @@ __global__ void __launch_bounds__(96 + NEPI * 32, 1)
   tc_fence_after();
   const uint32_t tbase = *tslot;
   pdl_trigger();
-  pdl_wait();
-  if (threadIdx.x == 0) CVR_TL_WAITED();
+  // The query GEMM's operand is the previous kernel's output: every warp waits for it. The tokeniser's copies need
+  // no wait (the weights, and the gather kernel's rows, which are complete before this grid can launch: the
+  // sequence encoder opens its edge only after its own wait for the gather kernel); its addend and epilogue warps,
+  // which read the column sums' qb, wait for the previous grid while the first MMAs run.
+  if (EPI != EPI_TOKENIZE || warp >= 2) pdl_wait();
+  if (threadIdx.x == (EPI == EPI_TOKENIZE ? 64 : 0)) CVR_TL_WAITED();
 
   if (warp == 0) {
     if (lane == 0) {
