@@ -285,8 +285,9 @@ def test_shape_errors_on_the_host():
 _TABLES = {}
 
 
-def _full(name, requests, n_cand=None):
-    wl = synth.make_workload(name, n_cand=n_cand)
+def _full(name, requests, n_cand=None, n_req=None):
+    wl = synth.make_workload(name, n_cand=n_cand) if n_req is None else synth.make_workload(name, n_cand=n_cand,
+                                                                                            n_req=n_req)
     w = synth.make_weights(wl.n_layers, wl.seed)
     g = GpuRun(wl, w, graph=True)
     g.run()
@@ -323,6 +324,12 @@ def test_embheavy_sampled():
 @pytest.mark.parametrize("c", [64, 512, 2048])
 def test_deep_sampled(c):
     _full("deep", requests=[0, 31] if c < 2048 else [5], n_cand=c)
+
+
+def test_deep_wide_query_tiles_with_a_ragged_row_tile():
+    # 24 x 500 = 12,000 candidates: the stacked layer's query GEMM takes its 128-column tiles (2 rounds of tiles
+    # over the grid instead of 3) and its last row tile holds 96 candidates
+    _full("deep", requests=[0, 23], n_cand=500, n_req=24)
 
 
 def test_async_calls_match_sync_and_report_errors():
