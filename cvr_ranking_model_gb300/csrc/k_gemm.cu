@@ -151,12 +151,24 @@ __global__ void __launch_bounds__(96 + NEPI * 32, 1)
   // no wait (the weights, and the gather kernel's rows, which are complete before this grid can launch: the
   // sequence encoder opens its edge only after its own wait for the gather kernel); its addend and epilogue warps,
   // which read the column sums' qb, wait for the previous grid while the first MMAs run.
-  if (EPI != EPI_TOKENIZE || warp >= 2) pdl_wait();
-  if (threadIdx.x == (EPI == EPI_TOKENIZE ? 64 : 0)) CVR_TL_WAITED();
+  // (the query GEMM's producer issues its first stages' weights before it waits, below)
+  if (EPI == EPI_TOKENIZE ? warp >= 2 : warp != 0) pdl_wait();
+  if (threadIdx.x == (EPI == EPI_TOKENIZE ? 64 : 32)) CVR_TL_WAITED();
 
   if (warp == 0) {
     if (lane == 0) {
-      int kc = 0;
+      int kc = 0, pre = 0;  // pre: k-blocks of the first tile whose weights are already in flight
+      if (EPI == EPI_QUERY) {
+        // the weights are constant: the first stages' copies start before the wait for the previous kernel
+        if ((int)blockIdx.x < n_tiles) {
+          pre = STAGES < nk ? STAGES : nk;
+          for (int kb = 0; kb < pre; ++kb) {
+            mbar_expect_tx(&full[kb], kATile + B_TILE);
+            tma_load_2d(sB + kb * B_TILE, &tmB, &full[kb], kb * kBK, ((int)blockIdx.x % tiles_n) * BN);
+          }
+        }
+        pdl_wait();
+      }
       bool ok = true;
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
         const int mt = tile / tiles_n, n0 = (tile % tiles_n) * BN;
@@ -168,9 +180,9 @@ __global__ void __launch_bounds__(96 + NEPI * 32, 1)
             ok = false;
             break;
           }
-          mbar_expect_tx(&full[s], kATile + B_TILE);
+          if (kc >= pre) mbar_expect_tx(&full[s], kATile + B_TILE);
           tma_load_2d(sA + s * kATile, user ? &tmU : &tmA, &full[s], kb * kBK, m0);
-          tma_load_2d(sB + s * B_TILE, user ? &tmWu : &tmB, &full[s], kb * kBK, n0);
+          if (kc >= pre) tma_load_2d(sB + s * B_TILE, user ? &tmWu : &tmB, &full[s], kb * kBK, n0);
         }
       }
     }
